@@ -1,0 +1,143 @@
+"""Pins for the oracle's RoPE, slot mapping and cache-write modes (CPU only)."""
+import numpy as np
+
+from oracle import cache, e4m3, quant, rope
+from quantized_paged_kv_varlen_gb300 import synth
+
+
+def test_rope_table_closed_form():
+    cos, sin = rope.cos_sin_table(50, 8, 1.0e4)
+    assert cos.dtype == np.float32 and cos.shape == (50, 4)
+    pos = np.arange(50, dtype=np.float64)
+    # i = 0 has inverse frequency 1; i = 2 (2i/D = 1/2) has theta^(-1/2) = 0.01
+    assert np.array_equal(cos[:, 0], np.cos(pos).astype(np.float32))
+    assert np.array_equal(sin[:, 0], np.sin(pos).astype(np.float32))
+    assert np.allclose(cos[:, 2], np.cos(pos * 0.01), atol=1e-7)
+    assert np.all(cos[0] == 1) and np.all(sin[0] == 0)
+
+
+def test_rope_identity_norm_and_direction():
+    rng = np.random.default_rng(0)
+    D = 16
+    cos, sin = rope.cos_sin_table(64, D, 1.0e4)
+    x = rng.standard_normal((64, 3, D)).astype(np.float32)
+    pos = np.arange(64)
+    y = rope.rotate(x, pos, cos, sin)
+    assert np.array_equal(y[0], x[0])                      # position 0: identity
+    pair_in = x[..., :D // 2].astype(np.float64) ** 2 + x[..., D // 2:].astype(np.float64) ** 2
+    pair_out = y[..., :D // 2].astype(np.float64) ** 2 + y[..., D // 2:].astype(np.float64) ** 2
+    assert np.allclose(pair_out, pair_in, rtol=2e-6, atol=1e-12)
+    # one pair (1, 0) at angle a goes to (cos a, sin a): counter-clockwise, pairs (i, i+D/2)
+    e = np.zeros((1, D), dtype=np.float32)
+    e[0, 0] = 1.0
+    r = rope.rotate(e, np.array([5]), cos, sin)
+    assert r[0, 0] == cos[5, 0] and r[0, D // 2] == sin[5, 0]
+
+
+def test_rope_dot_depends_only_on_relative_position():
+    rng = np.random.default_rng(1)
+    D = 32
+    cos, sin = rope.cos_sin_table(400, D, 1.0e4)
+    q = rng.standard_normal((1, D)).astype(np.float32)
+    k = rng.standard_normal((1, D)).astype(np.float32)
+    dots = []
+    for m, n in [(10, 3), (107, 100), (307, 300)]:
+        qm = rope.rotate(q, np.array([m]), cos, sin).astype(np.float64)
+        kn = rope.rotate(k, np.array([n]), cos, sin).astype(np.float64)
+        dots.append(float(qm[0] @ kn[0]))
+    assert np.allclose(dots, dots[0], rtol=1e-4, atol=1e-4)
+
+
+def test_rope_products_rounded_separately():
+    """x'_i = fl(fl(x_i c) - fl(x_j s)): differs from a fused evaluation."""
+    x = np.array([[1.0000001, 3.0000002]], dtype=np.float32)
+    c = np.array([[0.7]], dtype=np.float32)
+    s = np.array([[0.3000001]], dtype=np.float32)
+    y = rope.rotate(x, np.array([0]), c, s)
+    want0 = np.float32(np.float32(x[0, 0] * c[0, 0]) - np.float32(x[0, 1] * s[0, 0]))
+    want1 = np.float32(np.float32(x[0, 1] * c[0, 0]) + np.float32(x[0, 0] * s[0, 0]))
+    assert y[0, 0] == want0 and y[0, 1] == want1
+
+
+def _walk_slots(lengths, start_pos, bt, ps):
+    """Brute force: walk every request's tokens page by page."""
+    out = []
+    for b, L in enumerate(lengths):
+        page_idx, off = divmod(int(start_pos[b]), ps)
+        for _ in range(int(L)):
+            out.append(int(bt[b][page_idx]) * ps + off)
+            off += 1
+            if off == ps:
+                off = 0
+                page_idx += 1
+    return np.array(out, dtype=np.int32)
+
+
+def test_slot_mapping_matches_page_walk():
+    rng = np.random.default_rng(3)
+    lengths = np.array([5, 0, 33, 16, 1])
+    start = np.array([0, 7, 12, 16, 31])
+    total = [int(s + L) for s, L in zip(start, lengths)]
+    bt, _ = synth.page_tables(rng, total, 16)
+    cu = np.cumsum(lengths)
+    got = cache.slot_mapping(cu, start, bt, 16)
+    assert np.array_equal(got, _walk_slots(lengths, start, bt, 16))
+
+
+def test_fp8_write_bytes_and_untouched_slots():
+    wl = synth.tiny_decode(0)
+    k, v = wl.kv_all()
+    P, ps, H, D = wl.num_pages, 16, wl.Hkv, wl.D
+    fill = np.full((P, ps, H, D), 0x5A, dtype=np.uint8)
+    sfill = np.full((P, ps, H), -7.0, dtype=np.float32)
+    kp, vp, ks, vs, slots, _ = cache.write_fp8_token_head(
+        k, v, wl.cu_seqlens, np.zeros(2, np.int64), wl.block_table, ps,
+        fill, fill, sfill, sfill)
+    kc, kscale = quant.quant_fp8_last_axis(k)
+    flat = kp.reshape(P * ps, H, D)
+    assert np.array_equal(flat[slots], kc)
+    assert np.array_equal(ks.reshape(P * ps, H)[slots], kscale)
+    untouched = np.setdiff1d(np.arange(P * ps), slots)
+    assert np.all(flat[untouched] == 0x5A) and np.all(ks.reshape(-1, H)[untouched] == -7.0)
+    # each token's absmax element sits at +-448
+    deq = e4m3.decode(flat[slots]) * ks.reshape(P * ps, H)[slots][..., None]
+    assert np.allclose(np.abs(deq).max(-1), np.abs(k).max(-1), rtol=2 ** -4)
+
+
+def test_int8_block_scales_stay_inside_sequences():
+    """Blocks never straddle two sequences: a loud and a quiet sequence get
+    their own scales, and each block's absmax element is +-127."""
+    lengths = np.array([130, 70])
+    T, H, D = 200, 2, 8
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((T, H, D)).astype(np.float32)
+    x[:130] *= 100.0
+    cu = np.cumsum(lengths)
+    codes, scales = cache.block128_quant(x, cu, 2)
+    assert scales.shape == (2, 2, H)
+    assert np.all(scales[1, 1] == 0)                       # sequence 1 has one block
+    assert np.all(scales[0, 0] > 10 * scales[1, 0])
+    for (lo, hi, b, blk) in [(0, 128, 0, 0), (128, 130, 0, 1), (130, 200, 1, 0)]:
+        amax = np.abs(x[lo:hi]).max(axis=(0, 2))
+        assert np.array_equal(scales[b, blk], (amax / np.float32(127)).astype(np.float32))
+        assert np.all(np.abs(codes[lo:hi]).max(axis=(0, 2)) == 127)
+
+
+def test_mla_row_layout_roundtrip():
+    rng = np.random.default_rng(5)
+    kv = synth.bf16_normal(rng, (9, 576))
+    kv[3, :128] = 0.0                                       # a zero tile
+    rows = cache.mla_pack_rows(kv)
+    assert rows.shape == (9, 656)
+    # rope part: bytes 512..640 are the bf16 bits, little-endian
+    rope_bits = rows[:, 512:640].copy().view("<u2")
+    assert np.array_equal(cache.bf16_value(rope_bits), kv[:, 512:].astype(np.float64))
+    scales = rows[:, 640:].copy().view("<f4")
+    amax = np.abs(kv[:, :512].reshape(9, 4, 128)).max(-1)
+    assert np.array_equal(scales, (amax / np.float32(127)).astype(np.float32))
+    assert scales[3, 0] == 0 and np.all(rows[3, :128] == 0)
+    K, V = cache.mla_unpack_rows(rows)
+    assert np.array_equal(K[:, 512:], kv[:, 512:].astype(np.float64))
+    err = np.abs(V - kv[:, :512]).reshape(9, 4, 128)
+    assert np.all(err <= scales[..., None].astype(np.float64) * 0.5 * (1 + 1e-5))
+    assert np.array_equal(K[:, :512], V)
