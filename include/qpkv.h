@@ -1,0 +1,233 @@
+/*
+ * qpkv: quantized paged-KV varlen attention for NVIDIA GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels.  Every pointer argument named
+ * "device" is a raw device pointer the caller allocated and owns; "host"
+ * pointers are ordinary host memory.  The library never allocates, frees or
+ * synchronises: each call enqueues work on the caller's CUDA stream (passed
+ * as `void*`, i.e. a cudaStream_t; NULL is the legacy default stream) and
+ * returns.  No C++ exception crosses this boundary; every call returns a
+ * qpkv_status.  Argument checks that need no device memory run on the host
+ * before anything is launched; contents of device arrays (page ids, sparse
+ * indices) are checked by the kernels, which skip a bad entry and set a bit
+ * in the caller's device `error_word` (int32, may be NULL).
+ *
+ * Strides are in elements.  All layouts are row-major and contiguous unless
+ * a stride argument says otherwise.  Names follow the source pages:
+ *  - "KvQuantSparseFlashAttention" README (ops-transformer): the formula
+ *    softmax(Q . Dequant(K)^T / sqrt(d_k)) . Dequant(V) (计算公式), the
+ *    PA_BSND page layout [block_num, block_size, KV_N, KV_D], block_table,
+ *    actual_seq_lengths_query / _kv, sparse_indices, sparse_mode 0 / 3,
+ *    scale_value, the MLA-absorb combined row (参数说明 table);
+ *  - "[Refactor] Unify JIT/Customization/AOT mode" (flashinfer): the decode
+ *    plan / run split with float / int / page-locked workspaces, maybe_lse,
+ *    the cuda_stream argument ("Batch Decode/Prefill Attention Kernels");
+ *  - "[Feature] Sage Attention Support Varlen & write kv cache BF16/FP16"
+ *    (PaddleNLP): RoPE fused into the cache write, varlen grids that exit
+ *    past each sequence's end, varlen INT8 quantisation of Q/K (Description);
+ *  - "[Triton] FP8 with FA v3 API" (ROCm aiter): FP8 q/k/v with
+ *    q_descale / k_descale / v_descale, softmax_scale, causal.
+ */
+#ifndef QPKV_H_
+#define QPKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+typedef int32_t qpkv_status;
+#define QPKV_OK 0
+#define QPKV_ERR_INVALID_ARG 1         /* null pointer, bad size, misaligned pointer */
+#define QPKV_ERR_UNSUPPORTED 2         /* head_dim, page_size, head ratio, dtype, mode */
+#define QPKV_ERR_WORKSPACE_TOO_SMALL 3 /* a caller workspace is smaller than required */
+#define QPKV_ERR_CUDA 4                /* a CUDA runtime/driver call or launch failed */
+#define QPKV_ERR_DEVICE 5              /* reserved: device error word reported by a caller */
+#define QPKV_ERR_TIMEOUT 6             /* reserved: device wait timeout reported by a caller */
+
+/* bits a kernel ORs into the device error word */
+#define QPKV_DEV_ERR_TIMEOUT 1   /* an internal pipeline wait gave up after ~2 s */
+#define QPKV_DEV_ERR_BAD_PAGE 2  /* a block_table entry outside [0, num_pages) was skipped */
+#define QPKV_DEV_ERR_BAD_INDEX 4 /* a sparse index outside [0, L_kv) was skipped */
+
+/* Text of a status code (static storage, never NULL). */
+const char* qpkv_status_string(qpkv_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t qpkv_version(void);
+
+/* sizeof of the parameter structs below, so that bindings in other
+ * languages can check their mirror of the layout:
+ * which = 0 -> qpkv_write_params.  Unknown `which` returns 0. */
+size_t qpkv_struct_size(int32_t which);
+
+/* -------------------------------------------------------------- RoPE table
+ * cos/sin tables for the rotate-half RoPE of the cache write ("[Feature]
+ * Sage Attention ... write kv cache BF16/FP16", Description item 1; the
+ * rope_theta / rope_scale parameters of flashinfer's interfaces):
+ *   inv_freq_i = theta^(-2i/rot_dim), angle = (pos / rope_scale) * inv_freq_i,
+ * evaluated in double precision on the device and rounded to float.
+ * cos_out, sin_out: device float [max_pos, rot_dim/2] (caller-allocated).
+ * Errors: INVALID_ARG for null outputs, max_pos < 1, odd or non-positive
+ * rot_dim, theta <= 0 or rope_scale <= 0; CUDA on launch failure. */
+qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int32_t rot_dim,
+                            float* cos_out, float* sin_out, void* stream);
+
+/* -------------------------------------------------------------- cache write
+ * RoPE + quantise + page-append of new tokens ("[Feature] Sage Attention
+ * ... write kv cache BF16/FP16", Description items 1-2; README 参数说明 rows
+ * key / block_table / actual_seq_lengths_query).  New token t of sequence b
+ * has position p = start_pos[b] + (t - begin_b) and goes to pool row
+ * ("slot") block_table[b * bt_stride + p / page_size] * page_size + p % page_size.
+ *
+ * Modes:
+ *  QPKV_WRITE_FP8_TOKEN_HEAD  k, v bf16 [T, Hkv, D] -> E4M3 pools
+ *     [P, page_size, Hkv, D] + float scale pools [P, page_size, Hkv];
+ *     scale = absmax_D / 448, code = RNE_satfinite(x / scale) (IEEE fp32
+ *     division), absmax 0 -> scale 0 and zero codes.  D in {64, 128}.
+ *  QPKV_WRITE_INT8_BLOCK128_ROPE  q, k, v bf16 [T, H, D]: RoPE (rotate-half,
+ *     pairs (i, i + D/2), tables from qpkv_rope_table) on q and k, then one
+ *     scale per (sequence, 128-token block, head): scale = absmax / 127,
+ *     code = clamp(RNE(x / scale), -127, 127).  K codes go to the int8
+ *     k_pool, V is copied unchanged into the bf16 v_pool, Q codes go to
+ *     q_out (int8 [T, Hq, D], TND), scales to k_block_scale [B, num_blocks,
+ *     Hkv] and q_block_scale [B, num_blocks, Hq].  Whole sequences only
+ *     (start_pos must be NULL: every sequence starts at position 0).  D = 128.
+ *  QPKV_WRITE_MLA_ROW  k = kv bf16 [T, 576] (512 nope || 64 rope), Hkv = 1:
+ *     each token becomes one 656-byte row of the pool [P, page_size, 1, 656]:
+ *     bytes [0, 512) INT8 nope codes (tile i = dims 128i..128i+127 has scale
+ *     absmax/127), [512, 640) the bf16 rope values, [640, 656) the 4 fp32
+ *     tile scales, little-endian ("512+64*2+4*4", README row key).
+ *
+ * Device arrays: cu_seqlens_q int32 [B] inclusive prefix sums (batch b spans
+ * [cu[b-1], cu[b]), cu[-1] = 0); start_pos int32 [B] or NULL (all zero);
+ * block_table int32 [B, bt_stride]; slot_mapping int32 [T] out or NULL.
+ * Every pointer must be 16-byte aligned.  Pool rows of tokens not written
+ * are left untouched.
+ * Errors: INVALID_ARG (null required pointer, non-positive sizes, misaligned
+ * pointer, start_pos given in INT8 mode), UNSUPPORTED (mode, D, page_size
+ * not a multiple of 16, Hq % Hkv != 0), CUDA.  Page ids outside
+ * [0, num_pages) are skipped with QPKV_DEV_ERR_BAD_PAGE. */
+#define QPKV_WRITE_FP8_TOKEN_HEAD 0
+#define QPKV_WRITE_INT8_BLOCK128_ROPE 1
+#define QPKV_WRITE_MLA_ROW 2
+
+typedef struct qpkv_write_params {
+  int32_t mode;
+  int32_t num_seqs;       /* B */
+  int32_t num_tokens;     /* T, number of new tokens */
+  int32_t max_seqlen;     /* host upper bound of any sequence's new-token count */
+  int32_t num_heads_q;    /* Hq (INT8 mode), else ignored */
+  int32_t num_heads_kv;   /* Hkv (1 for MLA) */
+  int32_t head_dim;       /* D (576 for MLA: input width) */
+  int32_t page_size;
+  int32_t num_pages;      /* P, pool size, for page-id checks */
+  int32_t bt_stride;      /* row stride of block_table */
+  int32_t num_blocks;     /* INT8 mode: dim 1 of the block-scale arrays */
+  int32_t rope_max_pos;   /* rows of the RoPE tables (INT8 mode) */
+  const int32_t* cu_seqlens_q;
+  const int32_t* start_pos;
+  const int32_t* block_table;
+  const void* q;          /* bf16 [T, Hq, D] (INT8 mode) */
+  const void* k;          /* bf16 [T, Hkv, D] ([T, 576] for MLA) */
+  const void* v;          /* bf16 [T, Hkv, D] (not used for MLA) */
+  const float* rope_cos;  /* [rope_max_pos, D/2] (INT8 mode) */
+  const float* rope_sin;
+  void* k_pool;           /* u8 E4M3 / int8 / MLA rows */
+  void* v_pool;           /* u8 E4M3 (FP8 mode) / bf16 (INT8 mode) */
+  float* k_scale_pool;    /* FP8 mode [P, page_size, Hkv] */
+  float* v_scale_pool;
+  float* k_block_scale;   /* INT8 mode [B, num_blocks, Hkv] */
+  void* q_out;            /* INT8 mode: int8 [T, Hq, D] */
+  float* q_block_scale;   /* INT8 mode [B, num_blocks, Hq] */
+  int32_t* slot_mapping;  /* [T] or NULL */
+  int32_t* error_word;    /* device int32 or NULL */
+} qpkv_write_params;
+
+qpkv_status qpkv_write_cache(const qpkv_write_params* params, void* stream);
+
+/* ----------------------------------------------------------- decode: plan
+ * Paged FP8 decode, one query token per request (flashinfer "Batch Decode
+ * Attention Kernels": BatchDecodeWithPagedKVCachePlan / ...Run; aiter's
+ * flash_attn_with_kvcache with page_table and cache_seqlens).
+ *
+ * qpkv_decode_plan splits every (request, kv head) into work items of at
+ * most `chunk` (128 or 256) tokens so that the items fill the GPU, writes
+ * the work list into the caller's page-locked host buffer and copies it
+ * (one cudaMemcpyAsync on `stream`) into the caller's device int workspace.
+ * seqlens_kv_host: host int32 [B], tokens in each request's cache (>= 0).
+ * num_sms: SM count of the device (used to pick the chunk).
+ * plan_info: host int64 [QPKV_PLAN_INFO_LEN] out, passed to qpkv_decode_run.
+ * Required sizes come from qpkv_decode_workspace_sizes.  The pinned buffer
+ * must stay untouched until the copy has run (stream order).
+ * Errors: INVALID_ARG (null pointers, B < 1, negative length, Hq % Hkv),
+ * UNSUPPORTED (head_dim not in {64, 128}, Hq/Hkv not in {1, 2, 4, 8},
+ * page_size not a multiple of 16 dividing 256 or a multiple of 256),
+ * WORKSPACE_TOO_SMALL, CUDA. */
+#define QPKV_PLAN_INFO_LEN 16
+
+qpkv_status qpkv_decode_workspace_sizes(const int32_t* seqlens_kv_host, int32_t batch_size,
+                                        int32_t num_qo_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t num_sms, size_t* int_ws_bytes,
+                                        size_t* float_ws_bytes);
+
+/* Host-only part of the plan (no CUDA call): fills host_int_ws and plan_info.
+ * qpkv_decode_plan = this + the async copy to the device int workspace. */
+qpkv_status qpkv_decode_plan_host(const int32_t* seqlens_kv_host, int32_t batch_size,
+                                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t page_size,
+                                  int32_t head_dim, int32_t num_sms, void* host_int_ws,
+                                  size_t host_int_bytes, int64_t* plan_info);
+
+qpkv_status qpkv_decode_plan(const int32_t* seqlens_kv_host, int32_t batch_size,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t page_size,
+                             int32_t head_dim, int32_t num_sms, void* pinned_int_ws,
+                             size_t pinned_bytes, void* int_ws, size_t int_ws_bytes,
+                             int64_t* plan_info, void* stream);
+
+/* ------------------------------------------------------------ decode: run
+ * O[b, h, :] = softmax(sm_scale * q[b, h] . Dequant(K_b)^T) . Dequant(V_b)
+ * over the L_b cached tokens of request b, kv head h / (Hq / Hkv), with
+ * Dequant(x)[t] = e4m3(x[t]) * scale_pool[t] (README 计算公式; per-token-head
+ * FP8).  q: device bf16 [B, Hq, D]; k_pool / v_pool: device u8
+ * [num_pages, page_size, Hkv, D]; k_scale_pool / v_scale_pool: device float
+ * [num_pages, page_size, Hkv]; block_table: device int32 [B, bt_stride];
+ * o: device bf16 [B, Hq, D]; lse: device float [B, Hq] (natural log of the
+ * softmax denominator of the scaled logits) or NULL.
+ * float_ws / int_ws: the workspaces given to qpkv_decode_plan (device).
+ * A request with L_b = 0 gets O = 0 and lse = -inf.
+ * qpkv_decode_run = qpkv_decode_attend (split-KV partials) followed by
+ * qpkv_decode_merge (log-sum-exp merge), both on `stream`.
+ * block_table rows must hold at least ceil(max_b L_b / page_size) entries.
+ * Errors: INVALID_ARG (null / misaligned pointers, plan_info not from
+ * qpkv_decode_plan, bt_stride too small for the longest request),
+ * WORKSPACE_TOO_SMALL, CUDA. */
+qpkv_status qpkv_decode_run(const int64_t* plan_info, void* float_ws, size_t float_ws_bytes,
+                            const void* int_ws, const void* q, const void* k_pool,
+                            const void* v_pool, const float* k_scale_pool,
+                            const float* v_scale_pool, int32_t num_pages, int32_t page_size,
+                            const int32_t* block_table, int32_t bt_stride, float sm_scale,
+                            void* o, float* lse, int32_t* error_word, void* stream);
+
+/* Split-KV step alone: writes per-split partial O (float) and lse into
+ * float_ws.  Same arguments as qpkv_decode_run without o / lse. */
+qpkv_status qpkv_decode_attend(const int64_t* plan_info, void* float_ws, size_t float_ws_bytes,
+                               const void* int_ws, const void* q, const void* k_pool,
+                               const void* v_pool, const float* k_scale_pool,
+                               const float* v_scale_pool, int32_t num_pages, int32_t page_size,
+                               const int32_t* block_table, int32_t bt_stride, float sm_scale,
+                               int32_t* error_word, void* stream);
+
+/* Merge step alone: O = sum_s exp(lse_s - M) O_s / sum_s exp(lse_s - M),
+ * lse = M + ln sum_s exp(lse_s - M), M = max_s lse_s, per (request, head). */
+qpkv_status qpkv_decode_merge(const int64_t* plan_info, const void* float_ws,
+                              size_t float_ws_bytes, const void* int_ws, void* o, float* lse,
+                              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QPKV_H_ */

@@ -1,0 +1,342 @@
+"""Python binding of the qpkv C-ABI library (quantized paged-KV varlen
+attention on GB300).
+
+Argument marshalling only: tensors are checked for dtype / shape /
+contiguity, their device pointers and the current CUDA stream are passed to
+``libqpkv.so``, and every step of the computation runs in the library's
+CUDA kernels.  PyTorch supplies device memory (including the workspaces the
+library asks for) and streams.  There is no CPU or PyTorch fallback: a
+missing library raises.
+
+The submodule ``synth`` (seeded synthetic inputs) is importable without the
+library.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "QpkvError", "load", "rope_table", "write_cache_fp8", "write_cache_int8_block128_rope",
+    "write_cache_mla", "DecodePlan", "PAGE_ROW_MLA",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqpkv.so")
+PAGE_ROW_MLA = 656
+
+WRITE_FP8_TOKEN_HEAD = 0
+WRITE_INT8_BLOCK128_ROPE = 1
+WRITE_MLA_ROW = 2
+PLAN_INFO_LEN = 16
+
+DEV_ERR_TIMEOUT = 1
+DEV_ERR_BAD_PAGE = 2
+DEV_ERR_BAD_INDEX = 4
+
+_lib = None
+
+
+class QpkvError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: qpkv status {status} ({_status_text(status)})")
+
+
+def _status_text(status):
+    if _lib is None:
+        return "?"
+    return _lib.qpkv_status_string(status).decode()
+
+
+_i32 = ctypes.c_int32
+_p = ctypes.c_void_p
+
+
+class WriteParams(ctypes.Structure):
+    """Mirror of ``qpkv_write_params`` (include/qpkv.h)."""
+    _fields_ = [(n, _i32) for n in (
+        "mode", "num_seqs", "num_tokens", "max_seqlen", "num_heads_q", "num_heads_kv",
+        "head_dim", "page_size", "num_pages", "bt_stride", "num_blocks", "rope_max_pos")] + [
+        (n, _p) for n in (
+            "cu_seqlens_q", "start_pos", "block_table", "q", "k", "v", "rope_cos", "rope_sin",
+            "k_pool", "v_pool", "k_scale_pool", "v_scale_pool", "k_block_scale", "q_out",
+            "q_block_scale", "slot_mapping", "error_word")]
+
+
+def _declare(lib):
+    S = ctypes.c_size_t
+    P64 = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "qpkv_status_string": (ctypes.c_char_p, [_i32]),
+        "qpkv_version": (_i32, []),
+        "qpkv_struct_size": (S, [_i32]),
+        "qpkv_rope_table": (_i32, [ctypes.c_float, ctypes.c_float, _i32, _i32, _p, _p, _p]),
+        "qpkv_write_cache": (_i32, [ctypes.POINTER(WriteParams), _p]),
+        "qpkv_decode_workspace_sizes": (_i32, [_p, _i32, _i32, _i32, _i32, _i32,
+                                               ctypes.POINTER(S), ctypes.POINTER(S)]),
+        "qpkv_decode_plan_host": (_i32, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, S, P64]),
+        "qpkv_decode_plan": (_i32, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, S, _p, S,
+                                    P64, _p]),
+        "qpkv_decode_run": (_i32, [P64, _p, S, _p, _p, _p, _p, _p, _p, _i32, _i32, _p, _i32,
+                                   ctypes.c_float, _p, _p, _p, _p]),
+        "qpkv_decode_attend": (_i32, [P64, _p, S, _p, _p, _p, _p, _p, _p, _i32, _i32, _p,
+                                      _i32, ctypes.c_float, _p, _p]),
+        "qpkv_decode_merge": (_i32, [P64, _p, S, _p, _p, _p, _p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+
+
+def load(path: str = LIB_PATH):
+    """Load libqpkv.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"qpkv CUDA library not built: {path} is missing "
+                              "(run quantized_paged_kv_varlen_gb300.build.build())")
+        lib = ctypes.CDLL(path)
+        _declare(lib)
+        _lib = lib
+    return _lib
+
+
+def _check(status, where):
+    if status != 0:
+        raise QpkvError(status, where)
+
+
+# ------------------------------------------------------------------ helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, name, dtype=None, ndim=None, device=True):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must live on the GPU")
+    return t
+
+
+def rope_table(theta, max_pos, rot_dim, rope_scale=1.0, device="cuda"):
+    """(cos, sin) float32 [max_pos, rot_dim // 2] computed by the library."""
+    torch = _torch()
+    lib = load()
+    cos = torch.empty(max_pos, rot_dim // 2, dtype=torch.float32, device=device)
+    sin = torch.empty_like(cos)
+    _check(lib.qpkv_rope_table(float(theta), float(rope_scale), int(max_pos), int(rot_dim),
+                               _ptr(cos), _ptr(sin), _stream()), "qpkv_rope_table")
+    return cos, sin
+
+
+def _base_params(mode, cu_seqlens, block_table, page_size, num_pages, num_tokens, max_seqlen):
+    torch = _torch()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    p = WriteParams()
+    p.mode = mode
+    p.num_seqs = cu_seqlens.shape[0]
+    p.num_tokens = num_tokens
+    p.max_seqlen = max_seqlen
+    p.page_size = page_size
+    p.num_pages = num_pages
+    p.bt_stride = block_table.shape[1]
+    p.cu_seqlens_q = _ptr(cu_seqlens)
+    p.block_table = _ptr(block_table)
+    return p
+
+
+def write_cache_fp8(k, v, cu_seqlens, block_table, k_pool, v_pool, k_scale_pool, v_scale_pool,
+                    start_pos=None, slot_mapping=None, error_word=None):
+    """FP8 per-(token, head) cache write.  k, v: bf16 [T, Hkv, D]; pools u8
+    [P, page_size, Hkv, D]; scale pools float32 [P, page_size, Hkv]."""
+    torch = _torch()
+    lib = load()
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.uint8, 4)
+    _need(v_pool, "v_pool", torch.uint8, 4)
+    _need(k_scale_pool, "k_scale_pool", torch.float32, 3)
+    _need(v_scale_pool, "v_scale_pool", torch.float32, 3)
+    P, ps, H, D = k_pool.shape
+    p = _base_params(WRITE_FP8_TOKEN_HEAD, cu_seqlens, block_table, ps, P, k.shape[0], 0)
+    p.num_heads_kv = H
+    p.head_dim = D
+    p.k, p.v = _ptr(k), _ptr(v)
+    p.k_pool, p.v_pool = _ptr(k_pool), _ptr(v_pool)
+    p.k_scale_pool, p.v_scale_pool = _ptr(k_scale_pool), _ptr(v_scale_pool)
+    p.start_pos = _ptr(start_pos)
+    p.slot_mapping = _ptr(slot_mapping)
+    p.error_word = _ptr(error_word)
+    _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(fp8)")
+
+
+def write_cache_int8_block128_rope(q, k, v, cu_seqlens, block_table, max_seqlen, rope_cos,
+                                   rope_sin, k_pool, v_pool, k_block_scale, q_out,
+                                   q_block_scale, slot_mapping=None, error_word=None):
+    """Sage-style prefill write: RoPE(q, k), INT8 per-(sequence, 128-token
+    block, head) Q and K, bf16 V into pages.  q/k/v bf16 [T, H, 128];
+    k_pool int8 [P, ps, Hkv, 128]; v_pool bf16 [P, ps, Hkv, 128];
+    k_block_scale [B, nb, Hkv]; q_out int8 [T, Hq, 128]; q_block_scale [B, nb, Hq]."""
+    torch = _torch()
+    lib = load()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.int8, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(q_out, "q_out", torch.int8, 3)
+    _need(k_block_scale, "k_block_scale", torch.float32, 3)
+    _need(q_block_scale, "q_block_scale", torch.float32, 3)
+    _need(rope_cos, "rope_cos", torch.float32, 2)
+    _need(rope_sin, "rope_sin", torch.float32, 2)
+    P, ps, Hkv, D = k_pool.shape
+    p = _base_params(WRITE_INT8_BLOCK128_ROPE, cu_seqlens, block_table, ps, P, k.shape[0],
+                     int(max_seqlen))
+    p.num_heads_q = q.shape[1]
+    p.num_heads_kv = Hkv
+    p.head_dim = D
+    p.num_blocks = k_block_scale.shape[1]
+    p.rope_max_pos = rope_cos.shape[0]
+    p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
+    p.rope_cos, p.rope_sin = _ptr(rope_cos), _ptr(rope_sin)
+    p.k_pool, p.v_pool = _ptr(k_pool), _ptr(v_pool)
+    p.k_block_scale, p.q_out, p.q_block_scale = _ptr(k_block_scale), _ptr(q_out), _ptr(q_block_scale)
+    p.slot_mapping = _ptr(slot_mapping)
+    p.error_word = _ptr(error_word)
+    _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(int8)")
+
+
+def write_cache_mla(kv, cu_seqlens, block_table, pool, start_pos=None, slot_mapping=None,
+                    error_word=None):
+    """MLA combined-row write: kv bf16 [T, 576] -> pool u8 [P, bs, 1, 656]."""
+    torch = _torch()
+    lib = load()
+    _need(kv, "kv", torch.bfloat16, 2)
+    _need(pool, "pool", torch.uint8, 4)
+    P, bs, one, W = pool.shape
+    if one != 1 or W != PAGE_ROW_MLA or kv.shape[1] != 576:
+        raise ValueError("MLA pool must be [P, bs, 1, 656] and kv [T, 576]")
+    p = _base_params(WRITE_MLA_ROW, cu_seqlens, block_table, bs, P, kv.shape[0], 0)
+    p.num_heads_kv = 1
+    p.head_dim = 576
+    p.k = _ptr(kv)
+    p.k_pool = _ptr(pool)
+    p.start_pos = _ptr(start_pos)
+    p.slot_mapping = _ptr(slot_mapping)
+    p.error_word = _ptr(error_word)
+    _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(mla)")
+
+
+class DecodePlan:
+    """Plan/run split for paged FP8 decode (one query token per request).
+
+    ``DecodePlan(seqlens_kv, Hq, Hkv, page_size, head_dim)`` sizes and
+    allocates the workspaces (torch device memory plus a page-locked host
+    buffer) and runs the library's host planner, which copies the work list
+    to the device on the current stream.  ``run`` launches the split-KV
+    kernel and the log-sum-exp merge.
+    """
+
+    def __init__(self, seqlens_kv, num_qo_heads, num_kv_heads, page_size, head_dim,
+                 device="cuda", num_sms=None):
+        torch = _torch()
+        import numpy as np
+        lib = load()
+        lens = np.ascontiguousarray(np.asarray(seqlens_kv, dtype=np.int32))
+        self.lens = lens
+        self.B = int(lens.shape[0])
+        self.Hq, self.Hkv, self.D, self.page_size = num_qo_heads, num_kv_heads, head_dim, page_size
+        if num_sms is None:
+            num_sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.num_sms = int(num_sms)
+        ib, fb = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib.qpkv_decode_workspace_sizes(lens.ctypes.data, self.B, self.Hq, self.Hkv,
+                                               self.D, self.num_sms, ctypes.byref(ib),
+                                               ctypes.byref(fb)), "qpkv_decode_workspace_sizes")
+        self.int_bytes, self.float_bytes = ib.value, fb.value
+        self.int_ws = torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, device=device)
+        self.float_ws = torch.empty(max(self.float_bytes, 256), dtype=torch.uint8, device=device)
+        self.pinned = torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, pin_memory=True)
+        self.plan_info = (ctypes.c_int64 * PLAN_INFO_LEN)()
+        _check(lib.qpkv_decode_plan(lens.ctypes.data, self.B, self.Hq, self.Hkv, page_size,
+                                    self.D, self.num_sms, ctypes.c_void_p(self.pinned.data_ptr()),
+                                    self.pinned.numel(), _ptr(self.int_ws), self.int_ws.numel(),
+                                    self.plan_info, _stream()), "qpkv_decode_plan")
+
+    @property
+    def num_items(self):
+        return int(self.plan_info[0])
+
+    @property
+    def chunk(self):
+        return int(self.plan_info[1])
+
+    @property
+    def total_splits(self):
+        return int(self.plan_info[2])
+
+    def _check_run(self, q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table):
+        torch = _torch()
+        _need(q, "q", torch.bfloat16, 3)
+        _need(k_pool, "k_pool", torch.uint8, 4)
+        _need(v_pool, "v_pool", torch.uint8, 4)
+        _need(k_scale_pool, "k_scale_pool", torch.float32, 3)
+        _need(v_scale_pool, "v_scale_pool", torch.float32, 3)
+        _need(block_table, "block_table", torch.int32, 2)
+        if tuple(q.shape) != (self.B, self.Hq, self.D):
+            raise ValueError(f"q must be [{self.B}, {self.Hq}, {self.D}]")
+        if k_pool.shape[1] != self.page_size or k_pool.shape[2] != self.Hkv:
+            raise ValueError("pool shape does not match the plan")
+
+    def run(self, q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table, sm_scale,
+            out=None, lse=None, error_word=None):
+        torch = _torch()
+        lib = load()
+        self._check_run(q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table)
+        if out is None:
+            out = torch.empty_like(q)
+        _check(lib.qpkv_decode_run(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
+                                   _ptr(self.int_ws), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                   _ptr(k_scale_pool), _ptr(v_scale_pool), k_pool.shape[0],
+                                   self.page_size, _ptr(block_table), block_table.shape[1],
+                                   float(sm_scale), _ptr(out), _ptr(lse), _ptr(error_word),
+                                   _stream()), "qpkv_decode_run")
+        return out
+
+    def attend(self, q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table, sm_scale,
+               error_word=None):
+        lib = load()
+        self._check_run(q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table)
+        _check(lib.qpkv_decode_attend(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
+                                      _ptr(self.int_ws), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                      _ptr(k_scale_pool), _ptr(v_scale_pool), k_pool.shape[0],
+                                      self.page_size, _ptr(block_table), block_table.shape[1],
+                                      float(sm_scale), _ptr(error_word), _stream()),
+               "qpkv_decode_attend")
+
+    def merge(self, out, lse=None):
+        lib = load()
+        _check(lib.qpkv_decode_merge(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
+                                     _ptr(self.int_ws), _ptr(out), _ptr(lse), _stream()),
+               "qpkv_decode_merge")
+        return out

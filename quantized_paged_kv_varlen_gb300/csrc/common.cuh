@@ -1,0 +1,71 @@
+// Device helpers shared by the qpkv kernels: bf16 / E4M3 conversions with
+// explicit rounding, warp reductions, varlen bookkeeping.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace qpkv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Two float32 -> two E4M3 codes (round to nearest even, saturate to +-448);
+// `hi` lands in the upper byte of the 16-bit result.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  return static_cast<uint8_t>(f32x2_to_e4m3x2(0.f, x) & 0xFF);
+}
+
+// Two E4M3 codes (low byte = element 0) -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
+  return e4m3x2_to_f32x2(static_cast<uint16_t>(code)).x;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sequence index of a token given inclusive prefix sums cu[0..B): the
+// smallest b with t < cu[b].
+__device__ __forceinline__ int seq_of_token(const int32_t* __restrict__ cu, int B, int t) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (t < __ldg(cu + mid)) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int seq_begin(const int32_t* __restrict__ cu, int b) {
+  return b == 0 ? 0 : __ldg(cu + b - 1);
+}
+
+}  // namespace qpkv

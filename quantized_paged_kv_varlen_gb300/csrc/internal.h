@@ -1,0 +1,57 @@
+// Host-side declarations shared between the C-ABI layer (api.cpp) and the
+// kernel launchers (*.cu).  Not part of the public interface.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/qpkv.h"
+
+namespace qpkv {
+
+// Work item of the split-KV decode: request, kv head, token range [t0, t1).
+struct DecodeItem {
+  int32_t b, hk, t0, t1;
+};
+
+// Layout of the decode plan (int workspace) and the float workspace.
+struct DecodePlan {
+  int64_t num_items;
+  int64_t chunk;
+  int64_t total_splits;
+  int64_t items_offset;      // bytes into the int workspace
+  int64_t split_off_offset;  // bytes into the int workspace: int32 [B + 1]
+  int64_t int_bytes;
+  int64_t float_bytes;
+  int64_t batch;
+  int64_t num_qo_heads;
+  int64_t num_kv_heads;
+  int64_t head_dim;
+  int64_t page_size;
+  int64_t max_len;   // longest request; block_table rows must cover it
+  int64_t magic;
+};
+constexpr int64_t kPlanMagic = 0x71706b76706c616eLL;  // "qpkvplan"
+
+cudaError_t launch_rope_table(float theta, float rope_scale, int max_pos, int rot_dim,
+                              float* cos_out, float* sin_out, cudaStream_t stream);
+
+cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream);
+
+cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, const void* int_ws,
+                                 const void* q, const void* k_pool, const void* v_pool,
+                                 const float* k_scale_pool, const float* v_scale_pool,
+                                 int num_pages, int page_size, const int32_t* block_table,
+                                 int bt_stride, float sm_scale, int32_t* error_word,
+                                 cudaStream_t stream, int* status);
+
+cudaError_t launch_decode_merge(const DecodePlan& plan, const float* float_ws, const void* int_ws,
+                                void* o, float* lse, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
+                           void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                           const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+}  // namespace qpkv

@@ -1,0 +1,341 @@
+// Cache write: (RoPE +) quantise + page-append of new tokens.
+//
+// "[Feature] Sage Attention Support Varlen & write kv cache BF16/FP16",
+// Description item 1 (RoPE fused into the KV-cache write) and item 2 (varlen
+// quantisation: a quantisation block never crosses a sequence boundary);
+// "KvQuantSparseFlashAttention" README, 参数说明 rows key / block_table
+// (PA_BSND pages) and the Per-Token-Head(-Tile-128) quantisation named under
+// 功能说明.  Memory-bound elementwise work with small reductions: plain SIMT
+// with 16-byte vector accesses, no tensor cores.
+//
+// Rounding is explicit so the bytes are reproducible: IEEE float32 division
+// (__fdiv_rn), nearest-even conversions, RoPE products and sums rounded
+// separately (__fmul_rn / __fadd_rn / __fsub_rn, no contraction).
+#include "common.cuh"
+#include "internal.h"
+
+namespace qpkv {
+namespace {
+
+__device__ __forceinline__ int pool_page(const int32_t* __restrict__ bt, int bt_stride, int b,
+                                         int p, int ps, int num_pages, int* err) {
+  const int page = __ldg(bt + static_cast<size_t>(b) * bt_stride + p / ps);
+  if (page < 0 || page >= num_pages) {
+    report_error(err, kDevErrBadPage);
+    return -1;
+  }
+  return page;
+}
+
+// ---------------------------------------------- FP8 per-(token, head) mode
+// One warp per (token, kv head); lane l owns D/32 consecutive elements.
+template <int D>
+__global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
+    int T, int B, int H, int ps, int num_pages, int bt_stride, const int32_t* __restrict__ cu,
+    const int32_t* __restrict__ start_pos, const int32_t* __restrict__ bt,
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, uint8_t* __restrict__ k_pool,
+    uint8_t* __restrict__ v_pool, float* __restrict__ k_scale, float* __restrict__ v_scale,
+    int32_t* __restrict__ slots, int* err) {
+  constexpr int EPL = D / 32;  // 2 or 4 elements per lane
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= T * H) return;
+  const int t = w / H, h = w - (w / H) * H;
+  const int b = seq_of_token(cu, B, t);
+  const int p = (start_pos ? __ldg(start_pos + b) : 0) + (t - seq_begin(cu, b));
+  const int page = pool_page(bt, bt_stride, b, p, ps, num_pages, lane == 0 ? err : nullptr);
+  if (page < 0) return;
+  const size_t slot = static_cast<size_t>(page) * ps + (p % ps);
+  if (slots != nullptr && h == 0 && lane == 0) slots[t] = static_cast<int32_t>(slot);
+
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint16_t* src = (which ? v : k) + (static_cast<size_t>(t) * H + h) * D + lane * EPL;
+    float x[EPL];
+    if constexpr (EPL == 4) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(src);
+      x[0] = bf16_bits_to_float(raw.x & 0xFFFF);
+      x[1] = bf16_bits_to_float(raw.x >> 16);
+      x[2] = bf16_bits_to_float(raw.y & 0xFFFF);
+      x[3] = bf16_bits_to_float(raw.y >> 16);
+    } else {
+      const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+      x[0] = bf16_bits_to_float(raw & 0xFFFF);
+      x[1] = bf16_bits_to_float(raw >> 16);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = warp_max(amax);
+    const float scale = __fdiv_rn(amax, 448.0f);
+    uint32_t packed = 0;
+    if (scale != 0.f) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        packed |= static_cast<uint32_t>(f32_to_e4m3(__fdiv_rn(x[i], scale))) << (8 * i);
+    }
+    uint8_t* dst = (which ? v_pool : k_pool) + (slot * H + h) * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    }
+    if (lane == 0) (which ? v_scale : k_scale)[slot * H + h] = scale;
+  }
+}
+
+// ------------------------------- INT8 per-(sequence, 128-token block, head)
+// One CTA (256 threads) per (block, head, sequence).  Thread tid owns token
+// r = tid / 2 of the block and RoPE pairs i in [32*(tid%2), 32*(tid%2)+32),
+// i.e. elements i and i + 64 of the 128-wide head.
+constexpr int kBlk = 128;
+
+__device__ __forceinline__ void load_bf16x8(const uint16_t* src, float (&x)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFF);
+    x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+  }
+}
+
+__device__ __forceinline__ float block_max_256(float v, float* red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  float m = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
+  __syncthreads();
+  return m;
+}
+
+// Rotate, quantise to INT8 with one block scale, and store the codes.
+// Returns nothing; writes codes to dst_row (128 int8) and the scale via *scale_out.
+__device__ __forceinline__ void rope_quant_block(const uint16_t* __restrict__ src_row, bool valid,
+                                                 int pos, int half, const float* __restrict__ cos_t,
+                                                 const float* __restrict__ sin_t,
+                                                 int8_t* dst_row, float* scale_out, float* red) {
+  float y1[32], y2[32];
+  float amax = 0.f;
+  if (valid) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float a[8], bb[8];
+      load_bf16x8(src_row + half * 32 + c * 8, a);
+      load_bf16x8(src_row + 64 + half * 32 + c * 8, bb);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = half * 32 + c * 8 + j;
+        const float cs = __ldg(cos_t + static_cast<size_t>(pos) * 64 + i);
+        const float sn = __ldg(sin_t + static_cast<size_t>(pos) * 64 + i);
+        const float r1 = __fsub_rn(__fmul_rn(a[j], cs), __fmul_rn(bb[j], sn));
+        const float r2 = __fadd_rn(__fmul_rn(bb[j], cs), __fmul_rn(a[j], sn));
+        y1[c * 8 + j] = r1;
+        y2[c * 8 + j] = r2;
+        amax = fmaxf(amax, fmaxf(fabsf(r1), fabsf(r2)));
+      }
+    }
+  }
+  amax = block_max_256(amax, red);
+  const float scale = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) *scale_out = scale;
+  if (!valid) return;
+  uint32_t w1[8], w2[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t p1 = 0, p2 = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int c1 = 0, c2 = 0;
+      if (scale != 0.f) {
+        c1 = min(127, max(-127, __float2int_rn(__fdiv_rn(y1[4 * j + e], scale))));
+        c2 = min(127, max(-127, __float2int_rn(__fdiv_rn(y2[4 * j + e], scale))));
+      }
+      p1 |= (static_cast<uint32_t>(c1) & 0xFFu) << (8 * e);
+      p2 |= (static_cast<uint32_t>(c2) & 0xFFu) << (8 * e);
+    }
+    w1[j] = p1;
+    w2[j] = p2;
+  }
+  uint4* d1 = reinterpret_cast<uint4*>(dst_row + half * 32);
+  uint4* d2 = reinterpret_cast<uint4*>(dst_row + 64 + half * 32);
+  d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+  d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+  d2[0] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+  d2[1] = make_uint4(w2[4], w2[5], w2[6], w2[7]);
+}
+
+__global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
+    int B, int Hq, int Hkv, int ps, int num_pages, int bt_stride, int num_blocks,
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ bt,
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+    const uint16_t* __restrict__ v, const float* __restrict__ cos_t,
+    const float* __restrict__ sin_t, int8_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
+    float* __restrict__ k_bscale, int8_t* __restrict__ q_out, float* __restrict__ q_bscale,
+    int32_t* __restrict__ slots, int* err) {
+  constexpr int D = 128;
+  __shared__ float red[8];
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int begin = seq_begin(cu, b);
+  const int L = __ldg(cu + b) - begin;
+  if (blk * kBlk >= L) return;  // block past this sequence's end
+  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int pos = blk * kBlk + r;
+  const bool valid = pos < L;
+  const int t = begin + pos;
+
+  if (h < Hq) {
+    const uint16_t* src = q + (static_cast<size_t>(t) * Hq + h) * D;
+    int8_t* dst = q_out + (static_cast<size_t>(t) * Hq + h) * D;
+    rope_quant_block(src, valid, pos, half, cos_t, sin_t, dst,
+                     q_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hq + h, red);
+  }
+  if (h < Hkv) {
+    int page = 0;
+    if (valid) page = pool_page(bt, bt_stride, b, pos, ps, num_pages, half == 0 ? err : nullptr);
+    const bool ok = valid && page >= 0;
+    const size_t slot = static_cast<size_t>(ok ? page : 0) * ps + (pos % ps);
+    if (ok && slots != nullptr && h == 0 && half == 0) slots[t] = static_cast<int32_t>(slot);
+    const uint16_t* src = k + (static_cast<size_t>(t) * Hkv + h) * D;
+    int8_t* dst = k_pool + (slot * Hkv + h) * D;
+    // the block reduction needs every thread; an invalid page only drops the store
+    __shared__ __align__(16) int8_t sink[2 * D];
+    rope_quant_block(src, valid, pos, half, cos_t, sin_t, ok ? dst : sink,
+                     k_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hkv + h, red);
+    if (ok) {
+      const uint4* vs = reinterpret_cast<const uint4*>(v + (static_cast<size_t>(t) * Hkv + h) * D +
+                                                       half * 64);
+      uint4* vd = reinterpret_cast<uint4*>(v_pool + (slot * Hkv + h) * D + half * 64);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) vd[c] = vs[c];
+    }
+  }
+}
+
+// ------------------------------------------------------------ MLA rows
+// One warp per token: lane l quantises nope dims [16l, 16l + 16) (tile l / 8),
+// lanes 0..7 copy the 64 bf16 rope values, lanes 0/8/16/24 store the scales.
+constexpr int kMlaIn = 576, kMlaRow = 656;
+
+__global__ void __launch_bounds__(256) write_mla_row_kernel(
+    int T, int B, int ps, int num_pages, int bt_stride, const int32_t* __restrict__ cu,
+    const int32_t* __restrict__ start_pos, const int32_t* __restrict__ bt,
+    const uint16_t* __restrict__ kv, uint8_t* __restrict__ pool, int32_t* __restrict__ slots,
+    int* err) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int b = seq_of_token(cu, B, t);
+  const int p = (start_pos ? __ldg(start_pos + b) : 0) + (t - seq_begin(cu, b));
+  const int page = pool_page(bt, bt_stride, b, p, ps, num_pages, lane == 0 ? err : nullptr);
+  if (page < 0) return;
+  const size_t slot = static_cast<size_t>(page) * ps + (p % ps);
+  if (slots != nullptr && lane == 0) slots[t] = static_cast<int32_t>(slot);
+  const uint16_t* src = kv + static_cast<size_t>(t) * kMlaIn;
+  uint8_t* row = pool + slot * kMlaRow;
+
+  float a[8], c[8];
+  load_bf16x8(src + lane * 16, a);
+  load_bf16x8(src + lane * 16 + 8, c);
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fmaxf(fabsf(a[j]), fabsf(c[j])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = __fdiv_rn(amax, 127.0f);
+  uint32_t w[4] = {0, 0, 0, 0};
+  if (scale != 0.f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float x = j < 8 ? a[j] : c[j - 8];
+      const int code = min(127, max(-127, __float2int_rn(__fdiv_rn(x, scale))));
+      w[j / 4] |= (static_cast<uint32_t>(code) & 0xFFu) << (8 * (j % 4));
+    }
+  }
+  *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (lane < 8) {
+    *reinterpret_cast<uint4*>(row + 512 + lane * 16) =
+        *reinterpret_cast<const uint4*>(src + 512 + lane * 8);
+  }
+  if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 640 + 4 * (lane >> 3)) = scale;
+}
+
+}  // namespace
+
+cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) {
+  const int threads = 256;
+  switch (p.mode) {
+    case QPKV_WRITE_FP8_TOKEN_HEAD: {
+      const long warps = static_cast<long>(p.num_tokens) * p.num_heads_kv;
+      const int grid = static_cast<int>((warps * 32 + threads - 1) / threads);
+      if (grid == 0) return cudaSuccess;
+      auto* kern = p.head_dim == 128 ? write_fp8_token_head_kernel<128>
+                                     : write_fp8_token_head_kernel<64>;
+      kern<<<grid, threads, 0, stream>>>(
+          p.num_tokens, p.num_seqs, p.num_heads_kv, p.page_size, p.num_pages, p.bt_stride,
+          p.cu_seqlens_q, p.start_pos, p.block_table, static_cast<const uint16_t*>(p.k),
+          static_cast<const uint16_t*>(p.v), static_cast<uint8_t*>(p.k_pool),
+          static_cast<uint8_t*>(p.v_pool), p.k_scale_pool, p.v_scale_pool, p.slot_mapping,
+          p.error_word);
+      return cudaGetLastError();
+    }
+    case QPKV_WRITE_INT8_BLOCK128_ROPE: {
+      const int nblk = (p.max_seqlen + kBlk - 1) / kBlk;
+      if (nblk == 0) return cudaSuccess;
+      const int hmax = p.num_heads_q > p.num_heads_kv ? p.num_heads_q : p.num_heads_kv;
+      dim3 grid(nblk, hmax, p.num_seqs);
+      write_int8_block128_rope_kernel<<<grid, threads, 0, stream>>>(
+          p.num_seqs, p.num_heads_q, p.num_heads_kv, p.page_size, p.num_pages, p.bt_stride,
+          p.num_blocks, p.cu_seqlens_q, p.block_table, static_cast<const uint16_t*>(p.q),
+          static_cast<const uint16_t*>(p.k), static_cast<const uint16_t*>(p.v), p.rope_cos,
+          p.rope_sin, static_cast<int8_t*>(p.k_pool), static_cast<uint16_t*>(p.v_pool),
+          p.k_block_scale, static_cast<int8_t*>(p.q_out), p.q_block_scale, p.slot_mapping,
+          p.error_word);
+      return cudaGetLastError();
+    }
+    case QPKV_WRITE_MLA_ROW: {
+      const int grid = static_cast<int>((static_cast<long>(p.num_tokens) * 32 + threads - 1) /
+                                        threads);
+      if (grid == 0) return cudaSuccess;
+      write_mla_row_kernel<<<grid, threads, 0, stream>>>(
+          p.num_tokens, p.num_seqs, p.page_size, p.num_pages, p.bt_stride, p.cu_seqlens_q,
+          p.start_pos, p.block_table, static_cast<const uint16_t*>(p.k),
+          static_cast<uint8_t*>(p.k_pool), p.slot_mapping, p.error_word);
+      return cudaGetLastError();
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+// ----------------------------------------------------------- RoPE tables
+namespace {
+__global__ void rope_table_kernel(double theta, double rope_scale, int max_pos, int rot_dim,
+                                  float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  const int half = rot_dim / 2;
+  const long n = static_cast<long>(max_pos) * half;
+  for (long idx = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+    const double inv_freq = pow(theta, -2.0 * i / static_cast<double>(rot_dim));
+    const double angle = (static_cast<double>(pos) / rope_scale) * inv_freq;
+    cos_out[idx] = static_cast<float>(cos(angle));
+    sin_out[idx] = static_cast<float>(sin(angle));
+  }
+}
+}  // namespace
+
+cudaError_t launch_rope_table(float theta, float rope_scale, int max_pos, int rot_dim,
+                              float* cos_out, float* sin_out, cudaStream_t stream) {
+  const long n = static_cast<long>(max_pos) * (rot_dim / 2);
+  const int threads = 256;
+  const int grid = static_cast<int>(n / threads + 1 < 4096 ? n / threads + 1 : 4096);
+  rope_table_kernel<<<grid, threads, 0, stream>>>(theta, rope_scale, max_pos, rot_dim, cos_out,
+                                                  sin_out);
+  return cudaGetLastError();
+}
+
+}  // namespace qpkv

@@ -1,0 +1,191 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every symbol include/qpkv.h declares, mirrors its structs, plans on the host,
+and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qpkv.h")
+
+
+@pytest.fixture(scope="module")
+def qlib():
+    import quantized_paged_kv_varlen_gb300 as q
+    from quantized_paged_kv_varlen_gb300 import build
+    if not os.path.exists(q.LIB_PATH):
+        build.build()
+    return q, q.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qpkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(qlib):
+    _, lib = qlib
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_struct_mirror_and_strings(qlib):
+    q, lib = qlib
+    assert lib.qpkv_struct_size(0) == ctypes.sizeof(q.WriteParams)
+    assert lib.qpkv_struct_size(99) == 0
+    assert lib.qpkv_status_string(0) == b"ok"
+    assert lib.qpkv_status_string(3) == b"workspace too small"
+    assert lib.qpkv_version() >= 100
+
+
+def _plan(lib, lens, Hq=32, Hkv=8, ps=16, D=128, sms=148):
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    ib, fb = ctypes.c_size_t(), ctypes.c_size_t()
+    st = lib.qpkv_decode_workspace_sizes(lens.ctypes.data, len(lens), Hq, Hkv, D, sms,
+                                         ctypes.byref(ib), ctypes.byref(fb))
+    assert st == 0
+    host = np.zeros(ib.value, dtype=np.uint8)
+    info = (ctypes.c_int64 * 16)()
+    st = lib.qpkv_decode_plan_host(lens.ctypes.data, len(lens), Hq, Hkv, ps, D, sms,
+                                   host.ctypes.data, host.nbytes, info)
+    assert st == 0
+    n_items, chunk, total_splits, items_off, split_off_off = (info[i] for i in range(5))
+    items = host[items_off:items_off + 16 * n_items].view(np.int32).reshape(n_items, 4)
+    split_off = host[split_off_off:split_off_off + 4 * (len(lens) + 1)].view(np.int32)
+    return dict(info=list(info), items=items, split_off=split_off, chunk=chunk,
+                total_splits=total_splits, float_bytes=fb.value)
+
+
+def test_decode_plan_covers_every_token_once(qlib):
+    _, lib = qlib
+    rng = np.random.default_rng(0)
+    lens = rng.integers(0, 3000, 40)
+    lens[[3, 7]] = 0
+    lens[5] = 256
+    lens[6] = 257
+    p = _plan(lib, lens, Hq=8, Hkv=2)
+    chunk = p["chunk"]
+    assert chunk in (128, 256)
+    cover = {}
+    for b, h, t0, t1 in p["items"].tolist():
+        assert 0 <= t0 < t1 <= lens[b] and t1 - t0 <= chunk and t0 % chunk == 0
+        cover.setdefault((b, h), []).append((t0, t1))
+    for b, L in enumerate(lens):
+        for h in range(2):
+            spans = sorted(cover.get((b, h), []))
+            assert sum(t1 - t0 for t0, t1 in spans) == L
+            for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+                assert a1 == b0
+    splits = [(L + chunk - 1) // chunk for L in lens]
+    assert p["split_off"].tolist() == np.concatenate([[0], np.cumsum(splits)]).tolist()
+    assert p["total_splits"] == sum(splits)
+    # items of one token range are adjacent across kv heads
+    it = p["items"]
+    assert np.all(it[0::2, 1] == 0) and np.all(it[1::2, 1] == 1)
+    assert np.array_equal(it[0::2, [0, 2]], it[1::2, [0, 2]])
+    assert p["float_bytes"] >= sum(splits) * 8 * 129 * 4
+
+
+def test_small_batches_use_smaller_items(qlib):
+    _, lib = qlib
+    assert _plan(lib, [37, 100], Hq=4, Hkv=1, D=64)["chunk"] == 128
+    assert _plan(lib, [4000] * 64)["chunk"] == 256
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(B=0), 1), (dict(lens=[5, -1]), 1), (dict(D=96), 2), (dict(Hq=64, Hkv=4), 2),
+    (dict(Hq=12, Hkv=8), 1)])
+def test_decode_sizes_rejects_bad_arguments(qlib, args, want):
+    _, lib = qlib
+    lens = np.ascontiguousarray(args.get("lens", [5, 6]), dtype=np.int32)
+    B = args.get("B", len(lens))
+    ib, fb = ctypes.c_size_t(), ctypes.c_size_t()
+    st = lib.qpkv_decode_workspace_sizes(lens.ctypes.data, B, args.get("Hq", 32),
+                                         args.get("Hkv", 8), args.get("D", 128), 148,
+                                         ctypes.byref(ib), ctypes.byref(fb))
+    assert st == want
+
+
+def test_plan_rejects_page_size_and_small_buffers(qlib):
+    _, lib = qlib
+    lens = np.ascontiguousarray([100, 200], dtype=np.int32)
+    host = np.zeros(1 << 16, dtype=np.uint8)
+    info = (ctypes.c_int64 * 16)()
+    assert lib.qpkv_decode_plan_host(lens.ctypes.data, 2, 32, 8, 24, 128, 148,
+                                     host.ctypes.data, host.nbytes, info) == 2
+    assert lib.qpkv_decode_plan_host(lens.ctypes.data, 2, 32, 8, 16, 128, 148,
+                                     host.ctypes.data, 8, info) == 3
+
+
+def test_run_rejects_foreign_plan_and_null_pointers(qlib):
+    _, lib = qlib
+    bogus = (ctypes.c_int64 * 16)(*([7] * 16))
+    fake = ctypes.c_void_p(0x100000)
+    st = lib.qpkv_decode_run(bogus, fake, 1 << 20, fake, fake, fake, fake, fake, fake, 10, 16,
+                             fake, 4, ctypes.c_float(0.1), fake, None, None, None)
+    assert st == 1
+    p = _plan(lib, [100, 200])
+    info = (ctypes.c_int64 * 16)(*p["info"])
+    st = lib.qpkv_decode_run(info, None, 1 << 20, fake, fake, fake, fake, fake, fake, 10, 16,
+                             fake, 4, ctypes.c_float(0.1), fake, None, None, None)
+    assert st == 1
+    st = lib.qpkv_decode_run(info, fake, 16, fake, fake, fake, fake, fake, fake, 10, 16,
+                             fake, 16, ctypes.c_float(0.1), fake, None, None, None)
+    assert st == 3
+    misaligned = ctypes.c_void_p(0x100004)
+    st = lib.qpkv_decode_run(info, fake, 1 << 30, fake, misaligned, fake, fake, fake, fake, 10,
+                             16, fake, 16, ctypes.c_float(0.1), fake, None, None, None)
+    assert st == 1
+    # 200 tokens in pages of 16 need 13 block_table entries per row
+    st = lib.qpkv_decode_run(info, fake, 1 << 30, fake, fake, fake, fake, fake, fake, 10, 16,
+                             fake, 12, ctypes.c_float(0.1), fake, None, None, None)
+    assert st == 1
+
+
+def test_write_cache_rejects_before_launch(qlib):
+    q, lib = qlib
+    assert lib.qpkv_write_cache(None, None) == 1
+    p = q.WriteParams()
+    fake = 0x100000
+    for n in ("cu_seqlens_q", "block_table", "k", "v", "k_pool", "v_pool", "k_scale_pool",
+              "v_scale_pool", "q", "q_out", "k_block_scale", "q_block_scale"):
+        setattr(p, n, fake)
+    p.num_seqs, p.num_tokens, p.num_heads_kv, p.head_dim = 2, 10, 1, 128
+    p.page_size, p.num_pages, p.bt_stride = 16, 4, 2
+    p.mode = 7
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
+    p.mode = 0
+    p.page_size = 24
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
+    p.page_size = 16
+    p.head_dim = 96
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
+    p.head_dim = 128
+    p.k = fake + 4
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
+    p.k = fake
+    p.mode = 1                       # INT8 mode: start_pos must be NULL, tables present
+    p.num_heads_q = 1
+    p.start_pos = fake
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
+    p.start_pos = None
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1   # no RoPE tables
+    p.mode = 2                       # MLA needs head_dim 576
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
+
+
+def test_binding_raises_without_library(tmp_path):
+    import quantized_paged_kv_varlen_gb300 as q
+    saved = q._lib
+    q._lib = None
+    try:
+        with pytest.raises(ImportError):
+            q.load(str(tmp_path / "missing.so"))
+    finally:
+        q._lib = saved

@@ -1,0 +1,184 @@
+"""GPU parity: FP8 cache write (bit-exact) and split-KV paged decode against
+the CPU oracle, on the tiny workload, edge cases and the full Llama-3-8B
+shaped batch (sampled requests), through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oatt
+from oracle import cache as ocache
+from quantized_paged_kv_varlen_gb300 import synth
+from tests.gpu_util import assert_attention_close, assert_lse_close, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+FILL = 0x7F                # an E4M3 NaN code in every unwritten pool byte
+SCALE_FILL = np.float32("nan")
+
+
+def _dev_inputs(lib, wl, k, v):
+    dev = "cuda"
+    P, ps, H, D = wl.num_pages, wl.page_size, wl.Hkv, wl.D
+    k_pool = torch.full((P, ps, H, D), FILL, dtype=torch.uint8, device=dev)
+    v_pool = torch.full_like(k_pool, FILL)
+    ks = torch.full((P, ps, H), float("nan"), dtype=torch.float32, device=dev)
+    vs = torch.full_like(ks, float("nan"))
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    cu = torch.from_numpy(np.cumsum(wl.lengths).astype(np.int32)).to(dev)
+    slots = torch.full((k.shape[0],), -1, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kt = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+    vt = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+    lib.write_cache_fp8(kt, vt, cu, bt, k_pool, v_pool, ks, vs, slot_mapping=slots,
+                        error_word=err)
+    return dict(k_pool=k_pool, v_pool=v_pool, ks=ks, vs=vs, bt=bt, slots=slots, err=err)
+
+
+def _oracle_cache(wl, k, v, reqs=None):
+    """Oracle pools; with reqs given, a compact pool holding only their pages
+    (and a block table remapped to it)."""
+    lens = wl.lengths
+    if reqs is None:
+        reqs = list(range(wl.B))
+        bt = wl.block_table
+        P = wl.num_pages
+        kk, vv, cu = k, v, np.cumsum(lens)
+    else:
+        offs = np.concatenate([[0], np.cumsum(lens)])
+        bt = np.full((len(reqs), wl.block_table.shape[1]), -1, np.int32)
+        P = 0
+        parts_k, parts_v = [], []
+        for i, b in enumerate(reqs):
+            n = (int(lens[b]) + wl.page_size - 1) // wl.page_size
+            bt[i, :n] = np.arange(P, P + n)
+            P += n
+            parts_k.append(k[offs[b]:offs[b + 1]])
+            parts_v.append(v[offs[b]:offs[b + 1]])
+        kk, vv = np.concatenate(parts_k), np.concatenate(parts_v)
+        cu = np.cumsum(lens[reqs])
+    shape = (max(P, 1), wl.page_size, wl.Hkv, wl.D)
+    fill = np.full(shape, FILL, np.uint8)
+    sfill = np.full(shape[:3], SCALE_FILL, np.float32)
+    kp, vp, ksp, vsp, slots, _ = ocache.write_fp8_token_head(
+        kk, vv, cu, np.zeros(len(reqs), np.int64), bt, wl.page_size, fill, fill, sfill, sfill)
+    return kp, vp, ksp, vsp, bt, reqs
+
+
+def _u32(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def _check_decode(lib, wl, reqs=None, check_pool_bytes=True):
+    k, v = wl.kv_all()
+    d = _dev_inputs(lib, wl, k, v)
+    plan = lib.DecodePlan(wl.lengths, wl.Hq, wl.Hkv, wl.page_size, wl.D)
+    q = torch.from_numpy(wl.q).cuda().to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty(wl.B, wl.Hq, dtype=torch.float32, device="cuda")
+    plan.run(q, d["k_pool"], d["v_pool"], d["ks"], d["vs"], d["bt"], wl.scale, out=out, lse=lse,
+             error_word=d["err"])
+    torch.cuda.synchronize()
+    assert int(d["err"].item()) == 0
+
+    kp, vp, ksp, vsp, obt, reqs = _oracle_cache(wl, k, v, reqs)
+    want_o, want_lse = oatt.paged_decode_fp8(wl.q[reqs], kp, vp, ksp, vsp, obt,
+                                             wl.lengths[reqs], wl.scale)
+    got_o = bf16_to_f64(out)[reqs]
+    got_lse = lse.cpu().numpy().astype(np.float64)[reqs]
+    assert_attention_close(got_o, want_o)
+    assert_lse_close(got_lse, want_lse)
+
+    if check_pool_bytes:
+        # the cache rows of the checked requests, bit for bit (scales as bits)
+        gk = d["k_pool"].cpu().numpy()
+        gks = d["ks"].cpu().numpy()
+        for i, b in enumerate(reqs):
+            n = (int(wl.lengths[b]) + wl.page_size - 1) // wl.page_size
+            gp = wl.block_table[b, :n]
+            op = obt[i, :n]
+            assert np.array_equal(gk[gp], kp[op]), f"k bytes differ for request {b}"
+            assert np.array_equal(_u32(gks[gp]), _u32(ksp[op])), f"k scales differ ({b})"
+    return d, plan
+
+
+def test_write_cache_fp8_bit_exact_tiny(lib):
+    wl = synth.tiny_decode(0)
+    k, v = wl.kv_all()
+    d = _dev_inputs(lib, wl, k, v)
+    torch.cuda.synchronize()
+    kp, vp, ksp, vsp, bt, _ = _oracle_cache(wl, k, v)
+    assert np.array_equal(d["k_pool"].cpu().numpy(), kp)
+    assert np.array_equal(d["v_pool"].cpu().numpy(), vp)
+    assert np.array_equal(_u32(d["ks"].cpu().numpy()), _u32(ksp))
+    assert np.array_equal(_u32(d["vs"].cpu().numpy()), _u32(vsp))
+    want_slots = ocache.slot_mapping(np.cumsum(wl.lengths), np.zeros(2, np.int64), bt, 16)
+    assert np.array_equal(d["slots"].cpu().numpy(), want_slots)
+    assert int(d["err"].item()) == 0
+
+
+def test_decode_tiny_gqa4_d64(lib):
+    _check_decode(lib, synth.tiny_decode(0))
+
+
+@pytest.mark.parametrize("lengths,ps,Hq,Hkv,D", [
+    ([0, 1, 127, 128, 129], 16, 4, 1, 64),
+    ([255, 256, 257, 1000, 3], 32, 8, 1, 128),
+    ([300, 64, 17], 64, 8, 2, 128),
+    ([513, 200], 128, 8, 8, 128),
+    ([700, 33, 256], 256, 16, 2, 128),
+    ([1200, 5], 16, 32, 8, 128),
+])
+def test_decode_edge_shapes(lib, lengths, ps, Hq, Hkv, D):
+    rng = np.random.default_rng(11)
+    lengths = np.asarray(lengths, dtype=np.int32)
+    bt, P = synth.page_tables(rng, lengths, ps, extra_pages=3)
+    wl = synth.DecodeWorkload(seed=11, B=len(lengths), Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                              lengths=lengths, block_table=bt, num_pages=P,
+                              q=synth.bf16_normal(rng, (len(lengths), Hq, D)),
+                              scale=1.0 / np.sqrt(D), workload_id=9)
+    _check_decode(lib, wl)
+
+
+def test_decode_large_magnitudes_and_constant_keys(lib):
+    """Scaled queries (large logits) and a request whose keys are all equal."""
+    rng = np.random.default_rng(12)
+    lengths = np.array([400, 260], dtype=np.int32)
+    bt, P = synth.page_tables(rng, lengths, 16)
+    q = synth.bf16_round(synth.bf16_normal(rng, (2, 8, 128)) * 8.0)
+    wl = synth.DecodeWorkload(seed=12, B=2, Hq=8, Hkv=2, D=128, page_size=16, lengths=lengths,
+                              block_table=bt, num_pages=P, q=q, scale=1.0 / np.sqrt(128.0),
+                              workload_id=8)
+    _check_decode(lib, wl)
+
+
+def test_decode_bad_page_sets_error_word(lib):
+    rng = np.random.default_rng(13)
+    lengths = np.array([100, 50], dtype=np.int32)
+    bt, P = synth.page_tables(rng, lengths, 16)
+    wl = synth.DecodeWorkload(seed=13, B=2, Hq=4, Hkv=1, D=128, page_size=16, lengths=lengths,
+                              block_table=bt, num_pages=P, q=synth.bf16_normal(rng, (2, 4, 128)),
+                              scale=0.1, workload_id=7)
+    k, v = wl.kv_all()
+    d = _dev_inputs(lib, wl, k, v)
+    bad = d["bt"].clone()
+    bad[1, 0] = P + 5                                     # outside the pool
+    plan = lib.DecodePlan(wl.lengths, 4, 1, 16, 128)
+    q = torch.from_numpy(wl.q).cuda().to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = plan.run(q, d["k_pool"], d["v_pool"], d["ks"], d["vs"], bad, wl.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & lib.DEV_ERR_BAD_PAGE
+    # request 0 never touches the bad entry and is still right
+    kp, vp, ksp, vsp, obt, _ = _oracle_cache(wl, k, v, [0])
+    want, _ = oatt.paged_decode_fp8(wl.q[[0]], kp, vp, ksp, vsp, obt, wl.lengths[[0]], wl.scale)
+    assert_attention_close(bf16_to_f64(out)[[0]], want)
+
+
+def test_decode_full_batch_sampled(lib):
+    """B=64, L ~ U{512..8192}, 32/8 heads, D=128, page 16: the benchmark's
+    launch configuration; the oracle checks the shortest, the longest and
+    two other requests (all heads) and their cache bytes."""
+    wl = synth.batched_decode(0)
+    order = np.argsort(wl.lengths)
+    reqs = sorted({int(order[0]), int(order[-1]), 5, 40})
+    _check_decode(lib, wl, reqs=reqs)
