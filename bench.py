@@ -1,0 +1,488 @@
+"""Benchmark: paged FP8 decode step on the Llama-3-8B-shaped batch.
+
+Workload (one step = one pass of the decode hot path over one batch):
+  B = 64 requests, kv lengths ~ U{512..8192}, 32 query / 8 kv heads,
+  head_dim 128, page 16, pages randomly permuted in the pool, FP8 E4M3 K/V
+  with fp32 per-(token, head) scales.  Each step appends one new token per
+  request through the cache-write kernel, re-plans the split-KV work list
+  (host planner + one async copy), runs the split-KV attention kernel and the
+  log-sum-exp merge.  Inputs are resident in HBM (the cache is ~589 MB per
+  step of reads, larger than the 129 MB L2, so no flush is needed).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(test infrastructure) on a bounded sample of the same workload instead.
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
+collective on the data path); time = max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode HBM GB/s & tokens/s; FP8 prefill TFLOP/s (% of GB300 roofline)"
+WORKLOAD = ("Llama-3-8B-shaped paged FP8 decode: B=64, q_len=1, kv lengths ~U{512..8192}, "
+            "32 qo / 8 kv heads, head_dim 128, page 16, permuted page pool, E4M3 K/V with "
+            "fp32 per-(token, head) scales")
+B, HQ, HKV, D, PS, LO, HI = 64, 32, 8, 128, 16, 512, 8192
+L2_BYTES = 129 * 2 ** 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_attend_llama8b_b64.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "quantized_paged_kv_varlen_gb300", "csrc", "decode.cu")
+
+
+def algorithmic_bytes(lengths):
+    """Bytes the decode step must move at minimum (per request batch)."""
+    import numpy as np
+    lengths = np.asarray(lengths, dtype=np.int64)
+    kv = int(lengths.sum()) * HKV * D * 2                # E4M3 K and V
+    scales = int(lengths.sum()) * HKV * 4 * 2            # fp32 k/v scales
+    bt = int(((lengths + PS - 1) // PS).sum()) * 4       # block table entries
+    q = len(lengths) * HQ * D * 2                        # bf16 query
+    o = len(lengths) * HQ * (D * 2 + 4)                  # bf16 output + lse
+    new = len(lengths) * HKV * (D * 2 * 2 + (D + 4) * 2)  # new token: bf16 in, fp8+scale out
+    attend = kv + scales + bt + q
+    return attend + o + new, attend
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) while the GPU is loaded."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if len(r) >= 9]
+        inside = [r for t, r in self.rows if t0 <= t <= t1 and len(r) >= 9]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(use[0][2]), "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max((num(r[3]) or 0.0) for r in use)}
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value, world, device=None):
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- workload
+
+class DecodeBench:
+    """Device-resident decode workload for one rank (seed = base + rank)."""
+
+    def __init__(self, seed, device):
+        import numpy as np
+        import torch
+        import quantized_paged_kv_varlen_gb300 as q
+        from quantized_paged_kv_varlen_gb300 import synth
+        self.q, self.torch, self.device = q, torch, device
+        rng = np.random.default_rng((seed, 2))
+        self.lengths = rng.integers(LO, HI + 1, size=B).astype(np.int32)
+        bt, P = synth.page_tables(rng, self.lengths, PS)
+        self.P = P
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        dev = device
+        # cache holds L_b - 1 tokens; each step appends token L_b - 1 and decodes L_b tokens
+        prev = self.lengths - 1
+        T0 = int(prev.sum())
+        self.k_pool = torch.zeros((P, PS, HKV, D), dtype=torch.uint8, device=dev)
+        self.v_pool = torch.zeros_like(self.k_pool)
+        self.ks = torch.zeros((P, PS, HKV), dtype=torch.float32, device=dev)
+        self.vs = torch.zeros_like(self.ks)
+        self.bt = torch.from_numpy(bt).to(dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        chunk = 1 << 22
+        cu_prev = torch.from_numpy(np.cumsum(prev).astype(np.int32)).to(dev)
+        k_all = torch.empty((T0, HKV, D), dtype=torch.bfloat16, device=dev)
+        v_all = torch.empty_like(k_all)
+        for t in range(0, T0, chunk):
+            n = min(chunk, T0 - t)
+            k_all[t:t + n] = torch.randn((n, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+            v_all[t:t + n] = torch.randn((n, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+        q.write_cache_fp8(k_all, v_all, cu_prev, self.bt, self.k_pool, self.v_pool, self.ks,
+                          self.vs, error_word=self.err)
+        del k_all, v_all
+        # per-step inputs: one new token per request, the query
+        self.k_new = torch.randn((B, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+        self.v_new = torch.randn((B, HKV, D), generator=g, device=dev).to(torch.bfloat16)
+        self.qry = torch.randn((B, HQ, D), generator=g, device=dev).to(torch.bfloat16)
+        self.cu_new = torch.arange(1, B + 1, dtype=torch.int32, device=dev)
+        self.start_pos = torch.from_numpy(prev.astype(np.int32)).to(dev)
+        self.out = torch.empty((B, HQ, D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, HQ), dtype=torch.float32, device=dev)
+        self.scale = 1.0 / float(np.sqrt(D))
+        self.plan = q.DecodePlan(self.lengths, HQ, HKV, PS, D, device=dev)
+        torch.cuda.synchronize()
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error word {int(self.err.item())} during setup")
+        self.total_bytes, self.attend_bytes = algorithmic_bytes(self.lengths)
+
+    def step(self, ev_attend=None):
+        q = self.q
+        q.write_cache_fp8(self.k_new, self.v_new, self.cu_new, self.bt, self.k_pool, self.v_pool,
+                          self.ks, self.vs, start_pos=self.start_pos, error_word=self.err)
+        self.plan.replan()
+        if ev_attend is not None:
+            ev_attend[0].record()
+        self.plan.attend(self.qry, self.k_pool, self.v_pool, self.ks, self.vs, self.bt,
+                         self.scale, error_word=self.err)
+        if ev_attend is not None:
+            ev_attend[1].record()
+        self.plan.merge(self.out, self.lse)
+
+
+def kernel_source_hash():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per attend launch from the committed ncu summary, or None
+    when the kernel source changed since that capture."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    vals = {}
+    for line in open(PROFILE_SUMMARY):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def cpu_worker(seconds, n_req):
+    """Runs in a child process with one BLAS/OpenMP thread: times the oracle's
+    paged decode on n_req requests of the workload (repeated for `seconds`)."""
+    import numpy as np
+    from quantized_paged_kv_varlen_gb300 import synth
+    from oracle import attention as oatt
+    from oracle import cache as ocache
+    wl = synth.batched_decode(0)
+    order = np.argsort(wl.lengths)
+    reqs = [int(order[len(order) * (i + 1) // (n_req + 1)]) for i in range(n_req)]
+    prepared = []
+    for b in reqs:
+        k, v = wl.kv(b)
+        L = k.shape[0]
+        n = (L + PS - 1) // PS
+        bt = np.arange(n, dtype=np.int32)[None]
+        z8 = np.zeros((n, PS, HKV, D), np.uint8)
+        zs = np.zeros((n, PS, HKV), np.float32)
+        kp, vp, ksp, vsp, _, _ = ocache.write_fp8_token_head(
+            k, v, np.array([L]), np.array([0]), bt, PS, z8, z8, zs, zs)
+        prepared.append((b, L, kp, vp, ksp, vsp, bt))
+    lens = [p[1] for p in prepared]
+    total, _ = algorithmic_bytes(lens)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        for b, L, kp, vp, ksp, vsp, bt in prepared:
+            oatt.paged_decode_fp8(wl.q[[b]], kp, vp, ksp, vsp, bt, np.array([L]), wl.scale)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": total * passes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_req} requests of the workload (lengths {lens}), all 32 heads, "
+                      f"{passes} passes in {dt:.1f} s, one thread",
+            "seconds_per_pass": dt / passes, "tokens_per_s": len(lens) * passes / dt}
+
+
+def run_cpu_baseline(seconds, n_req):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(seconds), str(n_req)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args):
+    """The oracle as the reference arm: K timed steps, each the oracle's
+    decode of a bounded sample (2 requests) of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    from quantized_paged_kv_varlen_gb300 import synth
+    from oracle import attention as oatt
+    from oracle import cache as ocache
+    wl = synth.batched_decode(0)
+    order = np.argsort(wl.lengths)
+    reqs = [int(order[len(order) // 3]), int(order[2 * len(order) // 3])]
+    prepared = []
+    for b in reqs:
+        k, v = wl.kv(b)
+        L = k.shape[0]
+        n = (L + PS - 1) // PS
+        bt = np.arange(n, dtype=np.int32)[None]
+        z8 = np.zeros((n, PS, HKV, D), np.uint8)
+        zs = np.zeros((n, PS, HKV), np.float32)
+        kp, vp, ksp, vsp, _, _ = ocache.write_fp8_token_head(
+            k, v, np.array([L]), np.array([0]), bt, PS, z8, z8, zs, zs)
+        prepared.append((b, L, kp, vp, ksp, vsp, bt))
+    lens = [p[1] for p in prepared]
+    total, _ = algorithmic_bytes(lens)
+
+    def step():
+        for b, L, kp, vp, ksp, vsp, bt in prepared:
+            oatt.paged_decode_fp8(wl.q[[b]], kp, vp, ksp, vsp, bt, np.array([L]), wl.scale)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = total * args.steps / dt / 1e9
+    sample = f"2 requests (lengths {lens}) of the workload per step, all 32 heads"
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "tokens_per_s": len(lens) * args.steps / dt,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_qpkv(args):
+    import torch
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import quantized_paged_kv_varlen_gb300 as q
+    if not os.path.exists(q.LIB_PATH):
+        from quantized_paged_kv_varlen_gb300 import build
+        if rank == 0:
+            build.build()
+        barrier(world, device)
+    q.load()
+    wb = DecodeBench(seed=rank, device=device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    # warm-up: W steps, and at least ~1 s of work so clocks settle
+    t_w = time.time()
+    n_w = 0
+    while n_w < args.warmup or time.time() - t_w < args.min_warmup_s:
+        wb.step()
+        n_w += 1
+        if n_w % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_region0 = time.time()
+    ev0.record()
+    for i in range(args.steps):
+        wb.step(att[i])
+    ev1.record()
+    torch.cuda.synchronize()
+    t_region1 = time.time()
+    barrier(world, device)
+    ms = ev0.elapsed_time(ev1)
+    ms_attend = sum(a.elapsed_time(b) for a, b in att) / args.steps
+    ms_max = max_over_ranks(ms, world, device)
+    if int(wb.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(wb.err.item())}")
+
+    # end to end through the public API with host buffers in the timed region
+    pin_q = wb.qry.cpu().pin_memory()
+    pin_k = wb.k_new.cpu().pin_memory()
+    pin_v = wb.v_new.cpu().pin_memory()
+    pin_o = torch.empty(wb.out.shape, dtype=wb.out.dtype).pin_memory()
+    h2d = pin_q.numel() * 2 + pin_k.numel() * 2 + pin_v.numel() * 2
+    d2h = pin_o.numel() * 2
+
+    def e2e_step():
+        wb.qry.copy_(pin_q, non_blocking=True)
+        wb.k_new.copy_(pin_k, non_blocking=True)
+        wb.v_new.copy_(pin_v, non_blocking=True)
+        wb.step()
+        pin_o.copy_(wb.out, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, device)
+    sampler.stop()
+    clocks = sampler.summary(t_region0, t_region1)
+
+    if rank != 0:
+        return
+    step_s = ms_max / 1e3 / args.steps
+    value = wb.total_bytes * world / step_s / 1e9
+    peak, peak_kind = peaks()
+    achieved = wb.attend_bytes / (ms_attend / 1e3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args.cpu_seconds, 3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": f"U{{{LO}..{HI}}}",
+                   "parallelism": f"replicas x{world} (independent requests, no collective)",
+                   "l2": f"no flush: {wb.total_bytes / 1e6:.0f} MB moved per step > "
+                         f"{L2_BYTES / 1e6:.0f} MB L2",
+                   "step": "write_cache(1 token/request) + host plan + split-KV attend + "
+                           "LSE merge",
+                   "sum_kv_tokens": int(wb.lengths.sum())},
+        "tokens_per_s": B * world / step_s,
+        "algorithmic_bytes_per_step": wb.total_bytes,
+        "roofline": {"bound": "hbm", "kernel": "decode_attend", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": wb.attend_bytes,
+                     "ms_per_launch": ms_attend},
+        "cpu_baseline": cpu,
+        "e2e": {"value": wb.total_bytes * world / (ms_e2e / 1e3 / args.steps) / 1e9,
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e / args.steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-worker":
+        print(json.dumps(cpu_worker(float(sys.argv[2]), int(sys.argv[3]))))
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["qpkv", "reference"], default="qpkv")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up for at least this long so clocks settle")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_qpkv(args)
+
+
+if __name__ == "__main__":
+    main()

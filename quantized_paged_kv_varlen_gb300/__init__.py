@@ -276,12 +276,32 @@ class DecodePlan:
         self.int_bytes, self.float_bytes = ib.value, fb.value
         self.int_ws = torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, device=device)
         self.float_ws = torch.empty(max(self.float_bytes, 256), dtype=torch.uint8, device=device)
-        self.pinned = torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, pin_memory=True)
+        # two page-locked staging buffers: the host rewrites one only after the
+        # stream has copied out of it (an event recorded behind the copy)
+        self._pinned = [torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, pin_memory=True)
+                        for _ in range(2)]
+        self._copied = [None, None]
+        self._which = 0
         self.plan_info = (ctypes.c_int64 * PLAN_INFO_LEN)()
-        _check(lib.qpkv_decode_plan(lens.ctypes.data, self.B, self.Hq, self.Hkv, page_size,
-                                    self.D, self.num_sms, ctypes.c_void_p(self.pinned.data_ptr()),
-                                    self.pinned.numel(), _ptr(self.int_ws), self.int_ws.numel(),
-                                    self.plan_info, _stream()), "qpkv_decode_plan")
+        self.replan()
+
+    def replan(self):
+        """Run the host planner again and copy the work list to the device on
+        the current stream (the per-step cost of the plan/run split)."""
+        torch = _torch()
+        lib = load()
+        buf = self._pinned[self._which]
+        if self._copied[self._which] is not None:
+            self._copied[self._which].synchronize()
+        _check(lib.qpkv_decode_plan(self.lens.ctypes.data, self.B, self.Hq, self.Hkv,
+                                    self.page_size, self.D, self.num_sms,
+                                    ctypes.c_void_p(buf.data_ptr()), buf.numel(),
+                                    _ptr(self.int_ws), self.int_ws.numel(), self.plan_info,
+                                    _stream()), "qpkv_decode_plan")
+        ev = torch.cuda.Event()
+        ev.record()
+        self._copied[self._which] = ev
+        self._which ^= 1
 
     @property
     def num_items(self):

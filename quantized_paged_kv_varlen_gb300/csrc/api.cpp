@@ -52,13 +52,16 @@ bool supported_decode_shape(int64_t Hq, int64_t Hkv, int64_t D) {
   return (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
-// Work-item size: 256 tokens, or 128 when the batch is too small to fill
-// the GPU with 256-token items.
+// Work-item size: 512 tokens when that still gives every SM a few items,
+// else 256 or 128 so that small batches spread over the GPU.
 int64_t pick_chunk(const int32_t* lens, int32_t B, int64_t Hkv, int32_t num_sms) {
-  int64_t items = 0;
-  for (int32_t b = 0; b < B; ++b) items += (static_cast<int64_t>(lens[b]) + 255) / 256;
-  items *= Hkv;
-  return items < static_cast<int64_t>(num_sms > 0 ? num_sms : 148) ? 128 : 256;
+  const int64_t sms = num_sms > 0 ? num_sms : 148;
+  for (int64_t chunk : {512, 256}) {
+    int64_t items = 0;
+    for (int32_t b = 0; b < B; ++b) items += (static_cast<int64_t>(lens[b]) + chunk - 1) / chunk;
+    if (items * Hkv >= 4 * sms) return chunk;
+  }
+  return 128;
 }
 
 void fill_plan_layout(const int32_t* lens, int32_t B, int64_t Hq, int64_t Hkv, int64_t D,
@@ -241,7 +244,7 @@ qpkv_status qpkv_decode_plan_host(const int32_t* lens, int32_t B, int32_t Hq, in
     for (int64_t t0 = 0; t0 < lens[b]; t0 += p.chunk, ++s) {
       const int32_t t1 = static_cast<int32_t>(t0 + p.chunk < lens[b] ? t0 + p.chunk : lens[b]);
       for (int32_t h = 0; h < Hkv; ++h)
-        items[n++] = DecodeItem{b, h, static_cast<int32_t>(t0), t1};
+        items[n++] = DecodeItem{b, h, static_cast<int32_t>(t0), t1, static_cast<int32_t>(s), 0, 0, 0};
     }
   }
   split_off[B] = static_cast<int32_t>(s);

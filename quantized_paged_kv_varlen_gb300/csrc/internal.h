@@ -10,9 +10,10 @@
 
 namespace qpkv {
 
-// Work item of the split-KV decode: request, kv head, token range [t0, t1).
+// Work item of the split-KV decode: request, kv head, token range [t0, t1),
+// and the row of its partial result in the float workspace.
 struct DecodeItem {
-  int32_t b, hk, t0, t1;
+  int32_t b, hk, t0, t1, slot, pad0, pad1, pad2;
 };
 
 // Layout of the decode plan (int workspace) and the float workspace.

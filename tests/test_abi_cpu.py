@@ -56,7 +56,7 @@ def _plan(lib, lens, Hq=32, Hkv=8, ps=16, D=128, sms=148):
                                    host.ctypes.data, host.nbytes, info)
     assert st == 0
     n_items, chunk, total_splits, items_off, split_off_off = (info[i] for i in range(5))
-    items = host[items_off:items_off + 16 * n_items].view(np.int32).reshape(n_items, 4)
+    items = host[items_off:items_off + 32 * n_items].view(np.int32).reshape(n_items, 8)
     split_off = host[split_off_off:split_off_off + 4 * (len(lens) + 1)].view(np.int32)
     return dict(info=list(info), items=items, split_off=split_off, chunk=chunk,
                 total_splits=total_splits, float_bytes=fb.value)
@@ -71,10 +71,11 @@ def test_decode_plan_covers_every_token_once(qlib):
     lens[6] = 257
     p = _plan(lib, lens, Hq=8, Hkv=2)
     chunk = p["chunk"]
-    assert chunk in (128, 256)
+    assert chunk in (128, 256, 512)
     cover = {}
-    for b, h, t0, t1 in p["items"].tolist():
+    for b, h, t0, t1, slot, *_ in p["items"].tolist():
         assert 0 <= t0 < t1 <= lens[b] and t1 - t0 <= chunk and t0 % chunk == 0
+        assert slot == p["split_off"][b] + t0 // chunk
         cover.setdefault((b, h), []).append((t0, t1))
     for b, L in enumerate(lens):
         for h in range(2):
@@ -95,7 +96,8 @@ def test_decode_plan_covers_every_token_once(qlib):
 def test_small_batches_use_smaller_items(qlib):
     _, lib = qlib
     assert _plan(lib, [37, 100], Hq=4, Hkv=1, D=64)["chunk"] == 128
-    assert _plan(lib, [4000] * 64)["chunk"] == 256
+    assert _plan(lib, [4000] * 64)["chunk"] == 512
+    assert _plan(lib, [300] * 64, sms=148)["chunk"] == 256
 
 
 @pytest.mark.parametrize("args,want", [
