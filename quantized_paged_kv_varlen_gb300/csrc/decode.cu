@@ -127,11 +127,13 @@ struct SharedState {
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SharedState& sh,
                                               int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if (clock64() - t0 > kWaitTimeoutCycles) {
       sh.abort = 1;
       report_error(err, kDevErrTimeout);
       return false;

@@ -7,9 +7,10 @@
 
 namespace qpkv {
 
-// Every spin-wait gives up after this many nanoseconds and reports
+// Every spin-wait gives up after this many SM cycles (about 2 s at the
+// 2.07 GHz maximum clock, longer at lower clocks) and reports
 // QPKV_DEV_ERR_TIMEOUT through the caller's device error word.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 // bits of the device error word (atomicOr'ed by kernels)
 constexpr int kDevErrTimeout = 1;     // an mbarrier wait ran out
@@ -63,13 +64,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-suspending probe of the same condition (the thread keeps spinning
+// instead of sleeping until the phase completes).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; false on timeout.
+// The timeout uses the SM cycle counter, sampled every 64 polls, so a
+// completed phase is noticed within one poll.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitTimeoutCycles) return false;
   }
 }
 
