@@ -47,6 +47,7 @@ typedef int32_t qpkv_status;
 #define QPKV_ERR_CUDA 4                /* a CUDA runtime/driver call or launch failed */
 #define QPKV_ERR_DEVICE 5              /* reserved: device error word reported by a caller */
 #define QPKV_ERR_TIMEOUT 6             /* reserved: device wait timeout reported by a caller */
+#define QPKV_ERR_STATIC_LIMIT 7        /* problem too large for qpkv_decode_static's fixed scratch */
 
 /* bits a kernel ORs into the device error word */
 #define QPKV_DEV_ERR_TIMEOUT 1   /* an internal pipeline wait gave up after ~2 s */
@@ -225,6 +226,39 @@ qpkv_status qpkv_decode_attend(const int64_t* plan_info, void* float_ws, size_t 
 qpkv_status qpkv_decode_merge(const int64_t* plan_info, const void* float_ws,
                               size_t float_ws_bytes, const void* int_ws, void* o, float* lse,
                               void* stream);
+
+/* ------------------------------------------ decode without any allocation
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: code running where cudaMalloc is not
+ * allowed or not wanted (an embedding runtime that owns all device memory,
+ * a plugin with no allocator handle, a hard real-time loop that must not
+ * hit the allocator).  It runs the same paged FP8 decode as
+ * qpkv_decode_plan + qpkv_decode_run, with the same arguments minus the
+ * workspaces: the work list and the split-KV partials live in fixed arrays
+ * compiled into the library (QPKV_STATIC_INT_BYTES + QPKV_STATIC_FLOAT_BYTES
+ * of device memory per GPU, held from the first call until the process
+ * exits), and the plan is staged through a fixed host buffer.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on each device looks up the arrays' device addresses
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * outside any stream capture.  Every call reuses the same arrays: calls
+ * whose work overlaps on the GPU (different streams, or different host
+ * threads without ordering) race and corrupt each other's results; nothing
+ * in the arrays needs to start at zero (each call rewrites what it reads).
+ * Errors: as qpkv_decode_plan / qpkv_decode_run, plus QPKV_ERR_STATIC_LIMIT
+ * when the batch needs more work-list or partial-result space than the
+ * fixed arrays hold (checked on the host before any CUDA call). */
+#define QPKV_STATIC_INT_BYTES (2u << 20)    /* 2 MiB work list */
+#define QPKV_STATIC_FLOAT_BYTES (32u << 20) /* 32 MiB split-KV partials */
+
+qpkv_status qpkv_decode_static(const int32_t* seqlens_kv_host, int32_t batch_size,
+                               int32_t num_qo_heads, int32_t num_kv_heads, int32_t page_size,
+                               int32_t head_dim, int32_t num_sms, const void* q,
+                               const void* k_pool, const void* v_pool, const float* k_scale_pool,
+                               const float* v_scale_pool, int32_t num_pages,
+                               const int32_t* block_table, int32_t bt_stride, float sm_scale,
+                               void* o, float* lse, int32_t* error_word, void* stream);
 
 #ifdef __cplusplus
 }

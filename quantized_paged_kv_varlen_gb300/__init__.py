@@ -81,6 +81,8 @@ def _declare(lib):
         "qpkv_decode_attend": (_i32, [P64, _p, S, _p, _p, _p, _p, _p, _p, _i32, _i32, _p,
                                       _i32, ctypes.c_float, _p, _p]),
         "qpkv_decode_merge": (_i32, [P64, _p, S, _p, _p, _p, _p]),
+        "qpkv_decode_static": (_i32, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
+                                      _i32, _p, _i32, ctypes.c_float, _p, _p, _p, _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

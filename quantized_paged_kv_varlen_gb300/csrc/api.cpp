@@ -144,6 +144,7 @@ const char* qpkv_status_string(qpkv_status s) {
     case QPKV_ERR_CUDA: return "CUDA error";
     case QPKV_ERR_DEVICE: return "device error word set";
     case QPKV_ERR_TIMEOUT: return "device wait timed out";
+    case QPKV_ERR_STATIC_LIMIT: return "problem exceeds the fixed scratch of qpkv_decode_static";
     default: return "unknown status";
   }
 }

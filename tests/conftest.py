@@ -20,5 +20,8 @@ def lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import quantized_paged_kv_varlen_gb300 as q
+    if not os.path.exists(q.LIB_PATH):
+        from quantized_paged_kv_varlen_gb300 import build
+        build.build()
     q.load()
     return q
