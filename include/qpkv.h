@@ -197,7 +197,11 @@ qpkv_status qpkv_decode_plan(const int32_t* seqlens_kv_host, int32_t batch_size,
  * [num_pages, page_size, Hkv]; block_table: device int32 [B, bt_stride];
  * o: device bf16 [B, Hq, D]; lse: device float [B, Hq] (natural log of the
  * softmax denominator of the scaled logits) or NULL.
- * float_ws / int_ws: the workspaces given to qpkv_decode_plan (device).
+ * float_ws / int_ws: the workspaces given to qpkv_decode_plan (device).  The
+ * run also writes the int workspace: when the plan takes all kv heads per
+ * work item it holds two work counters that the attend kernel advances and
+ * re-arms before it finishes (so the same plan can be run repeatedly, in
+ * stream order).
  * A request with L_b = 0 gets O = 0 and lse = -inf.
  * qpkv_decode_run = qpkv_decode_attend (split-KV partials) followed by
  * qpkv_decode_merge (log-sum-exp merge), both on `stream`.
@@ -206,7 +210,7 @@ qpkv_status qpkv_decode_plan(const int32_t* seqlens_kv_host, int32_t batch_size,
  * qpkv_decode_plan, bt_stride too small for the longest request),
  * WORKSPACE_TOO_SMALL, CUDA. */
 qpkv_status qpkv_decode_run(const int64_t* plan_info, void* float_ws, size_t float_ws_bytes,
-                            const void* int_ws, const void* q, const void* k_pool,
+                            void* int_ws, const void* q, const void* k_pool,
                             const void* v_pool, const float* k_scale_pool,
                             const float* v_scale_pool, int32_t num_pages, int32_t page_size,
                             const int32_t* block_table, int32_t bt_stride, float sm_scale,
@@ -215,7 +219,7 @@ qpkv_status qpkv_decode_run(const int64_t* plan_info, void* float_ws, size_t flo
 /* Split-KV step alone: writes per-split partial O (float) and lse into
  * float_ws.  Same arguments as qpkv_decode_run without o / lse. */
 qpkv_status qpkv_decode_attend(const int64_t* plan_info, void* float_ws, size_t float_ws_bytes,
-                               const void* int_ws, const void* q, const void* k_pool,
+                               void* int_ws, const void* q, const void* k_pool,
                                const void* v_pool, const float* k_scale_pool,
                                const float* v_scale_pool, int32_t num_pages, int32_t page_size,
                                const int32_t* block_table, int32_t bt_stride, float sm_scale,

@@ -2,6 +2,7 @@
 // maps, and dispatch to the kernel launchers.  No exception leaves this file;
 // no allocation, free or synchronisation happens here.
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -52,8 +53,8 @@ bool supported_decode_shape(int64_t Hq, int64_t Hkv, int64_t D) {
   return (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
-// Work-item size: 512 tokens when that still gives every SM a few items,
-// else 256 or 128 so that small batches spread over the GPU.
+// Per-head work items (kind 0): 512 tokens when that still gives every SM a
+// few items, else 256 or 128 so that small batches spread over the GPU.
 int64_t pick_chunk(const int32_t* lens, int32_t B, int64_t Hkv, int32_t num_sms) {
   const int64_t sms = num_sms > 0 ? num_sms : 148;
   for (int64_t chunk : {512, 256}) {
@@ -64,17 +65,52 @@ int64_t pick_chunk(const int32_t* lens, int32_t B, int64_t Hkv, int32_t num_sms)
   return 128;
 }
 
+// All-heads work items (kind 1): the largest power-of-two number of tiles
+// (up to the kernel's register budget) that still gives every SM two items.
+int64_t pick_chunk_heads(const int32_t* lens, int32_t B, int nt, int max_tiles, int32_t num_sms) {
+  const int64_t sms = num_sms > 0 ? num_sms : 148;
+  for (int64_t tiles = max_tiles; tiles > 1; tiles /= 2) {
+    const int64_t chunk = tiles * nt;
+    int64_t items = 0;
+    for (int32_t b = 0; b < B; ++b) items += (static_cast<int64_t>(lens[b]) + chunk - 1) / chunk;
+    if (items >= 2 * sms) return chunk;
+  }
+  return nt;
+}
+
+// Whether the all-heads kernel handles this shape for some page size.
+bool heads_shape_ok(int64_t Hq, int64_t Hkv, int64_t D) {
+  int nt, bt, nb, mt;
+  return Hkv > 0 && heads_geometry(static_cast<int>(Hq), static_cast<int>(Hkv), static_cast<int>(D),
+                                   static_cast<int>(128 / Hkv), &nt, &bt, &nb, &mt);
+}
+
+// Plan layout for the given kind (0: per kv head, 1: all kv heads per item).
 void fill_plan_layout(const int32_t* lens, int32_t B, int64_t Hq, int64_t Hkv, int64_t D,
-                      int32_t num_sms, DecodePlan* p) {
+                      int32_t num_sms, int kind, DecodePlan* p) {
   std::memset(p, 0, sizeof(*p));
-  p->chunk = pick_chunk(lens, B, Hkv, num_sms);
+  p->kind = kind;
+  int64_t items_per_split = Hkv;
+  int64_t head_bytes = 0;
+  if (kind == 1) {
+    int nt, bt, nb, mt;
+    heads_geometry(static_cast<int>(Hq), static_cast<int>(Hkv), static_cast<int>(D),
+                   static_cast<int>(128 / Hkv), &nt, &bt, &nb, &mt);
+    p->chunk = pick_chunk_heads(lens, B, nt, mt, num_sms);
+    items_per_split = 1;
+    p->counter_offset = 0;
+    head_bytes = 256;   // two int32 work counters, padded
+  } else {
+    p->chunk = pick_chunk(lens, B, Hkv, num_sms);
+    p->counter_offset = -1;
+  }
   int64_t splits = 0;
   for (int32_t b = 0; b < B; ++b) splits += (static_cast<int64_t>(lens[b]) + p->chunk - 1) / p->chunk;
   p->total_splits = splits;
-  p->num_items = splits * Hkv;
-  p->items_offset = 0;
-  p->split_off_offset =
-      static_cast<int64_t>(align_up(static_cast<size_t>(p->num_items) * sizeof(DecodeItem), 256));
+  p->num_items = splits * items_per_split;
+  p->items_offset = head_bytes;
+  p->split_off_offset = static_cast<int64_t>(
+      align_up(static_cast<size_t>(head_bytes + p->num_items * sizeof(DecodeItem)), 256));
   p->int_bytes = static_cast<int64_t>(
       align_up(static_cast<size_t>(p->split_off_offset) + (B + 1) * sizeof(int32_t), 256));
   p->float_bytes = static_cast<int64_t>(align_up(
@@ -216,10 +252,17 @@ qpkv_status qpkv_decode_workspace_sizes(const int32_t* lens, int32_t B, int32_t 
                                         size_t* float_ws_bytes) {
   const qpkv_status st = check_decode_common(lens, B, Hq, Hkv, D);
   if (st != QPKV_OK) return st;
+  // the page size is not known yet: size for every layout the plan may pick
   DecodePlan p;
-  fill_plan_layout(lens, B, Hq, Hkv, D, num_sms, &p);
-  if (int_ws_bytes) *int_ws_bytes = static_cast<size_t>(p.int_bytes);
-  if (float_ws_bytes) *float_ws_bytes = static_cast<size_t>(p.float_bytes);
+  fill_plan_layout(lens, B, Hq, Hkv, D, num_sms, 0, &p);
+  size_t ib = static_cast<size_t>(p.int_bytes), fb = static_cast<size_t>(p.float_bytes);
+  if (heads_shape_ok(Hq, Hkv, D)) {
+    fill_plan_layout(lens, B, Hq, Hkv, D, num_sms, 1, &p);
+    ib = ib > static_cast<size_t>(p.int_bytes) ? ib : static_cast<size_t>(p.int_bytes);
+    fb = fb > static_cast<size_t>(p.float_bytes) ? fb : static_cast<size_t>(p.float_bytes);
+  }
+  if (int_ws_bytes) *int_ws_bytes = ib;
+  if (float_ws_bytes) *float_ws_bytes = fb;
   return QPKV_OK;
 }
 
@@ -230,25 +273,41 @@ qpkv_status qpkv_decode_plan_host(const int32_t* lens, int32_t B, int32_t Hq, in
   if (st != QPKV_OK) return st;
   if (host_int_ws == nullptr || plan_info == nullptr) return QPKV_ERR_INVALID_ARG;
   if (!page_size_ok(page_size)) return QPKV_ERR_UNSUPPORTED;
+  int nt, bt, nb, mt;
+  const int kind = heads_geometry(Hq, Hkv, D, page_size, &nt, &bt, &nb, &mt) ? 1 : 0;
   DecodePlan p;
-  fill_plan_layout(lens, B, Hq, Hkv, D, num_sms, &p);
+  fill_plan_layout(lens, B, Hq, Hkv, D, num_sms, kind, &p);
   p.page_size = page_size;
   if (host_int_bytes < static_cast<size_t>(p.int_bytes)) return QPKV_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* base = static_cast<uint8_t*>(host_int_ws);
   DecodeItem* items = reinterpret_cast<DecodeItem*>(base + p.items_offset);
   int32_t* split_off = reinterpret_cast<int32_t*>(base + p.split_off_offset);
-  // items of one token range are adjacent across kv heads, so the CTAs that
-  // share the per-token scale sectors run together
   int64_t n = 0, s = 0;
   for (int32_t b = 0; b < B; ++b) {
     split_off[b] = static_cast<int32_t>(s);
     for (int64_t t0 = 0; t0 < lens[b]; t0 += p.chunk, ++s) {
       const int32_t t1 = static_cast<int32_t>(t0 + p.chunk < lens[b] ? t0 + p.chunk : lens[b]);
-      for (int32_t h = 0; h < Hkv; ++h)
-        items[n++] = DecodeItem{b, h, static_cast<int32_t>(t0), t1, static_cast<int32_t>(s), 0, 0, 0};
+      if (kind == 1) {
+        items[n++] = DecodeItem{b, 0, static_cast<int32_t>(t0), t1, static_cast<int32_t>(s), 0, 0, 0};
+      } else {
+        // items of one token range are adjacent across kv heads, so the CTAs
+        // that share the per-token scale sectors run together
+        for (int32_t h = 0; h < Hkv; ++h)
+          items[n++] = DecodeItem{b, h, static_cast<int32_t>(t0), t1, static_cast<int32_t>(s), 0, 0, 0};
+      }
     }
   }
   split_off[B] = static_cast<int32_t>(s);
+  if (kind == 1) {
+    // taken from a shared counter, largest first: full chunks, then the
+    // partial last chunks of the requests from long to short
+    std::stable_sort(items, items + n, [](const DecodeItem& x, const DecodeItem& y) {
+      return (x.t1 - x.t0) > (y.t1 - y.t0);
+    });
+    int32_t* counters = reinterpret_cast<int32_t*>(base + p.counter_offset);
+    counters[0] = 0;
+    counters[1] = 0;
+  }
   std::memset(plan_info, 0, QPKV_PLAN_INFO_LEN * sizeof(int64_t));
   std::memcpy(plan_info, &p, sizeof(p));
   return QPKV_OK;
@@ -272,7 +331,7 @@ qpkv_status qpkv_decode_plan(const int32_t* lens, int32_t B, int32_t Hq, int32_t
 }
 
 qpkv_status qpkv_decode_attend(const int64_t* plan_info, void* float_ws, size_t float_ws_bytes,
-                               const void* int_ws, const void* q, const void* k_pool,
+                               void* int_ws, const void* q, const void* k_pool,
                                const void* v_pool, const float* k_scale_pool,
                                const float* v_scale_pool, int32_t num_pages, int32_t page_size,
                                const int32_t* block_table, int32_t bt_stride, float sm_scale,
@@ -308,7 +367,7 @@ qpkv_status qpkv_decode_merge(const int64_t* plan_info, const void* float_ws,
 }
 
 qpkv_status qpkv_decode_run(const int64_t* plan_info, void* float_ws, size_t float_ws_bytes,
-                            const void* int_ws, const void* q, const void* k_pool,
+                            void* int_ws, const void* q, const void* k_pool,
                             const void* v_pool, const float* k_scale_pool,
                             const float* v_scale_pool, int32_t num_pages, int32_t page_size,
                             const int32_t* block_table, int32_t bt_stride, float sm_scale,

@@ -709,7 +709,7 @@ cudaError_t launch_attend_t(const CUtensorMap& km, const CUtensorMap& vm, const 
 
 }  // namespace
 
-cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, const void* int_ws,
+cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, void* int_ws,
                                  const void* q, const void* k_pool, const void* v_pool,
                                  const float* k_scale_pool, const float* v_scale_pool,
                                  int num_pages, int page_size, const int32_t* block_table,
@@ -717,6 +717,10 @@ cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, const 
                                  cudaStream_t stream, int* status) {
   *status = QPKV_OK;
   if (plan.num_items == 0) return cudaSuccess;
+  if (plan.kind == 1)
+    return launch_decode_heads(plan, float_ws, int_ws, q, k_pool, v_pool, k_scale_pool,
+                               v_scale_pool, num_pages, page_size, block_table, bt_stride, sm_scale,
+                               error_word, stream, status);
   const int D = static_cast<int>(plan.head_dim);
   const int Hkv = static_cast<int>(plan.num_kv_heads);
   const int G = static_cast<int>(plan.num_qo_heads / plan.num_kv_heads);

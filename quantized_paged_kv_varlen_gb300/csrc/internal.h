@@ -31,6 +31,8 @@ struct DecodePlan {
   int64_t head_dim;
   int64_t page_size;
   int64_t max_len;   // longest request; block_table rows must cover it
+  int64_t kind;      // 0: one kv head per work item, 1: all kv heads per work item
+  int64_t counter_offset;  // kind 1: bytes into the int workspace of 2 int32 work counters
   int64_t magic;
 };
 constexpr int64_t kPlanMagic = 0x71706b76706c616eLL;  // "qpkvplan"
@@ -40,12 +42,22 @@ cudaError_t launch_rope_table(float theta, float rope_scale, int max_pos, int ro
 
 cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream);
 
-cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, const void* int_ws,
+cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, void* int_ws,
                                  const void* q, const void* k_pool, const void* v_pool,
                                  const float* k_scale_pool, const float* v_scale_pool,
                                  int num_pages, int page_size, const int32_t* block_table,
                                  int bt_stride, float sm_scale, int32_t* error_word,
                                  cudaStream_t stream, int* status);
+
+// All-heads decode (decode_heads.cu): geometry check and launcher.
+bool heads_geometry(int Hq, int Hkv, int D, int page_size, int* nt, int* bt, int* nb,
+                    int* max_tiles);
+cudaError_t launch_decode_heads(const DecodePlan& plan, float* float_ws, void* int_ws,
+                                const void* q, const void* k_pool, const void* v_pool,
+                                const float* k_scale_pool, const float* v_scale_pool,
+                                int num_pages, int page_size, const int32_t* block_table,
+                                int bt_stride, float sm_scale, int32_t* error_word,
+                                cudaStream_t stream, int* status);
 
 cudaError_t launch_decode_merge(const DecodePlan& plan, const float* float_ws, const void* int_ws,
                                 void* o, float* lse, cudaStream_t stream);

@@ -56,29 +56,35 @@ def _plan(lib, lens, Hq=32, Hkv=8, ps=16, D=128, sms=148):
                                    host.ctypes.data, host.nbytes, info)
     assert st == 0
     n_items, chunk, total_splits, items_off, split_off_off = (info[i] for i in range(5))
+    int_bytes, float_bytes, kind, counter_off = info[5], info[6], info[13], info[14]
+    assert int_bytes <= ib.value and float_bytes <= fb.value
     items = host[items_off:items_off + 32 * n_items].view(np.int32).reshape(n_items, 8)
     split_off = host[split_off_off:split_off_off + 4 * (len(lens) + 1)].view(np.int32)
-    return dict(info=list(info), items=items, split_off=split_off, chunk=chunk,
-                total_splits=total_splits, float_bytes=fb.value)
+    counters = host[counter_off:counter_off + 8].view(np.int32) if kind == 1 else None
+    return dict(info=list(info), items=items, split_off=split_off, chunk=chunk, kind=kind,
+                total_splits=total_splits, float_bytes=fb.value, counters=counters)
 
 
-def test_decode_plan_covers_every_token_once(qlib):
+@pytest.mark.parametrize("Hq,Hkv,kind", [(64, 8, 0), (8, 2, 1)])
+def test_decode_plan_covers_every_token_once(qlib, Hq, Hkv, kind):
     _, lib = qlib
     rng = np.random.default_rng(0)
     lens = rng.integers(0, 3000, 40)
     lens[[3, 7]] = 0
     lens[5] = 256
     lens[6] = 257
-    p = _plan(lib, lens, Hq=8, Hkv=2)
+    p = _plan(lib, lens, Hq=Hq, Hkv=Hkv)
+    assert p["kind"] == kind
     chunk = p["chunk"]
-    assert chunk in (128, 256, 512)
+    heads = Hkv if kind == 0 else 1
     cover = {}
     for b, h, t0, t1, slot, *_ in p["items"].tolist():
         assert 0 <= t0 < t1 <= lens[b] and t1 - t0 <= chunk and t0 % chunk == 0
         assert slot == p["split_off"][b] + t0 // chunk
+        assert 0 <= h < heads
         cover.setdefault((b, h), []).append((t0, t1))
     for b, L in enumerate(lens):
-        for h in range(2):
+        for h in range(heads):
             spans = sorted(cover.get((b, h), []))
             assert sum(t1 - t0 for t0, t1 in spans) == L
             for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
@@ -86,18 +92,25 @@ def test_decode_plan_covers_every_token_once(qlib):
     splits = [(L + chunk - 1) // chunk for L in lens]
     assert p["split_off"].tolist() == np.concatenate([[0], np.cumsum(splits)]).tolist()
     assert p["total_splits"] == sum(splits)
-    # items of one token range are adjacent across kv heads
     it = p["items"]
-    assert np.all(it[0::2, 1] == 0) and np.all(it[1::2, 1] == 1)
-    assert np.array_equal(it[0::2, [0, 2]], it[1::2, [0, 2]])
-    assert p["float_bytes"] >= sum(splits) * 8 * 129 * 4
+    if kind == 0:
+        # items of one token range are adjacent across kv heads
+        assert np.all(it[0::Hkv, 1] == 0) and np.all(it[1::Hkv, 1] == 1)
+        assert np.array_equal(it[0::Hkv, [0, 2]], it[1::Hkv, [0, 2]])
+    else:
+        # one item per token range, handed out largest first, counters armed
+        sizes = it[:, 3] - it[:, 2]
+        assert np.all(np.diff(sizes) <= 0)
+        assert p["counters"].tolist() == [0, 0]
+    assert p["float_bytes"] >= sum(splits) * Hq * 129 * 4
 
 
 def test_small_batches_use_smaller_items(qlib):
     _, lib = qlib
     assert _plan(lib, [37, 100], Hq=4, Hkv=1, D=64)["chunk"] == 128
-    assert _plan(lib, [4000] * 64)["chunk"] == 512
-    assert _plan(lib, [300] * 64, sms=148)["chunk"] == 256
+    assert _plan(lib, [4000] * 64)["chunk"] == 256              # all heads: 16 tiles of 16 tokens
+    assert _plan(lib, [4000] * 64, Hq=64)["chunk"] == 512       # per kv head
+    assert _plan(lib, [300] * 64, Hq=64, sms=148)["chunk"] == 256
 
 
 @pytest.mark.parametrize("args,want", [

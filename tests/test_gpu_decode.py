@@ -127,6 +127,8 @@ def test_decode_tiny_gqa4_d64(lib):
     ([513, 200], 128, 8, 8, 128),
     ([700, 33, 256], 256, 16, 2, 128),
     ([1200, 5], 16, 32, 8, 128),
+    ([900, 130, 17], 16, 64, 8, 128),       # 3*Hq > 96: one kv head per work item
+    ([777, 64], 32, 16, 8, 128),            # a tile is half a page of 32
 ])
 def test_decode_edge_shapes(lib, lengths, ps, Hq, Hkv, D):
     rng = np.random.default_rng(11)
