@@ -317,6 +317,11 @@ class DecodePlan:
     def total_splits(self):
         return int(self.plan_info[2])
 
+    @property
+    def kind(self):
+        """0: one kv head per work item, 1: all kv heads of a token range."""
+        return int(self.plan_info[13])
+
     def _check_run(self, q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table):
         torch = _torch()
         _need(q, "q", torch.bfloat16, 3)

@@ -155,6 +155,11 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
                : "memory");
 }
 
+// Wait until every cp.async this thread issued has landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");

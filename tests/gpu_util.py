@@ -1,9 +1,12 @@
 """Shared helpers of the GPU parity tests: tolerances and comparisons."""
 import numpy as np
 
-# Attention output against the float64 oracle: max-abs and relative L2 with
-# P in bf16 / fp32 (the FP8-P bound is looser); LSE absolute.
-ATOL_MAX = 1e-2
+# Attention output against the float64 oracle: elementwise |got - want| <=
+# ATOL_MAX + BF16_REL * |want| (a bf16 output carries 8 significant bits, so
+# rounding alone moves it by up to 2^-8 of its magnitude) and relative L2
+# with P in bf16 / fp32 (the FP8-P bound is looser); LSE absolute.
+ATOL_MAX = 2e-3
+BF16_REL = 2.0 ** -8
 REL_L2 = 5e-3
 REL_L2_FP8_P = 2e-2
 LSE_ATOL = 1e-3
@@ -27,9 +30,11 @@ def assert_attention_close(got, want, rel=REL_L2, atol=ATOL_MAX, what="O"):
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
-    err = float(np.max(np.abs(got - want))) if got.size else 0.0
+    excess = np.abs(got - want) - BF16_REL * np.abs(want)
+    err = float(np.max(excess)) if got.size else 0.0
     r = rel_l2(got, want)
-    assert err <= atol and r <= rel, f"{what}: max-abs {err:.3e} (<= {atol}), rel-L2 {r:.3e} (<= {rel})"
+    assert err <= atol and r <= rel, (
+        f"{what}: max(|err| - 2^-8 |want|) {err:.3e} (<= {atol}), rel-L2 {r:.3e} (<= {rel})")
 
 
 def assert_lse_close(got, want, atol=LSE_ATOL):

@@ -65,7 +65,7 @@ def _plan(lib, lens, Hq=32, Hkv=8, ps=16, D=128, sms=148):
                 total_splits=total_splits, float_bytes=fb.value, counters=counters)
 
 
-@pytest.mark.parametrize("Hq,Hkv,kind", [(64, 8, 0), (8, 2, 1)])
+@pytest.mark.parametrize("Hq,Hkv,kind", [(64, 8, 0), (8, 2, 0), (16, 4, 1), (32, 8, 1)])
 def test_decode_plan_covers_every_token_once(qlib, Hq, Hkv, kind):
     _, lib = qlib
     rng = np.random.default_rng(0)
@@ -73,7 +73,7 @@ def test_decode_plan_covers_every_token_once(qlib, Hq, Hkv, kind):
     lens[[3, 7]] = 0
     lens[5] = 256
     lens[6] = 257
-    p = _plan(lib, lens, Hq=Hq, Hkv=Hkv)
+    p = _plan(lib, lens, Hq=Hq, Hkv=Hkv, ps=32)
     assert p["kind"] == kind
     chunk = p["chunk"]
     heads = Hkv if kind == 0 else 1

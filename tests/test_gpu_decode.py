@@ -68,8 +68,8 @@ def _u32(a):
     return np.ascontiguousarray(a).view(np.uint32)
 
 
-def _check_decode(lib, wl, reqs=None, check_pool_bytes=True):
-    k, v = wl.kv_all()
+def _check_decode(lib, wl, reqs=None, check_pool_bytes=True, kv=None):
+    k, v = wl.kv_all() if kv is None else kv
     d = _dev_inputs(lib, wl, k, v)
     plan = lib.DecodePlan(wl.lengths, wl.Hq, wl.Hkv, wl.page_size, wl.D)
     q = torch.from_numpy(wl.q).cuda().to(torch.bfloat16)
@@ -120,17 +120,21 @@ def test_decode_tiny_gqa4_d64(lib):
     _check_decode(lib, synth.tiny_decode(0))
 
 
-@pytest.mark.parametrize("lengths,ps,Hq,Hkv,D", [
-    ([0, 1, 127, 128, 129], 16, 4, 1, 64),
-    ([255, 256, 257, 1000, 3], 32, 8, 1, 128),
-    ([300, 64, 17], 64, 8, 2, 128),
-    ([513, 200], 128, 8, 8, 128),
-    ([700, 33, 256], 256, 16, 2, 128),
-    ([1200, 5], 16, 32, 8, 128),
-    ([900, 130, 17], 16, 64, 8, 128),       # 3*Hq > 96: one kv head per work item
-    ([777, 64], 32, 16, 8, 128),            # a tile is half a page of 32
+@pytest.mark.parametrize("lengths,ps,Hq,Hkv,D,kind", [
+    ([0, 1, 127, 128, 129], 16, 4, 1, 64, 0),
+    ([255, 256, 257, 1000, 3], 32, 8, 1, 128, 0),
+    ([300, 64, 17], 64, 8, 2, 128, 0),
+    ([513, 200], 128, 8, 8, 128, 1),
+    ([700, 33, 256], 256, 16, 2, 128, 0),
+    ([1200, 5], 16, 32, 8, 128, 1),
+    ([900, 130, 17], 16, 64, 8, 128, 0),       # 3*Hq > 96: one kv head per work item
+    ([777, 64], 32, 16, 8, 128, 1),            # a tile is half a page of 32
+    ([300, 64, 17, 1], 32, 16, 4, 128, 1),     # 4 kv heads: 32-token tiles
+    ([1000, 33], 64, 32, 4, 64, 1),            # 8 query heads per kv head, D = 64
+    ([129, 16, 1, 250], 16, 8, 8, 64, 1),
+    ([600, 31], 16, 16, 4, 128, 0),            # 32-token tiles would cross 16-token pages
 ])
-def test_decode_edge_shapes(lib, lengths, ps, Hq, Hkv, D):
+def test_decode_edge_shapes(lib, lengths, ps, Hq, Hkv, D, kind):
     rng = np.random.default_rng(11)
     lengths = np.asarray(lengths, dtype=np.int32)
     bt, P = synth.page_tables(rng, lengths, ps, extra_pages=3)
@@ -138,19 +142,44 @@ def test_decode_edge_shapes(lib, lengths, ps, Hq, Hkv, D):
                               lengths=lengths, block_table=bt, num_pages=P,
                               q=synth.bf16_normal(rng, (len(lengths), Hq, D)),
                               scale=1.0 / np.sqrt(D), workload_id=9)
-    _check_decode(lib, wl)
+    _, plan = _check_decode(lib, wl)
+    assert plan.kind == kind
 
 
-def test_decode_large_magnitudes_and_constant_keys(lib):
-    """Scaled queries (large logits) and a request whose keys are all equal."""
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 8), (16, 4)])
+def test_decode_large_magnitudes(lib, Hq, Hkv):
+    """Queries scaled by 8: logits spread over many octaves."""
     rng = np.random.default_rng(12)
     lengths = np.array([400, 260], dtype=np.int32)
-    bt, P = synth.page_tables(rng, lengths, 16)
-    q = synth.bf16_round(synth.bf16_normal(rng, (2, 8, 128)) * 8.0)
-    wl = synth.DecodeWorkload(seed=12, B=2, Hq=8, Hkv=2, D=128, page_size=16, lengths=lengths,
+    ps = 32 if Hkv == 4 else 16
+    bt, P = synth.page_tables(rng, lengths, ps)
+    q = synth.bf16_round(synth.bf16_normal(rng, (2, Hq, 128)) * 8.0)
+    wl = synth.DecodeWorkload(seed=12, B=2, Hq=Hq, Hkv=Hkv, D=128, page_size=ps, lengths=lengths,
                               block_table=bt, num_pages=P, q=q, scale=1.0 / np.sqrt(128.0),
                               workload_id=8)
     _check_decode(lib, wl)
+
+
+@pytest.mark.parametrize("Hq,Hkv,ps", [(32, 8, 16), (16, 4, 32), (8, 2, 16)])
+def test_decode_running_max_jumps(lib, Hq, Hkv, ps):
+    """Keys grow 6x from token 100 on, inside the first work item: later
+    tiles beat the running maximum by far more than 2^8, so the kernels
+    must rescale what they have already accumulated."""
+    rng = np.random.default_rng(14)
+    lengths = np.array([700, 300], dtype=np.int32)
+    bt, P = synth.page_tables(rng, lengths, ps)
+    wl = synth.DecodeWorkload(seed=14, B=2, Hq=Hq, Hkv=Hkv, D=128, page_size=ps,
+                              lengths=lengths, block_table=bt, num_pages=P,
+                              q=synth.bf16_normal(rng, (2, Hq, 128)), scale=1.0 / np.sqrt(128.0),
+                              workload_id=6)
+    k, v = wl.kv_all()
+    first = np.concatenate([[0], np.cumsum(lengths)[:-1]])
+    grow = np.zeros(k.shape[0], dtype=bool)
+    for b, L in enumerate(lengths):
+        grow[first[b] + 100:first[b] + L] = True
+    k = k.copy()
+    k[grow] = synth.bf16_round(k[grow] * 6.0)
+    _check_decode(lib, wl, kv=(k, v))
 
 
 def test_decode_bad_page_sets_error_word(lib):
