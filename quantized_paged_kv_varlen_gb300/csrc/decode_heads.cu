@@ -52,9 +52,10 @@ namespace qpkv {
 namespace {
 
 constexpr int kTile = 128;        // (kv head, token) rows per tile = MMA M
-constexpr int kThreads = 224;     // 7 warps
+constexpr int kThreads = 352;     // 11 warps
 constexpr int kWarpItems = 0, kWarpStream = 1, kWarpMma = 2;
-constexpr int kSoftmax = 128;     // warps 3..6
+constexpr int kSoftmax = 128;     // warps 3..6 (softmax), 7..10 (epilogue)
+constexpr int kWarpEpi0 = 7;
 constexpr int kMaxStages = 16;
 constexpr int kMaxTilesItem = 16;
 constexpr int kSBufs = 2;         // S accumulators in TMEM
@@ -72,7 +73,7 @@ struct HCfg {
   static constexpr int kPBytes = kTile * kTile;                   // 128 rows x 128 tile rows
   static constexpr int kScaleBytes = kMaxTilesItem * kTile * 4;   // one item's k- or v-scales
   static constexpr int kFixed = 2 * kQTBytes + kPBufs * kPBytes + 4 * kScaleBytes;
-  static constexpr int kBudget = 222 * 1024;   // + ~1 KB static shared state
+  static constexpr int kBudget = 221 * 1024;   // + ~3.2 KB static shared state
   static constexpr int kStagesRaw = (kBudget - kFixed) / kTileBytes;
   static constexpr int kStages = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kOffQT = kStages * kTileBytes;
@@ -83,7 +84,7 @@ struct HCfg {
   static constexpr int kSmem = kBytes + 1024;
   static constexpr int kOCol0 = kSBufs * kMaxN;   // first O column in TMEM
   static_assert(kStages >= 6, "ring too small");
-  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(kSmem + 4096 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(kOCol0 + kOBufs * D <= 512, "TMEM");
 };
 
@@ -119,10 +120,14 @@ struct HShared {
   uint64_t p_ready[kPBufs], p_free[kPBufs];
   uint64_t o_full[kOBufs], o_free[kOBufs];
   uint64_t mma_done;
+  uint64_t ep_ready[2];      // item's O scales written, O may be read once complete
   DecodeItem desc[2];
   int tab[2][kMaxTilesItem];   // pool row of each tile's box, -1 if its page is bad
   float sig_q[2][32];          // query term scale per query head
   float sig_p[2][32];          // probability term scale per query head
+  float ep_scale[2][kTile];   // per O row: sig_p / softmax denominator
+  float ep_lse[2][kTile];     // per O row: natural-log LSE
+  int ep_slot[2];             // partial-output slot, -1: stop
   uint32_t tmem_base;
   int abort;
 };
@@ -170,14 +175,18 @@ __device__ __forceinline__ int htiles(const DecodeItem& it, int nt) {
   return (it.t1 - it.t0 + nt - 1) / nt;
 }
 
-// Three-term E4M3 split of x with term scales s1, s1/16, s1/256.
-__device__ __forceinline__ void hsplit3(float x, float inv1, float s1, uint8_t& c1, uint8_t& c2,
-                                       uint8_t& c3) {
-  c1 = f32_to_e4m3(x * inv1);
-  const float r1 = fmaf(-e4m3_to_f32(c1), s1, x);
-  c2 = f32_to_e4m3(r1 * inv1 * 16.0f);
-  const float r2 = fmaf(-e4m3_to_f32(c2), s1 * (1.0f / 16.0f), r1);
-  c3 = f32_to_e4m3(r2 * inv1 * 256.0f);
+// Three-term E4M3 split with term scales s1, s1/16, s1/256, for a pair
+// of values (codes: low byte = x0).
+__device__ __forceinline__ void hsplit3x2(float x0, float x1, float inv1, float s1, uint16_t& c1,
+                                         uint16_t& c2, uint16_t& c3) {
+  c1 = f32x2_to_e4m3x2(x1 * inv1, x0 * inv1);
+  const float2 d1 = e4m3x2_to_f32x2(c1);
+  const float r0 = fmaf(-d1.x, s1, x0), r1 = fmaf(-d1.y, s1, x1);
+  c2 = f32x2_to_e4m3x2(r1 * inv1 * 16.0f, r0 * inv1 * 16.0f);
+  const float2 d2 = e4m3x2_to_f32x2(c2);
+  const float s16 = s1 * (1.0f / 16.0f);
+  const float q0 = fmaf(-d2.x, s16, r0), q1 = fmaf(-d2.y, s16, r1);
+  c3 = f32x2_to_e4m3x2(q1 * inv1 * 256.0f, q0 * inv1 * 256.0f);
 }
 
 // Row of the P operand / O accumulator that holds (query head qh, term):
@@ -227,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.o_full[b], 1);
       mbar_init(&sh.o_free[b], kSoftmax);
     }
+    for (int d = 0; d < 2; ++d) mbar_init(&sh.ep_ready[d], kSoftmax);
     mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
     fence_mbar_init();
@@ -322,14 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int half = 0; half < 2; ++half) {
             uint32_t p1 = 0, p2 = 0, p3 = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t word = w[2 * half + i / 2];
-              const uint16_t bits = static_cast<uint16_t>((i & 1) ? (word >> 16) : (word & 0xFFFFu));
-              uint8_t c1, c2, c3;
-              hsplit3(bf16_bits_to_float(bits), inv1, s1, c1, c2, c3);
-              p1 |= static_cast<uint32_t>(c1) << (8 * i);
-              p2 |= static_cast<uint32_t>(c2) << (8 * i);
-              p3 |= static_cast<uint32_t>(c3) << (8 * i);
+            for (int pr = 0; pr < 2; ++pr) {
+              const uint32_t word = w[2 * half + pr];
+              uint16_t c1, c2, c3;
+              hsplit3x2(bf16_bits_to_float(static_cast<uint16_t>(word & 0xFFFFu)),
+                        bf16_bits_to_float(static_cast<uint16_t>(word >> 16)), inv1, s1, c1, c2, c3);
+              p1 |= static_cast<uint32_t>(c1) << (16 * pr);
+              p2 |= static_cast<uint32_t>(c2) << (16 * pr);
+              p3 |= static_cast<uint32_t>(c3) << (16 * pr);
             }
             const int k = d0 + e + 4 * half;
             *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0, k, D)) = p1;
@@ -548,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(&sh.mma_done, 0, a.err);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------- softmax / epilogue
+  } else if (warp < kWarpEpi0) {
+    // ---------------------------------------------------------- softmax
     constexpr int kG3 = 3 * G;
     const int sw = warp & 3;                  // TMEM lane quarter
     const int tl = sw * 32 + lane;            // tile row = S lane
@@ -561,24 +571,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sidx = my_t * Hkv + my_h;       // [token][head] scale index within a tile
     const int sel = my_h % hpw;
     const int w_h0 = sw * hpw;
-    // this lane's O row: (query head qh_o, term term_o) when lane < 3 * qpw
+    // this lane's O row: (query head qh_o, term) when lane < 3 * qpw
     const bool o_lane = lane < 3 * qpw;
     const int qh_o = o_lane ? sw * qpw + lane / 3 : 0;
-    const int term_o = lane % 3;
     const int g_o = qh_o % G;
     const int src_o = ((qh_o / G) % hpw) * nt;   // first S lane of qh_o's kv head
+    // byte offsets of this row's entries in the P tile: (query head g, term)
+    int poff[kG3];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int t = 0; t < 3; ++t)
+        poff[3 * g + t] = static_cast<int>(swizzled_offset(o_row(my_h * G + g, t, qpw), tl, 128));
     int st = 0, pt = 0;
     for (int o = 0;; ++o) {
       const int d = o & 1;
       if (!warp_wait(&sh.desc_full[d], (o >> 1) & 1, sh, a.err, lane)) break;
       const DecodeItem cur = sh.desc[d];
-      if (cur.b < 0) break;
+      if (cur.b < 0) {
+        // tell the epilogue warps to stop, once they are done with item o-2
+        hwait(&sh.o_free[d], ((o >> 1) & 1) ^ 1, sh, a.err);
+        if (tl == 0) sh.ep_slot[d] = -1;
+        mbar_arrive(&sh.ep_ready[d]);
+        break;
+      }
       const int ntl = htiles(cur, nt);
       float sq[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) sq[g] = sh.sig_q[d][my_h * G + g] * a.sm_scale_log2;
       const float sp = sh.sig_p[d][my_h * G];
       const float spinv = sp > 0.f ? 1.0f / sp : 0.f;
+      const float spo = o_lane ? sh.sig_p[d][qh_o] : 0.f;
       const float* ksb = sKS + d * (kMaxTilesItem * kTile);
       const float* vsb = sVS + d * (kMaxTilesItem * kTile);
       float m_run[G], lpart[G];
@@ -610,13 +633,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float sdot = v0 + v1 * (1.0f / 16.0f) + v2 * (1.0f / 256.0f);
           l[g] = valid ? ks * sq[g] * sdot : -INFINITY;
         }
+        // tile maximum per query head over the nt lanes of this kv head
+        float tmx[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) tmx[g] = l[g];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          if (off < nt) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              tmx[g] = fmaxf(tmx[g], __shfl_xor_sync(0xffffffffu, tmx[g], off));
+          }
+        }
         // ---- running maximum per query head (moved only by more than 2^8)
         bool need = false;
         float fac[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float x = l[g];
-          for (int off = 1; off < nt; off <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+          const float x = tmx[g];
           fac[g] = 1.f;
           if (x > m_run[g] + kRescaleLog2) {
             if (m_run[g] > -INFINITY) {
@@ -658,18 +692,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before_sync();
         }
         // ---- P' = p * v-scale, three E4M3 terms, into the block-diagonal P
+        uint8_t c[kG3];
+#pragma unroll
+        for (int g = 0; g + 1 < G; g += 2) {
+          uint16_t c1, c2, c3;
+          hsplit3x2(p[g] * vs, p[g + 1] * vs, spinv, sp, c1, c2, c3);
+          c[3 * g] = c1 & 0xFF;
+          c[3 * g + 1] = c2 & 0xFF;
+          c[3 * g + 2] = c3 & 0xFF;
+          c[3 * g + 3] = c1 >> 8;
+          c[3 * g + 4] = c2 >> 8;
+          c[3 * g + 5] = c3 >> 8;
+        }
+        if (G & 1) {
+          uint16_t c1, c2, c3;
+          hsplit3x2(p[G - 1] * vs, 0.f, spinv, sp, c1, c2, c3);
+          c[kG3 - 3] = c1 & 0xFF;
+          c[kG3 - 2] = c2 & 0xFF;
+          c[kG3 - 1] = c3 & 0xFF;
+        }
         const int pb = pt % kPBufs;
         hwait(&sh.p_free[pb], ((pt / kPBufs) & 1) ^ 1, sh, a.err);
         uint8_t* dst = sP + pb * C::kPBytes;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          uint8_t c1, c2, c3;
-          hsplit3(p[g] * vs, spinv, sp, c1, c2, c3);
-          const int r0 = o_row(my_h * G + g, 0, qpw);
-          dst[swizzled_offset(r0, tl, 128)] = c1;
-          dst[swizzled_offset(r0 + 1, tl, 128)] = c2;
-          dst[swizzled_offset(r0 + 2, tl, 128)] = c3;
-        }
+        for (int i = 0; i < kG3; ++i) dst[poff[i]] = c[i];
         fence_proxy_async_smem();
         mbar_arrive(&sh.p_ready[pb]);
         ++pt;
@@ -679,50 +725,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float x = lpart[g];
-        for (int off = 1; off < nt; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-        const float tl_sum = __shfl_sync(0xffffffffu, x, src_o);
-        const float tl_max = __shfl_sync(0xffffffffu, m_run[g], src_o);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1)
+          if (off < nt) x += __shfl_xor_sync(0xffffffffu, x, off);
+        const float hsum = __shfl_sync(0xffffffffu, x, src_o);
+        const float hmax = __shfl_sync(0xffffffffu, m_run[g], src_o);
         if (g == g_o) {
-          lo = tl_sum;
-          mo = tl_max;
+          lo = hsum;
+          mo = hmax;
         }
       }
-      const float spo = o_lane ? sh.sig_p[d][qh_o] : 0.f;
+      // hand the item to the epilogue warps (after they finished item o-2)
+      hwait(&sh.o_free[d], ((o >> 1) & 1) ^ 1, sh, a.err);
+      sh.ep_scale[d][tl] = lo > 0.f ? spo / lo : 0.f;
+      sh.ep_lse[d][tl] = lo > 0.f ? (mo + log2f(lo)) * kLn2 : -INFINITY;
+      if (tl == 0) sh.ep_slot[d] = cur.slot;
       mbar_arrive(&sh.desc_free[d]);   // done with the item's scales and descriptor
-      // ---- epilogue: O rows -> fp32 partial output (terms combined) and lse
+      mbar_arrive(&sh.ep_ready[d]);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    // O rows -> fp32 partial output (terms combined) and lse, overlapping
+    // the softmax of the next item
+    const int sw = warp & 3;
+    const int tl = sw * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+    const int qpw = Hq / 4;
+    const bool o_lane = lane < 3 * qpw;
+    const int qh_o = o_lane ? sw * qpw + lane / 3 : 0;
+    const bool writer = o_lane && lane % 3 == 0;
+    for (int o = 0;; ++o) {
+      const int d = o & 1;
+      if (!warp_wait(&sh.ep_ready[d], (o >> 1) & 1, sh, a.err, lane)) break;
+      const int slot = sh.ep_slot[d];
+      if (slot < 0) break;
+      const float so = sh.ep_scale[d][tl];
+      const float lse = sh.ep_lse[d][tl];
       hwait(&sh.o_full[d], (o >> 1) & 1, sh, a.err);
       tc_fence_after_sync();
-      const float so = lo > 0.f ? spo / lo : 0.f;
-      const bool writer = o_lane && term_o == 0;
-      float* out = a.part_o + (static_cast<size_t>(cur.slot) * Hq + qh_o) * D;
+      float* out = a.part_o + (static_cast<size_t>(slot) * Hq + qh_o) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + C::kOCol0 + d * D + 16 * c, v);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::kOCol0 + d * D + 32 * c, v);
         tmem_ld_wait();
-        float y[16];
+        float y[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           const float x0 = __uint_as_float(v[i]);
           const float x1 = __shfl_down_sync(0xffffffffu, x0, 1);
           const float x2 = __shfl_down_sync(0xffffffffu, x0, 2);
           y[i] = (x0 + x1 * (1.0f / 16.0f) + x2 * (1.0f / 256.0f)) * so;
         }
         if (writer) {
-          float4* o4 = reinterpret_cast<float4*>(out + 16 * c);
+          float4* o4 = reinterpret_cast<float4*>(out + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 8; ++i)
             o4[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
         }
       }
       tc_fence_before_sync();
       mbar_arrive(&sh.o_free[d]);
-      if (writer)
-        a.part_lse[static_cast<size_t>(cur.slot) * Hq + qh_o] =
-            lo > 0.f ? (mo + log2f(lo)) * kLn2 : -INFINITY;
+      if (writer) a.part_lse[static_cast<size_t>(slot) * Hq + qh_o] = lse;
     }
   }
-
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kWarpMma) {
