@@ -189,6 +189,47 @@ __device__ __forceinline__ void hsplit3x2(float x0, float x1, float inv1, float 
   c3 = f32x2_to_e4m3x2(q1 * inv1 * 256.0f, q0 * inv1 * 256.0f);
 }
 
+// Ring order shared by the stream warp, which fills the stages, and the MMA
+// warp, which consumes them in the same order: K tiles run up to two tiles
+// ahead of V tiles (QK(t+2) needs only S(t) read, not P(t) written) and at
+// most one work item ahead.
+struct RingSched {
+  int ko, kj, vo, vj, lead;
+  int ntl0, ntl1;   // tiles of the items in flight, by parity
+  bool kdone;
+  __device__ __forceinline__ int ntl(int o) const { return (o & 1) ? ntl1 : ntl0; }
+  __device__ __forceinline__ void set_ntl(int o, int n) {
+    if (o & 1) ntl1 = n; else ntl0 = n;
+  }
+};
+enum : int { kStepK = 0, kStepV = 1, kStepDone = 2, kStepFail = 3 };
+
+// open(o) waits until item o is published and returns its tile count, 0 at
+// the end of the work, -1 on failure.
+template <class Open>
+__device__ __forceinline__ int ring_next(RingSched& q, Open&& open) {
+  if (q.vj == q.ntl(q.vo) && q.vo < q.ko) {
+    ++q.vo;
+    q.vj = 0;
+  }
+  if (!q.kdone && q.lead < 2) {
+    if (q.kj < q.ntl(q.ko)) return kStepK;
+    if (q.ko == q.vo) {
+      const int n = open(q.ko + 1);
+      if (n < 0) return kStepFail;
+      if (n == 0) {
+        q.kdone = true;
+      } else {
+        ++q.ko;
+        q.kj = 0;
+        q.set_ntl(q.ko, n);
+        return kStepK;
+      }
+    }
+  }
+  return q.vj < q.ntl(q.vo) ? kStepV : kStepDone;
+}
+
 // Row of the P operand / O accumulator that holds (query head qh, term):
 // the lane quarter of the warp owning qh's kv head, three rows per head.
 __device__ __forceinline__ int o_row(int qh, int term, int qpw) {
@@ -416,43 +457,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       it = sh.desc[o & 1];
       return true;
     };
-    DecodeItem kI;
-    bool ok = open(0, kI) && kI.b >= 0;
-    if (ok) {
-      int ko = 0, kj = 1, kntl = htiles(kI, nt);
-      ok = emit(kI, 0, 0, false);
-      DecodeItem vI = kI;
-      int vo = 0, vj = 0, vntl = kntl;
-      bool kdone = false;
-      while (ok) {
-        if (!kdone) {
-          if (kj < kntl) {
-            ok = emit(kI, ko & 1, kj, false);
-            ++kj;
-          } else {
-            DecodeItem nI;
-            if (!open(ko + 1, nI)) break;
-            if (nI.b < 0) {
-              kdone = true;
-            } else {
-              ++ko;
-              kI = nI;
-              kntl = htiles(kI, nt);
-              ok = emit(kI, ko & 1, 0, false);
-              kj = 1;
-            }
-          }
-        }
-        if (!ok) break;
-        ok = emit(vI, vo & 1, vj, true);
-        ++vj;
-        if (ok && vj == vntl) {
-          if (lane == 0) mbar_arrive(&sh.desc_free[vo & 1]);   // done with its row table
-          if (vo == ko) break;
-          vo = ko;
-          vI = kI;
-          vntl = kntl;
-          vj = 0;
+    DecodeItem it0{}, it1{};
+    auto open_item = [&](int o) -> int {
+      DecodeItem it;
+      if (!open(o, it)) return -1;
+      if (o & 1) it1 = it; else it0 = it;
+      return it.b < 0 ? 0 : htiles(it, nt);
+    };
+    RingSched q{0, 0, 0, 0, 0, 0, 0, false};
+    q.ntl0 = open_item(0);
+    if (q.ntl0 > 0) {
+      while (true) {
+        const int step = ring_next(q, open_item);
+        if (step == kStepK) {
+          if (!emit((q.ko & 1) ? it1 : it0, q.ko & 1, q.kj, false)) break;
+          ++q.kj;
+          ++q.lead;
+        } else if (step == kStepV) {
+          const bool last = q.vj == q.ntl(q.vo) - 1;
+          if (!emit((q.vo & 1) ? it1 : it0, q.vo & 1, q.vj, true)) break;
+          if (last && lane == 0) mbar_arrive(&sh.desc_free[q.vo & 1]);   // done with its row table
+          ++q.vj;
+          --q.lead;
+        } else {
+          break;
         }
       }
     }
@@ -466,6 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
       const uint32_t idesc_pv = make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, 128, D);
+      // operand descriptors at offset 0 of each region; an operand at byte
+      // offset x adds x >> 4 to the start-address field
+      const uint64_t kdesc0 = make_smem_desc(smem_u32(smem), 16, C::kSBO, C::kSwz);
+      const uint64_t vdesc0 = make_smem_desc(smem_u32(smem), 0, C::kSBO, C::kSwz);
+      const uint64_t qdesc0 = make_smem_desc(smem_u32(sQT), 16, C::kSBO, C::kSwz);
+      const uint64_t pdesc0 = make_smem_desc(smem_u32(sP), 16, 1024, kSwizzle128B);
       int pos = 0, st = 0, pt = 0;
       auto qk = [&](int o, int j, int ntl) -> bool {
         const int sb = st % kSBufs;
@@ -474,14 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             !hwait(&sh.full[s], (pos / NS) & 1, sh, a.err))
           return false;
         tc_fence_after_sync();
-        const uint32_t tile = smem_u32(smem + s * C::kTileBytes);
-        const uint32_t qt = smem_u32(sQT + (o & 1) * C::kQTBytes);
+        const uint64_t da0 = kdesc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
+        const uint64_t db0 = qdesc0 + static_cast<uint64_t>(((o & 1) * C::kQTBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) {
-          const uint64_t da = make_smem_desc(tile + 32 * kk, 16, C::kSBO, C::kSwz);
-          const uint64_t db = make_smem_desc(qt + 32 * kk, 16, C::kSBO, C::kSwz);
-          tc_mma_f8(tmem + sb * kMaxN, da, db, idesc_qk, kk > 0);
-        }
+        for (int kk = 0; kk < D / 32; ++kk)
+          tc_mma_f8(tmem + sb * kMaxN, da0 + 2 * kk, db0 + 2 * kk, idesc_qk, kk > 0);
         tc_commit(&sh.empty[s]);
         tc_commit(&sh.s_full[sb]);
         if (j == ntl - 1) tc_commit(&sh.desc_free[o & 1]);   // last read of its query terms
@@ -496,16 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             !hwait(&sh.full[s], (pos / NS) & 1, sh, a.err))
           return false;
         tc_fence_after_sync();
-        const uint32_t tile = smem_u32(smem + s * C::kTileBytes);
-        const uint32_t ptile = smem_u32(sP + pb * C::kPBytes);
+        // A = P (K-major, 128-byte rows); B = V rows as stored (d contiguous:
+        // MN-major, one swizzle atom wide); K steps of 32 tile rows
+        const uint64_t da0 = pdesc0 + static_cast<uint64_t>((pb * C::kPBytes) >> 4);
+        const uint64_t db0 = vdesc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 32; ++kk) {
-          // A = P (K-major, 128-byte rows); B = V rows as stored (d contiguous:
-          // MN-major, one swizzle atom wide)
-          const uint64_t da = make_smem_desc(ptile + 32 * kk, 16, 1024, kSwizzle128B);
-          const uint64_t db = make_smem_desc(tile + kk * 32 * D, 0, C::kSBO, C::kSwz);
-          tc_mma_f8(tmem + C::kOCol0 + (o & 1) * D, da, db, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 32; ++kk)
+          tc_mma_f8(tmem + C::kOCol0 + (o & 1) * D, da0 + 2 * kk, db0 + (2 * D) * kk, idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.empty[s]);
         tc_commit(&sh.p_free[pb]);
         if (j == ntl - 1) tc_commit(&sh.o_full[o & 1]);
@@ -513,43 +542,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pt;
         return true;
       };
-      auto open = [&](int o, DecodeItem& it) -> bool {
-        if (!hwait(&sh.desc_full[o & 1], (o >> 1) & 1, sh, a.err)) return false;
-        it = sh.desc[o & 1];
-        return it.b >= 0;
+      auto open_item = [&](int o) -> int {
+        if (!hwait(&sh.desc_full[o & 1], (o >> 1) & 1, sh, a.err)) return -1;
+        const DecodeItem it = sh.desc[o & 1];
+        return it.b < 0 ? 0 : htiles(it, nt);
       };
-      DecodeItem kI;
-      if (open(0, kI)) {
-        int ko = 0, kj = 1, kntl = htiles(kI, nt);
-        bool ok = qk(0, 0, kntl);
-        int vo = 0, vj = 0, vntl = kntl;
-        bool kdone = false;
-        while (ok) {
-          if (!kdone) {
-            if (kj < kntl) {
-              ok = qk(ko, kj, kntl);
-              ++kj;
-            } else {
-              DecodeItem nI;
-              if (open(ko + 1, nI)) {
-                ++ko;
-                kntl = htiles(nI, nt);
-                ok = qk(ko, 0, kntl);
-                kj = 1;
-              } else {
-                kdone = true;
-              }
-            }
-          }
-          if (!ok) break;
-          if (vj == 0 && !hwait(&sh.o_free[vo & 1], ((vo >> 1) & 1) ^ 1, sh, a.err)) break;
-          ok = pv(vo, vj, vntl);
-          ++vj;
-          if (ok && vj == vntl) {
-            if (vo == ko) break;
-            vo = ko;
-            vntl = kntl;
-            vj = 0;
+      RingSched q{0, 0, 0, 0, 0, 0, 0, false};
+      q.ntl0 = open_item(0);
+      if (q.ntl0 > 0) {
+        while (true) {
+          const int step = ring_next(q, open_item);
+          if (step == kStepK) {
+            if (!qk(q.ko, q.kj, q.ntl(q.ko))) break;
+            ++q.kj;
+            ++q.lead;
+          } else if (step == kStepV) {
+            if (q.vj == 0 && !hwait(&sh.o_free[q.vo & 1], ((q.vo >> 1) & 1) ^ 1, sh, a.err)) break;
+            if (!pv(q.vo, q.vj, q.ntl(q.vo))) break;
+            ++q.vj;
+            --q.lead;
+          } else {
+            break;
           }
         }
       }
