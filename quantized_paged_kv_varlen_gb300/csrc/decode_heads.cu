@@ -32,16 +32,19 @@
 // rescaled).  Probabilities are at most 2^8 and carry the per-token v-scale,
 // so the item's largest v-scale fixes the probability term scale up front.
 //
-// Roles (one persistent CTA per SM, 7 warps):
+// Roles (one persistent CTA per SM, 12 warps):
 //   warp 0  items: takes work items (the first by CTA index, then from a
 //           global counter, largest first), resolves the item's pages into a
-//           row table, loads its k/v-scales, splits its queries into E4M3
-//           terms and fixes the term scales;
+//           row table, loads its k/v-scales and fixes the probability term
+//           scales;
 //   warp 1  stream: lane 0 issues one TMA per tile in the order
-//           K(0) | K(1) V(0) | K(2) V(1) | ... (K one tile ahead of V across
-//           item boundaries); the warp copies partial tail tiles row by row;
-//   warp 2  MMA: QK(t+1) before PV(t);
-//   warps 3-6 softmax and epilogue.
+//           K(0) K(1) | K(2) V(0) | K(3) V(1) | ... (K two tiles ahead of V,
+//           at most one item ahead); the warp copies partial tail tiles row
+//           by row;
+//   warp 2  QK MMAs, warp 11 PV MMAs (one issuing lane each);
+//   warps 3-6 softmax;
+//   warps 7-10 split each item's queries into E4M3 terms (two items ahead)
+//           and move finished O rows out of TMEM (the epilogue).
 // The last CTA to finish re-arms the counter.
 #include <cmath>
 
@@ -52,10 +55,11 @@ namespace qpkv {
 namespace {
 
 constexpr int kTile = 128;        // (kv head, token) rows per tile = MMA M
-constexpr int kThreads = 352;     // 11 warps
-constexpr int kWarpItems = 0, kWarpStream = 1, kWarpMma = 2;
+constexpr int kThreads = 384;     // 12 warps
+constexpr int kWarpItems = 0, kWarpStream = 1, kWarpMma = 2, kWarpSoftmax0 = 3;
 constexpr int kSoftmax = 128;     // warps 3..6 (softmax), 7..10 (epilogue)
-constexpr int kWarpEpi0 = 7;
+constexpr int kWarpEpi0 = 7;      // warps 7..10
+constexpr int kWarpPv = 11;
 constexpr int kMaxStages = 16;
 constexpr int kMaxTilesItem = 16;
 constexpr int kSBufs = 2;         // S accumulators in TMEM
@@ -119,8 +123,9 @@ struct HShared {
   uint64_t s_full[kSBufs], s_free[kSBufs];
   uint64_t p_ready[kPBufs], p_free[kPBufs];
   uint64_t o_full[kOBufs], o_free[kOBufs];
-  uint64_t mma_done;
+  uint64_t mma_done[2];      // QK and PV issuers' MMAs complete
   uint64_t ep_ready[2];      // item's O scales written, O may be read once complete
+  uint64_t q_done[2];        // item's query terms and their scales written
   DecodeItem desc[2];
   int tab[2][kMaxTilesItem];   // pool row of each tile's box, -1 if its page is bad
   float sig_q[2][32];          // query term scale per query head
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.tab_full[d], 1);
       mbar_init(&sh.scl_full[d], 1);
       mbar_init(&sh.desc_full[d], 1);
-      mbar_init(&sh.desc_free[d], 1 + 1 + kSoftmax);   // MMA commit, stream, softmax
+      mbar_init(&sh.desc_free[d], 1 + 1 + 1 + kSoftmax);   // QK commit, PV issuer, stream, softmax
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&sh.s_full[b], 1);
@@ -277,8 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.o_full[b], 1);
       mbar_init(&sh.o_free[b], kSoftmax);
     }
-    for (int d = 0; d < 2; ++d) mbar_init(&sh.ep_ready[d], kSoftmax);
-    mbar_init(&sh.mma_done, 1);
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&sh.ep_ready[d], kSoftmax);
+      mbar_init(&sh.q_done[d], kSoftmax);
+    }
+    mbar_init(&sh.mma_done[0], 1);
+    mbar_init(&sh.mma_done[1], 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -295,10 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpItems) {
     // ------------------------------------------------------------ items
-    const int lph = 32 / Hq;           // lanes per query head in the query split
-    const int qh = lane / lph;
-    const int E = D / lph;             // query elements per lane
-    const int d0 = (lane % lph) * E;
     for (int o = 0;; ++o) {
       const int d = o & 1;
       int idx = static_cast<int>(blockIdx.x);
@@ -335,59 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // k- and v-scales of every tile (one 512-byte piece each)
       float* ks = sKS + d * (kMaxTilesItem * kTile);
       float* vs = sVS + d * (kMaxTilesItem * kTile);
-      const int bytes = (lane < ntl && row >= 0) ? 2 * kTile * 4 : 0;
-      const int total = __reduce_add_sync(0xffffffffu, bytes);
+      const bool load = lane < ntl && row >= 0;
+      const int total = __popc(__ballot_sync(0xffffffffu, load)) * (2 * kTile * 4);
       if (lane == 0) mbar_arrive_expect_tx(&sh.scl_full[d], total);
       __syncwarp();
-      if (bytes > 0) {
+      if (load) {
         bulk_load(ks + lane * kTile, a.k_scale + static_cast<size_t>(row) * Hkv, kTile * 4,
                   &sh.scl_full[d]);
         bulk_load(vs + lane * kTile, a.v_scale + static_cast<size_t>(row) * Hkv, kTile * 4,
                   &sh.scl_full[d]);
       }
-      // queries -> three E4M3 terms: rows h*3G + term*G + g of the QK B operand
-      {
-        const uint16_t* src = a.q + (static_cast<size_t>(it.b) * Hq + qh) * D + d0;
-        float amax = 0.f;
-        for (int e = 0; e < E; e += 8) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + e));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            amax = fmaxf(amax, fabsf(bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu))));
-            amax = fmaxf(amax, fabsf(bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16))));
-          }
-        }
-        for (int off = 1; off < lph; off <<= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float s1 = amax * (1.0f / 448.0f);
-        const float inv1 = s1 > 0.f ? 1.0f / s1 : 0.f;
-        if (lane % lph == 0) sh.sig_q[d][qh] = s1;
-        uint8_t* qt = sQT + d * C::kQTBytes;
-        const int h = qh / G, g = qh % G;
-        const int n0 = h * 3 * G + g;
-        for (int e = 0; e < E; e += 8) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + e));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t p1 = 0, p2 = 0, p3 = 0;
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-              const uint32_t word = w[2 * half + pr];
-              uint16_t c1, c2, c3;
-              hsplit3x2(bf16_bits_to_float(static_cast<uint16_t>(word & 0xFFFFu)),
-                        bf16_bits_to_float(static_cast<uint16_t>(word >> 16)), inv1, s1, c1, c2, c3);
-              p1 |= static_cast<uint32_t>(c1) << (16 * pr);
-              p2 |= static_cast<uint32_t>(c2) << (16 * pr);
-              p3 |= static_cast<uint32_t>(c3) << (16 * pr);
-            }
-            const int k = d0 + e + 4 * half;
-            *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0, k, D)) = p1;
-            *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0 + G, k, D)) = p2;
-            *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0 + 2 * G, k, D)) = p3;
-          }
-        }
+      // the epilogue warps split the item's queries into E4M3 terms
+      if (!warp_wait(&sh.q_done[d], (o >> 1) & 1, sh, a.err, lane)) {
+        if (lane == 0) drain_wait(&sh.scl_full[d], (o >> 1) & 1, a.err);
+        break;
       }
       // probability term scale per query head from its kv head's largest
       // v-scale over the item's valid tokens
@@ -489,8 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = pos > NS ? pos - NS : 0; i < pos; ++i)
         drain_wait(&sh.full[i % NS], (i / NS) & 1, a.err);
     __syncwarp();
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || warp == kWarpPv) {
     // ---------------------------------------------------------------- MMA
+    // Lane 0 of warp 2 issues the QK MMAs, lane 0 of warp 11 the PV MMAs;
+    // both walk the ring schedule and skip the other side's stages, so
+    // neither waits behind the other's issue.
+    const bool is_qk = warp == kWarpMma;
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
       const uint32_t idesc_pv = make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, 128, D);
@@ -545,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto open_item = [&](int o) -> int {
         if (!hwait(&sh.desc_full[o & 1], (o >> 1) & 1, sh, a.err)) return -1;
         const DecodeItem it = sh.desc[o & 1];
+        if (!is_qk) mbar_arrive(&sh.desc_free[o & 1]);   // the QK side releases by commit
         return it.b < 0 ? 0 : htiles(it, nt);
       };
       RingSched q{0, 0, 0, 0, 0, 0, 0, false};
@@ -553,12 +524,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (true) {
           const int step = ring_next(q, open_item);
           if (step == kStepK) {
-            if (!qk(q.ko, q.kj, q.ntl(q.ko))) break;
+            if (is_qk) {
+              if (!qk(q.ko, q.kj, q.ntl(q.ko))) break;
+            } else {
+              ++pos;
+            }
             ++q.kj;
             ++q.lead;
           } else if (step == kStepV) {
-            if (q.vj == 0 && !hwait(&sh.o_free[q.vo & 1], ((q.vo >> 1) & 1) ^ 1, sh, a.err)) break;
-            if (!pv(q.vo, q.vj, q.ntl(q.vo))) break;
+            if (!is_qk) {
+              if (q.vj == 0 && !hwait(&sh.o_free[q.vo & 1], ((q.vo >> 1) & 1) ^ 1, sh, a.err)) break;
+              if (!pv(q.vo, q.vj, q.ntl(q.vo))) break;
+            } else {
+              ++pos;
+            }
             ++q.vj;
             --q.lead;
           } else {
@@ -567,11 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // every MMA issued here completes before TMEM is released
-      tc_commit(&sh.mma_done);
-      drain_wait(&sh.mma_done, 0, a.err);
+      tc_commit(&sh.mma_done[is_qk ? 0 : 1]);
+      drain_wait(&sh.mma_done[is_qk ? 0 : 1], 0, a.err);
     }
     __syncwarp();
-  } else if (warp < kWarpEpi0) {
+  } else if (warp >= kWarpSoftmax0 && warp < kWarpEpi0) {
     // ---------------------------------------------------------- softmax
     constexpr int kG3 = 3 * G;
     const int sw = warp & 3;                  // TMEM lane quarter
@@ -757,9 +736,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.ep_ready[d]);
     }
   } else {
-    // --------------------------------------------------------- epilogue
-    // O rows -> fp32 partial output (terms combined) and lse, overlapping
-    // the softmax of the next item
+    // ------------------------------------------ query split and epilogue
+    // These warps split the queries of each item into E4M3 terms (two items
+    // ahead) and move each finished item's O rows out of TMEM.
+    const int et = tid - kWarpEpi0 * 32;      // 0..127
+    const int E = (Hq * D) / kSoftmax >= 8 ? (Hq * D) / kSoftmax : 8;   // query elements per thread
+    const int tph = D / E;                    // threads per query head (<= 16)
+    const bool q_thread = et < Hq * tph;      // whole warps (Hq * tph is a multiple of 32)
+    const int qh_s = et / tph;
+    const int d0 = (et % tph) * E;
+    // Query split of item o: rows h*3G + term*G + g of the QK B operand and
+    // the term scale of every query head.  1: done, 0: end of work, -1: failed.
+    auto qprep = [&](int o) -> int {
+      const int d = o & 1;
+      if (!warp_wait(&sh.tab_full[d], (o >> 1) & 1, sh, a.err, lane)) return -1;
+      const DecodeItem it = sh.desc[d];
+      if (it.b < 0) return 0;
+      if (q_thread) {
+        const uint16_t* src = a.q + (static_cast<size_t>(it.b) * Hq + qh_s) * D + d0;
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (8 * i < E) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + 8 * i));
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+          }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (2 * i < E) {
+            amax = fmaxf(amax, fabsf(bf16_bits_to_float(static_cast<uint16_t>(w[i] & 0xFFFFu))));
+            amax = fmaxf(amax, fabsf(bf16_bits_to_float(static_cast<uint16_t>(w[i] >> 16))));
+          }
+        }
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1)
+          if (off < tph) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float s1 = amax * (1.0f / 448.0f);
+        const float inv1 = s1 > 0.f ? 1.0f / s1 : 0.f;
+        if (et % tph == 0) sh.sig_q[d][qh_s] = s1;
+        uint8_t* qt = sQT + d * C::kQTBytes;
+        const int n0 = (qh_s / G) * 3 * G + qh_s % G;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {   // 4 elements -> one 32-bit word per term row
+          if (4 * i < E) {
+            uint16_t a1, a2, a3, b1, b2, b3;
+            const uint32_t lo = w[2 * i], hi = w[2 * i + 1];
+            hsplit3x2(bf16_bits_to_float(static_cast<uint16_t>(lo & 0xFFFFu)),
+                      bf16_bits_to_float(static_cast<uint16_t>(lo >> 16)), inv1, s1, a1, a2, a3);
+            hsplit3x2(bf16_bits_to_float(static_cast<uint16_t>(hi & 0xFFFFu)),
+                      bf16_bits_to_float(static_cast<uint16_t>(hi >> 16)), inv1, s1, b1, b2, b3);
+            const int k = d0 + 4 * i;
+            *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0, k, D)) = a1 | (uint32_t(b1) << 16);
+            *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0 + G, k, D)) = a2 | (uint32_t(b2) << 16);
+            *reinterpret_cast<uint32_t*>(qt + swizzled_offset(n0 + 2 * G, k, D)) =
+                a3 | (uint32_t(b3) << 16);
+          }
+        }
+        fence_proxy_async_smem();   // generic stores, read by the tensor cores
+      }
+      mbar_arrive(&sh.q_done[d]);
+      return 1;
+    };
+    int q_next = 0;
+    bool q_more = true;
+    auto q_step = [&]() {
+      if (!q_more) return;
+      const int r = qprep(q_next);
+      if (r > 0) ++q_next; else q_more = false;
+    };
+    q_step();
+    q_step();
+
+    // epilogue: O rows -> fp32 partial output (terms combined) and lse
     const int sw = warp & 3;
     const int tl = sw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
@@ -800,6 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       mbar_arrive(&sh.o_free[d]);
       if (writer) a.part_lse[static_cast<size_t>(slot) * Hq + qh_o] = lse;
+      q_step();
     }
   }
   tc_fence_before_sync();
