@@ -235,11 +235,6 @@ __device__ __forceinline__ int ring_next(RingSched& q, Open&& open) {
   return q.vj < q.ntl(q.vo) ? kStepV : kStepDone;
 }
 
-// Row of the P operand / O accumulator that holds (query head qh, term):
-// the lane quarter of the warp owning qh's kv head, three rows per head.
-__device__ __forceinline__ int o_row(int qh, int term, int qpw) {
-  return (qh / qpw) * 32 + (qh % qpw) * 3 + term;
-}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -463,13 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_qk = warp == kWarpMma;
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, 128, N);
-      const uint32_t idesc_pv = make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, 128, D);
+      const uint32_t idesc_pv = make_idesc(kFmtE4M3, kFmtE4M3, 1, 1, 128, D);
       // operand descriptors at offset 0 of each region; an operand at byte
       // offset x adds x >> 4 to the start-address field
       const uint64_t kdesc0 = make_smem_desc(smem_u32(smem), 16, C::kSBO, C::kSwz);
       const uint64_t vdesc0 = make_smem_desc(smem_u32(smem), 0, C::kSBO, C::kSwz);
       const uint64_t qdesc0 = make_smem_desc(smem_u32(sQT), 16, C::kSBO, C::kSwz);
-      const uint64_t pdesc0 = make_smem_desc(smem_u32(sP), 16, 1024, kSwizzle128B);
+      const uint64_t pdesc0 = make_smem_desc(smem_u32(sP), 0, 1024, kSwizzle128B);
       int pos = 0, st = 0, pt = 0;
       auto qk = [&](int o, int j, int ntl) -> bool {
         const int sb = st % kSBufs;
@@ -497,14 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             !hwait(&sh.full[s], (pos / NS) & 1, sh, a.err))
           return false;
         tc_fence_after_sync();
-        // A = P (K-major, 128-byte rows); B = V rows as stored (d contiguous:
-        // MN-major, one swizzle atom wide); K steps of 32 tile rows
+        // A = P and B = V, both stored row per tile row (MN-major, one
+        // 128-byte swizzle atom wide for P); K steps of 32 tile rows
         const uint64_t da0 = pdesc0 + static_cast<uint64_t>((pb * C::kPBytes) >> 4);
         const uint64_t db0 = vdesc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 32; ++kk)
-          tc_mma_f8(tmem + C::kOCol0 + (o & 1) * D, da0 + 2 * kk, db0 + (2 * D) * kk, idesc_pv,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f8(tmem + C::kOCol0 + (o & 1) * D, da0 + (32 * 128 / 16) * kk, db0 + (2 * D) * kk,
+                    idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.empty[s]);
         tc_commit(&sh.p_free[pb]);
         if (j == ntl - 1) tc_commit(&sh.o_full[o & 1]);
@@ -557,24 +552,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tl = sw * 32 + lane;            // tile row = S lane
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
     const int hpw = Hkv / 4;                  // kv heads per warp
-    const int qpw = Hq / 4;                   // query heads per warp
     const int my_h = tl / nt;                 // kv head of this row
     const int my_t = tl % nt;                 // token of this row within the tile
     const int sidx = my_t * Hkv + my_h;       // [token][head] scale index within a tile
     const int sel = my_h % hpw;
     const int w_h0 = sw * hpw;
-    // this lane's O row: (query head qh_o, term) when lane < 3 * qpw
-    const bool o_lane = lane < 3 * qpw;
-    const int qh_o = o_lane ? sw * qpw + lane / 3 : 0;
-    const int g_o = qh_o % G;
-    const int src_o = ((qh_o / G) % hpw) * nt;   // first S lane of qh_o's kv head
-    // byte offsets of this row's entries in the P tile: (query head g, term)
-    int poff[kG3];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int t = 0; t < 3; ++t)
-        poff[3 * g + t] = static_cast<int>(swizzled_offset(o_row(my_h * G + g, t, qpw), tl, 128));
+    // this lane's O row (see o_lane_role); S lanes of its kv head start at src_o
+    const int o_slot = lane / nt, o_within = lane % nt;
+    const bool o_lane = o_within < kG3;
+    const int g_o = o_within / 3;
+    const int qh_o = o_lane ? (sw * hpw + o_slot) * G + g_o : 0;
+    const int src_o = o_slot * nt;
+    // this row's 3G probability bytes: P tile row tl, bytes r0 .. r0 + 3G - 1
+    const int r0 = sw * 32 + sel * nt;
     int st = 0, pt = 0;
     for (int o = 0;; ++o) {
       const int d = o & 1;
@@ -625,31 +615,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float sdot = v0 + v1 * (1.0f / 16.0f) + v2 * (1.0f / 256.0f);
           l[g] = valid ? ks * sq[g] * sdot : -INFINITY;
         }
-        // tile maximum per query head over the nt lanes of this kv head
-        float tmx[G];
+        // ---- running maximum per query head, moved only when a tile beats it
+        // by more than 2^8: a warp vote first, the tile maxima only then
+        bool beat = false;
 #pragma unroll
-        for (int g = 0; g < G; ++g) tmx[g] = l[g];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          if (off < nt) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-              tmx[g] = fmaxf(tmx[g], __shfl_xor_sync(0xffffffffu, tmx[g], off));
-          }
-        }
-        // ---- running maximum per query head (moved only by more than 2^8)
+        for (int g = 0; g < G; ++g) beat |= l[g] > m_run[g] + kRescaleLog2;
         bool need = false;
         float fac[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float x = tmx[g];
-          fac[g] = 1.f;
-          if (x > m_run[g] + kRescaleLog2) {
-            if (m_run[g] > -INFINITY) {
-              need = true;
-              fac[g] = exp2f(m_run[g] - x);
+        for (int g = 0; g < G; ++g) fac[g] = 1.f;
+        if (__any_sync(0xffffffffu, beat)) {
+          float tmx[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) tmx[g] = l[g];
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            if (off < nt) {
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+                tmx[g] = fmaxf(tmx[g], __shfl_xor_sync(0xffffffffu, tmx[g], off));
             }
-            m_run[g] = x;
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if (tmx[g] > m_run[g] + kRescaleLog2) {
+              if (m_run[g] > -INFINITY) {
+                need = true;
+                fac[g] = exp2f(m_run[g] - tmx[g]);
+              }
+              m_run[g] = tmx[g];
+            }
           }
         }
         float p[G];
@@ -683,31 +678,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before_sync();
         }
-        // ---- P' = p * v-scale, three E4M3 terms, into the block-diagonal P
-        uint8_t c[kG3];
+        // ---- P' = p * v-scale, three E4M3 terms, into the block-diagonal P:
+        // bytes (g, term) at r0 + 3g + term of row tl, packed into words
+        constexpr int kWords = (kG3 + 3) / 4;
+        uint32_t wd[kWords];
 #pragma unroll
-        for (int g = 0; g + 1 < G; g += 2) {
+        for (int i = 0; i < kWords; ++i) wd[i] = 0;
+#pragma unroll
+        for (int g = 0; g < G; g += 2) {
           uint16_t c1, c2, c3;
-          hsplit3x2(p[g] * vs, p[g + 1] * vs, spinv, sp, c1, c2, c3);
-          c[3 * g] = c1 & 0xFF;
-          c[3 * g + 1] = c2 & 0xFF;
-          c[3 * g + 2] = c3 & 0xFF;
-          c[3 * g + 3] = c1 >> 8;
-          c[3 * g + 4] = c2 >> 8;
-          c[3 * g + 5] = c3 >> 8;
-        }
-        if (G & 1) {
-          uint16_t c1, c2, c3;
-          hsplit3x2(p[G - 1] * vs, 0.f, spinv, sp, c1, c2, c3);
-          c[kG3 - 3] = c1 & 0xFF;
-          c[kG3 - 2] = c2 & 0xFF;
-          c[kG3 - 1] = c3 & 0xFF;
+          hsplit3x2(p[g] * vs, g + 1 < G ? p[g + 1] * vs : 0.f, spinv, sp, c1, c2, c3);
+          const uint32_t b[6] = {c1 & 0xFFu, c2 & 0xFFu, c3 & 0xFFu,
+                                 static_cast<uint32_t>(c1 >> 8), static_cast<uint32_t>(c2 >> 8),
+                                 static_cast<uint32_t>(c3 >> 8)};
+#pragma unroll
+          for (int i = 0; i < 6; ++i) {
+            const int m = 3 * g + i;
+            if (m < kG3) wd[m / 4] |= b[i] << (8 * (m % 4));
+          }
         }
         const int pb = pt % kPBufs;
         hwait(&sh.p_free[pb], ((pt / kPBufs) & 1) ^ 1, sh, a.err);
         uint8_t* dst = sP + pb * C::kPBytes;
 #pragma unroll
-        for (int i = 0; i < kG3; ++i) dst[poff[i]] = c[i];
+        for (int i = 0; i < kWords; ++i)
+          *reinterpret_cast<uint32_t*>(dst + swizzled_offset(tl, r0 + 4 * i, 128)) = wd[i];
         fence_proxy_async_smem();
         mbar_arrive(&sh.p_ready[pb]);
         ++pt;
@@ -816,10 +811,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = warp & 3;
     const int tl = sw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-    const int qpw = Hq / 4;
-    const bool o_lane = lane < 3 * qpw;
-    const int qh_o = o_lane ? sw * qpw + lane / 3 : 0;
-    const bool writer = o_lane && lane % 3 == 0;
+    const int hpw = Hkv / 4;
+    const int o_slot = lane / nt, o_within = lane % nt;
+    const bool o_lane = o_within < 3 * G;
+    const int qh_o = o_lane ? (sw * hpw + o_slot) * G + o_within / 3 : 0;
+    const bool writer = o_lane && o_within % 3 == 0;
     for (int o = 0;; ++o) {
       const int d = o & 1;
       if (!warp_wait(&sh.ep_ready[d], (o >> 1) & 1, sh, a.err, lane)) break;
