@@ -34,8 +34,8 @@ WORKLOAD = ("Llama-3-8B-shaped paged FP8 decode: B=64, q_len=1, kv lengths ~U{51
             "fp32 per-(token, head) scales")
 B, HQ, HKV, D, PS, LO, HI = 64, 32, 8, 128, 16, 512, 8192
 L2_BYTES = 129 * 2 ** 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_attend_llama8b_b64.txt")
-KERNEL_SOURCE = os.path.join(ROOT, "quantized_paged_kv_varlen_gb300", "csrc", "decode.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_heads_llama8b_b64.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "quantized_paged_kv_varlen_gb300", "csrc", "decode_heads.cu")
 
 
 def algorithmic_bytes(lengths):
@@ -448,7 +448,7 @@ def run_qpkv(args):
                    "sum_kv_tokens": int(wb.lengths.sum())},
         "tokens_per_s": B * world / step_s,
         "algorithmic_bytes_per_step": wb.total_bytes,
-        "roofline": {"bound": "hbm", "kernel": "decode_attend", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "decode_heads_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs (copy)",
                      "traffic": profiled_traffic(),
@@ -464,6 +464,14 @@ def run_qpkv(args):
     print(json.dumps(line), flush=True)
 
 
+def set_batch(n):
+    """Number of requests per rank (the workload's B)."""
+    global B, WORKLOAD
+    if n != B:
+        WORKLOAD = WORKLOAD.replace(f"B={B},", f"B={n},")
+        B = n
+
+
 def main():
     if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-worker":
         print(json.dumps(cpu_worker(float(sys.argv[2]), int(sys.argv[3]))))
@@ -477,7 +485,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up for at least this long so clocks settle")
+    ap.add_argument("--batch", type=int, default=B,
+                    help="requests per rank (64 is the benchmark; smaller batches are for "
+                         "profiler captures)")
     args = ap.parse_args()
+    set_batch(args.batch)
     if args.impl == "reference":
         run_reference(args)
     else:
