@@ -264,6 +264,35 @@ qpkv_status qpkv_decode_static(const int32_t* seqlens_kv_host, int32_t batch_siz
                                const int32_t* block_table, int32_t bt_stride, float sm_scale,
                                void* o, float* lse, int32_t* error_word, void* stream);
 
+/* ------------------------------------------ dense FP8 attention forward
+ * "[Triton] FP8 with FA v3 API" (flash_attn_func with q/k/v in FP8 and
+ * their descale values):
+ *   O = softmax(softmax_scale * qd[b,h] * kd[b,hk] * Q8 . K8^T + mask)
+ *       . V8 * vd[b,hk]
+ * Q8/K8/V8 are E4M3 codes; a code times its descale is the value.
+ *   q          device, E4M3 [B, Sq, Hq, D] (BSND, contiguous)
+ *   k, v       device, E4M3 [B, Sk, Hkv, D]
+ *   q_descale  device fp32 [B, Hq]; k_descale, v_descale fp32 [B, Hkv]
+ *   softmax_scale  <= 0 selects 1/sqrt(D)
+ *   causal     0: every key visible; 1: bottom-right aligned, key j visible
+ *              to query i iff j <= i + Sk - Sq
+ *   o          device bf16 [B, Sq, Hq, D]; rows that see no key are 0
+ *   lse        device fp32 [B, Sq, Hq] or NULL: natural log of the sum of
+ *              exp(scaled logits); -inf for rows that see no key
+ *   error_word device int32 or NULL: QPKV_DEV_ERR_* bits set by the kernel
+ * kv head of q head h: h / (Hq / Hkv).  Supported: D = 128, Hq % Hkv == 0;
+ * every pointer 16-byte aligned.  P enters the PV product as two E4M3
+ * terms (hi + lo, about 8 significant bits).  The caller owns all
+ * memory; nothing is allocated.  Errors: QPKV_ERR_INVALID_ARG (null or
+ * misaligned pointers, negative sizes), QPKV_ERR_UNSUPPORTED (D, head
+ * grouping), QPKV_ERR_CUDA (launch). */
+qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32_t batch,
+                              int32_t seqlen_q, int32_t seqlen_k, int32_t num_qo_heads,
+                              int32_t num_kv_heads, int32_t head_dim, const float* q_descale,
+                              const float* k_descale, const float* v_descale,
+                              float softmax_scale, int32_t causal, void* o, float* lse,
+                              int32_t* error_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

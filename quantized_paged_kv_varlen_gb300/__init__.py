@@ -83,6 +83,8 @@ def _declare(lib):
         "qpkv_decode_merge": (_i32, [P64, _p, S, _p, _p, _p, _p]),
         "qpkv_decode_static": (_i32, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
                                       _i32, _p, _i32, ctypes.c_float, _p, _p, _p, _p]),
+        "qpkv_fp8_attn_fwd": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p,
+                                     ctypes.c_float, _i32, _p, _p, _p, _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -367,3 +369,33 @@ class DecodePlan:
                                      _ptr(self.int_ws), _ptr(out), _ptr(lse), _stream()),
                "qpkv_decode_merge")
         return out
+
+
+def fp8_attn_fwd(q, k, v, q_descale, k_descale, v_descale, softmax_scale=None, causal=False,
+                 out=None, lse=None, error_word=None):
+    """Dense FP8 attention (BSND E4M3 codes as uint8 tensors): returns bf16 O
+    [B, Sq, Hq, D]; ``lse`` (fp32 [B, Sq, Hq]) is filled when given."""
+    torch = _torch()
+    lib = load()
+    _need(q, "q", torch.uint8, 4)
+    _need(k, "k", torch.uint8, 4)
+    _need(v, "v", torch.uint8, 4)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Sk, Hkv, D] matching q")
+    for t, n, h in ((q_descale, "q_descale", Hq), (k_descale, "k_descale", Hkv),
+                    (v_descale, "v_descale", Hkv)):
+        _need(t, n, torch.float32, 2)
+        if tuple(t.shape) != (B, h):
+            raise ValueError(f"{n} must be [{B}, {h}]")
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    _check(lib.qpkv_fp8_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Sq, Sk, Hq, Hkv, D,
+                                 _ptr(q_descale), _ptr(k_descale), _ptr(v_descale),
+                                 float(softmax_scale) if softmax_scale else 0.0,
+                                 1 if causal else 0, _ptr(out), _ptr(lse), _ptr(error_word),
+                                 _stream()), "qpkv_fp8_attn_fwd")
+    return out

@@ -380,4 +380,27 @@ qpkv_status qpkv_decode_run(const int64_t* plan_info, void* float_ws, size_t flo
   return qpkv_decode_merge(plan_info, float_ws, float_ws_bytes, int_ws, o, lse, stream);
 }
 
+qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32_t batch,
+                              int32_t seqlen_q, int32_t seqlen_k, int32_t num_qo_heads,
+                              int32_t num_kv_heads, int32_t head_dim, const float* q_descale,
+                              const float* k_descale, const float* v_descale,
+                              float softmax_scale, int32_t causal, void* o, float* lse,
+                              int32_t* error_word, void* stream) {
+  if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return QPKV_ERR_INVALID_ARG;
+  if (num_qo_heads <= 0 || num_kv_heads <= 0) return QPKV_ERR_INVALID_ARG;
+  if (head_dim != 128 || num_qo_heads % num_kv_heads != 0) return QPKV_ERR_UNSUPPORTED;
+  if (batch == 0 || seqlen_q == 0) return QPKV_OK;
+  if (o == nullptr || q_descale == nullptr || k_descale == nullptr || v_descale == nullptr)
+    return QPKV_ERR_INVALID_ARG;
+  if (seqlen_k > 0 && (q == nullptr || k == nullptr || v == nullptr)) return QPKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return QPKV_ERR_INVALID_ARG;
+  int status = QPKV_OK;
+  const cudaError_t e = launch_fp8_attn(q, k, v, batch, seqlen_q, seqlen_k, num_qo_heads,
+                                        num_kv_heads, head_dim, q_descale, k_descale, v_descale,
+                                        softmax_scale, causal, o, lse, error_word,
+                                        static_cast<cudaStream_t>(stream), &status);
+  if (status != QPKV_OK) return static_cast<qpkv_status>(status);
+  return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
+}
+
 }  // extern "C"

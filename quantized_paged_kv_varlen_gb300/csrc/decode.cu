@@ -456,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float (&lsum)[G], const float (&pmax)[G]) {
       const int b = k % kBufs;
       wait_or_abort(&sh.o_full[b], (k / kBufs) & 1, sh, a.err);
+      __syncwarp();   // converged before the .sync.aligned TMEM loads
       tc_fence_after_sync();
       uint32_t r[C::kN];
 #pragma unroll
@@ -508,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- logits with the k-scales folded in
       wait_or_abort(&sh.s_full[b], (k / kBufs) & 1, sh, a.err);
+      __syncwarp();   // converged before the .sync.aligned TMEM loads
       tc_fence_after_sync();
       float l2[kMaxTiles][G];
       float vsc[kMaxTiles];

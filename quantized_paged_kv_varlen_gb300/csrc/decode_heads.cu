@@ -50,6 +50,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ring_sched.cuh"
 
 namespace qpkv {
 namespace {
@@ -194,46 +195,6 @@ __device__ __forceinline__ void hsplit3x2(float x0, float x1, float inv1, float 
   c3 = f32x2_to_e4m3x2(q1 * inv1 * 256.0f, q0 * inv1 * 256.0f);
 }
 
-// Ring order shared by the stream warp, which fills the stages, and the MMA
-// warp, which consumes them in the same order: K tiles run up to two tiles
-// ahead of V tiles (QK(t+2) needs only S(t) read, not P(t) written) and at
-// most one work item ahead.
-struct RingSched {
-  int ko, kj, vo, vj, lead;
-  int ntl0, ntl1;   // tiles of the items in flight, by parity
-  bool kdone;
-  __device__ __forceinline__ int ntl(int o) const { return (o & 1) ? ntl1 : ntl0; }
-  __device__ __forceinline__ void set_ntl(int o, int n) {
-    if (o & 1) ntl1 = n; else ntl0 = n;
-  }
-};
-enum : int { kStepK = 0, kStepV = 1, kStepDone = 2, kStepFail = 3 };
-
-// open(o) waits until item o is published and returns its tile count, 0 at
-// the end of the work, -1 on failure.
-template <class Open>
-__device__ __forceinline__ int ring_next(RingSched& q, Open&& open) {
-  if (q.vj == q.ntl(q.vo) && q.vo < q.ko) {
-    ++q.vo;
-    q.vj = 0;
-  }
-  if (!q.kdone && q.lead < 2) {
-    if (q.kj < q.ntl(q.ko)) return kStepK;
-    if (q.ko == q.vo) {
-      const int n = open(q.ko + 1);
-      if (n < 0) return kStepFail;
-      if (n == 0) {
-        q.kdone = true;
-      } else {
-        ++q.ko;
-        q.kj = 0;
-        q.set_ntl(q.ko, n);
-        return kStepK;
-      }
-    }
-  }
-  return q.vj < q.ntl(q.vo) ? kStepV : kStepDone;
-}
 
 
 template <int D, int G>
@@ -596,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- logits of this row against its kv head's query heads
         const int sb = st % kSBufs;
         hwait(&sh.s_full[sb], (st / kSBufs) & 1, sh, a.err);
+        __syncwarp();   // converged before the .sync.aligned TMEM accesses
         tc_fence_after_sync();
         uint32_t r[32];
         tmem_ld32(tmem + lane_base + sb * kMaxN + w_h0 * kG3, r);
@@ -664,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!o_lane) fo = 1.f;
           hwait(&sh.p_free[(pt - 1) % kPBufs], ((pt - 1) / kPBufs) & 1, sh, a.err);
+          __syncwarp();
           tc_fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
@@ -824,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float so = sh.ep_scale[d][tl];
       const float lse = sh.ep_lse[d][tl];
       hwait(&sh.o_full[d], (o >> 1) & 1, sh, a.err);
+      __syncwarp();
       tc_fence_after_sync();
       float* out = a.part_o + (static_cast<size_t>(slot) * Hq + qh_o) * D;
 #pragma unroll 1

@@ -62,6 +62,12 @@ cudaError_t launch_decode_heads(const DecodePlan& plan, float* float_ws, void* i
 cudaError_t launch_decode_merge(const DecodePlan& plan, const float* float_ws, const void* int_ws,
                                 void* o, float* lse, cudaStream_t stream);
 
+// Dense FP8 attention forward (fp8_attn.cu).
+cudaError_t launch_fp8_attn(const void* q, const void* k, const void* v, int B, int Sq, int Sk,
+                            int Hq, int Hkv, int D, const float* q_descale, const float* k_descale,
+                            const float* v_descale, float softmax_scale, int causal, void* o,
+                            float* lse, int32_t* error_word, cudaStream_t stream, int* status);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
                            void* base, const uint64_t* dims, const uint64_t* strides_bytes,

@@ -182,6 +182,26 @@ def dense_fp8(seed: int = 0, B: int = 4, S: int = 8192, H: int = 32,
     return DenseWorkload(seed, B, S, H, D, 1.0 / np.sqrt(float(D)))
 
 
+def dense_fp8_device(seed: int, B: int, S: int, H: int, D: int, device):
+    """Full-size FP8 inputs made on the GPU: for q, k and v in turn, N(0,1)
+    float32 draws [B, S, H, D] from a seeded device generator, one fp32
+    descale per (b, h) = absmax / 448, codes = torch's float8_e4m3fn cast of
+    x / descale (round to nearest even) viewed as uint8.
+    Returns q8, k8, v8, q_descale, k_descale, v_descale."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = []
+    for _ in range(3):
+        x = torch.randn((B, S, H, D), generator=g, device=device, dtype=torch.float32)
+        scale = x.abs().amax(dim=(1, 3)) / 448.0
+        codes = (x / scale[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        out.append((codes.contiguous(), scale.contiguous()))
+        del x
+    (q8, qd), (k8, kd), (v8, vd) = out
+    return q8, k8, v8, qd, kd, vd
+
+
 # ------------------------------------------------------ MLA sparse decode
 
 @dataclass
