@@ -19,10 +19,12 @@
 //   warps 2-5  online softmax, one thread per query row (TMEM lane), so row
 //              maxima and sums need no shuffles; the running maximum moves
 //              only when a tile beats it by more than 2^8, then the thread
-//              rescales its own O row;
-//   warps 6-9  epilogue: O / l * vd -> bf16, lse.
+//              rescales its own O row; at the end of a work item the same
+//              threads write O / l * vd as bf16 and the lse.
 // S and O are double-buffered in TMEM (4 x 128 columns), so QK of the next
-// tile and the epilogue of the previous work item overlap the softmax.
+// tile overlaps the softmax and the next item's tiles overlap the epilogue.
+// Six warps keep at most two per SM sub-partition, leaving each softmax
+// thread room for its whole 128-logit row in registers.
 //
 // Work: a unit is the pair of q tiles (t, n-1-t) of one (batch, head), so
 // every unit costs the same number of causal K/V tiles; units are dealt to
@@ -39,8 +41,8 @@ namespace {
 
 constexpr int kT = 128;             // q rows per tile = keys per tile = MMA M and N
 constexpr int kD = 128;             // head dim
-constexpr int kThreads = 320;       // 10 warps
-constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpEpi0 = 6;   // softmax: warps 2..5
+constexpr int kThreads = 192;       // 6 warps: at most 2 per SM sub-partition
+constexpr int kWarpLoad = 0, kWarpMma = 1;   // softmax + epilogue: warps 2..5
 constexpr int kSoftmax = 128;
 constexpr int kStages = 10;         // K/V ring, 16 KB each
 constexpr int kTileBytes = kT * kD; // one E4M3 tile
@@ -70,11 +72,7 @@ struct Shared {
   uint64_t s_full[2], p_ready[2];
   uint64_t pv_done;            // one phase per PV step
   uint64_t o_full[2], o_free[2];
-  uint64_t ep_ready[2];
   uint64_t mma_done;
-  float ep_scale[2][kT];       // per row: vd / l (0 when no key is visible)
-  float ep_lse[2][kT];
-  int ep_item[2][3];           // b, h, q tile
   uint32_t tmem_base;
   int abort;
 };
@@ -106,13 +104,11 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity, int* err) 
   }
 }
 
-__device__ __forceinline__ bool warp_await(uint64_t* bar, uint32_t parity, Shared& sh, int* err,
-                                           int lane) {
-  int ok = 1;
-  if (lane == 0) ok = awaitb(bar, parity, sh, err) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
+// 2^x by the hardware approximation (relative error ~2^-22; -inf -> 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // This CTA's work items in order: units blockIdx.x, +grid, ...; a unit is
@@ -172,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.p_ready[d], kSoftmax);
       mbar_init(&sh.o_full[d], 1);
       mbar_init(&sh.o_free[d], kSoftmax);
-      mbar_init(&sh.ep_ready[d], kSoftmax);
     }
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.mma_done, 1);
@@ -321,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain(&sh.mma_done, 0, a.err);
     }
     __syncwarp();
-  } else if (warp < kWarpEpi0) {
+  } else {
     // ---------------------------------------------------------- softmax
     const int sw = warp & 3;
     const int r = sw * 32 + lane;                 // tile row = TMEM lane
@@ -350,19 +345,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t srow = tmem + lane_base + kColS + sb * kT;
         const int climit = lim - j * kT;            // columns c <= climit are visible
         const bool whole = climit >= kT - 1;
-        // ---- pass 1: row maximum (log2 units)
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(srow + 32 * c4, v);
-          tmem_ld_wait();
+        // ---- the row's 128 logits, one TMEM round trip
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        tmem_ld32(srow, v0);
+        tmem_ld32(srow + 32, v1);
+        tmem_ld32(srow + 64, v2);
+        tmem_ld32(srow + 96, v3);
+        tmem_ld_wait();
+        float x[kT];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = (whole || 32 * c4 + i <= climit) ? __uint_as_float(v[i]) * sc : -INFINITY;
-            mx = fmaxf(mx, x);
-          }
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(v0[i]) * sc;
+          x[32 + i] = __uint_as_float(v1[i]) * sc;
+          x[64 + i] = __uint_as_float(v2[i]) * sc;
+          x[96 + i] = __uint_as_float(v3[i]) * sc;
         }
+        if (!whole) {
+#pragma unroll
+          for (int c = 0; c < kT; ++c)
+            if (c > climit) x[c] = -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kT; ++c) mx = fmaxf(mx, x[c]);
         // ---- running maximum, moved only by more than 2^8; then O is
         // rescaled.  The decision is per row, the TMEM access warp-wide (the
         // tcgen05.ld/st forms are .sync.aligned): rows that keep their
@@ -385,31 +390,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t orow = tmem + lane_base + kColO + d * kD;
 #pragma unroll 1
           for (int c4 = 0; c4 < kD / 32; ++c4) {
-            uint32_t v[32];
-            tmem_ld32(orow + 32 * c4, v);
+            uint32_t w[32];
+            tmem_ld32(orow + 32 * c4, w);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-            tmem_st32(orow + 32 * c4, v);
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * f);
+            tmem_st32(orow + 32 * c4, w);
             tmem_st_wait();
           }
         }
-        // ---- pass 2: P = 2^(x - m) as two E4M3 terms hi + lo (about 8
-        // significant bits), packed four keys per column
-        uint32_t pk[32], pl[32];
+        // ---- P = 2^(x - m) as two E4M3 terms hi + lo (about 8 significant
+        // bits), packed four keys per column
         float ls = 0.f;
-#pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(srow + 32 * c4, v);
-          tmem_ld_wait();
+        const float mref = m > -INFINITY ? m : 0.f;   // a row that sees no key gets p = 0
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
+        for (int half = 0; half < 2; ++half) {   // keys [64 half, 64 half + 64)
+          uint32_t pk[16], pl[16];
+#pragma unroll
+          for (int wq = 0; wq < 16; ++wq) {
             float p[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int c = 32 * c4 + i + e;
-              p[e] = (whole || c <= climit) ? exp2f(__uint_as_float(v[i + e]) * sc - m) : 0.f;
+              p[e] = fast_exp2(x[64 * half + 4 * wq + e] - mref);
               ls += p[e];
             }
             const uint16_t h01 = f32x2_to_e4m3x2(p[1], p[0]);
@@ -418,62 +420,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 d23 = e4m3x2_to_f32x2(h23);
             const uint16_t l01 = f32x2_to_e4m3x2(p[1] - d01.y, p[0] - d01.x);
             const uint16_t l23 = f32x2_to_e4m3x2(p[3] - d23.y, p[2] - d23.x);
-            const uint32_t whi = h01 | (static_cast<uint32_t>(h23) << 16);
-            const uint32_t wlo = l01 | (static_cast<uint32_t>(l23) << 16);
-            // keep the register indices static: c4 is a runtime loop index
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              if (w == c4) {
-                pk[8 * w + i / 4] = whi;
-                pl[8 * w + i / 4] = wlo;
-              }
-            }
+            pk[wq] = h01 | (static_cast<uint32_t>(h23) << 16);
+            pl[wq] = l01 | (static_cast<uint32_t>(l23) << 16);
           }
+          tmem_st16(srow + 16 * half, pk);        // columns [0, 32): hi terms
+          tmem_st16(srow + 32 + 16 * half, pl);   // columns [32, 64): lo terms
         }
         l += ls;
-        tmem_st32(srow, pk);        // columns [0, 32): hi terms
-        tmem_st32(srow + 32, pl);   // columns [32, 64): lo terms
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&sh.p_ready[sb]);
         ++st;
       }
-      // ---- hand the item to the epilogue warps (after their item o-2)
-      awaitb(&sh.o_free[d], ((o >> 1) & 1) ^ 1, sh, a.err);
+      // ---- epilogue: O / l * vd -> bf16 and lse, once the item's last PV
+      // has landed; then the O buffer is free for item o+2
       const float vd = __ldg(a.vd + b * a.Hkv + hk);
-      sh.ep_scale[d][r] = l > 0.f ? vd / l : 0.f;
-      sh.ep_lse[d][r] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      if (r == 0) {
-        sh.ep_item[d][0] = b;
-        sh.ep_item[d][1] = h;
-        sh.ep_item[d][2] = qt;
-      }
-      mbar_arrive(&sh.ep_ready[d]);
-    }
-    // stop marker for the epilogue warps
-    {
-      const int d = o & 1;
-      awaitb(&sh.o_free[d], ((o >> 1) & 1) ^ 1, sh, a.err);
-      if (r == 0) sh.ep_item[d][0] = -1;
-      mbar_arrive(&sh.ep_ready[d]);
-    }
-  } else {
-    // --------------------------------------------------------- epilogue
-    const int sw = warp & 3;
-    const int r = sw * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-    for (int o = 0;; ++o) {
-      const int d = o & 1;
-      if (!warp_await(&sh.ep_ready[d], (o >> 1) & 1, sh, a.err, lane)) break;
-      const int b = sh.ep_item[d][0];
-      if (b < 0) break;
-      const int h = sh.ep_item[d][1], qt = sh.ep_item[d][2];
-      const float so = sh.ep_scale[d][r];
-      const float lse = sh.ep_lse[d][r];
+      const float so = l > 0.f ? vd / l : 0.f;
       awaitb(&sh.o_full[d], (o >> 1) & 1, sh, a.err);
       __syncwarp();
       tc_fence_after_sync();
-      const int row = qt * kT + r;
       const bool write = row < a.Sq;
       uint16_t* out = a.o + ((static_cast<size_t>(b) * a.Sq + row) * a.Hq + h) * kD;
       const uint32_t orow = tmem + lane_base + kColO + d * kD;
@@ -492,12 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (write) {
           uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
       tc_fence_before_sync();
       mbar_arrive(&sh.o_free[d]);
-      if (write && a.lse != nullptr) a.lse[(static_cast<size_t>(b) * a.Sq + row) * a.Hq + h] = lse;
+      if (write && a.lse != nullptr)
+        a.lse[(static_cast<size_t>(b) * a.Sq + row) * a.Hq + h] =
+            l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
