@@ -37,6 +37,34 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
   return __half22float2(h);
 }
 
+// Two float32 -> packed f16x2 (round to nearest even); `hi` in the upper half.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float hi, float lo) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Packed f16x2 -> two E4M3 codes (round to nearest even, saturate to +-448).
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+
+// Two E4M3 codes -> packed f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
+
+// Packed f16x2 a - b (round to nearest even).
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
   return e4m3x2_to_f32x2(static_cast<uint16_t>(code)).x;
 }

@@ -332,7 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.advance(a);
       const int nkv = kv_tiles(a, qt);
       const int hk = h / a.G;
-      const float sc = a.scale_log2 * __ldg(a.qd + b * a.Hq + h) * __ldg(a.kd + b * a.Hkv + hk);
+      // logit multiplier (log2 units); kept above 0 so that -inf * sc stays -inf
+      const float sc = fmaxf(a.scale_log2 * __ldg(a.qd + b * a.Hq + h) * __ldg(a.kd + b * a.Hkv + hk),
+                             1e-30f);
       const int row = qt * kT + r;
       // last key this row sees (may be negative: none)
       const int lim = a.causal ? min(a.Sk - 1, row + a.Sk - a.Sq) : a.Sk - 1;
@@ -352,22 +354,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(srow + 64, v2);
         tmem_ld32(srow + 96, v3);
         tmem_ld_wait();
+        // raw logits; masked keys -inf (sc > 0, so max and order carry over)
         float x[kT];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(v0[i]) * sc;
-          x[32 + i] = __uint_as_float(v1[i]) * sc;
-          x[64 + i] = __uint_as_float(v2[i]) * sc;
-          x[96 + i] = __uint_as_float(v3[i]) * sc;
+          x[i] = __uint_as_float(v0[i]);
+          x[32 + i] = __uint_as_float(v1[i]);
+          x[64 + i] = __uint_as_float(v2[i]);
+          x[96 + i] = __uint_as_float(v3[i]);
         }
         if (!whole) {
 #pragma unroll
           for (int c = 0; c < kT; ++c)
             if (c > climit) x[c] = -INFINITY;
         }
-        float mx = -INFINITY;
+        float xm = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kT; ++c) mx = fmaxf(mx, x[c]);
+        for (int c = 0; c < kT; ++c) xm = fmaxf(xm, x[c]);
+        const float mx = xm * sc;   // the tile maximum in log2 units
         // ---- running maximum, moved only by more than 2^8; then O is
         // rescaled.  The decision is per row, the TMEM access warp-wide (the
         // tcgen05.ld/st forms are .sync.aligned): rows that keep their
@@ -399,10 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
         }
-        // ---- P = 2^(x - m) as two E4M3 terms hi + lo (about 8 significant
-        // bits), packed four keys per column
+        // ---- P = 2^(x sc - m) as two E4M3 terms hi + lo (about 8
+        // significant bits, built in f16x2), packed four keys per column
         float ls = 0.f;
-        const float mref = m > -INFINITY ? m : 0.f;   // a row that sees no key gets p = 0
+        const float nm = m > -INFINITY ? -m : 0.f;   // a row that sees no key gets p = 0
 #pragma unroll
         for (int half = 0; half < 2; ++half) {   // keys [64 half, 64 half + 64)
           uint32_t pk[16], pl[16];
@@ -411,15 +415,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              p[e] = fast_exp2(x[64 * half + 4 * wq + e] - mref);
+              p[e] = fast_exp2(fmaf(x[64 * half + 4 * wq + e], sc, nm));
               ls += p[e];
             }
-            const uint16_t h01 = f32x2_to_e4m3x2(p[1], p[0]);
-            const uint16_t h23 = f32x2_to_e4m3x2(p[3], p[2]);
-            const float2 d01 = e4m3x2_to_f32x2(h01);
-            const float2 d23 = e4m3x2_to_f32x2(h23);
-            const uint16_t l01 = f32x2_to_e4m3x2(p[1] - d01.y, p[0] - d01.x);
-            const uint16_t l23 = f32x2_to_e4m3x2(p[3] - d23.y, p[2] - d23.x);
+            const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
+            const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
+            const uint16_t h01 = f16x2_to_e4m3x2(f01);
+            const uint16_t h23 = f16x2_to_e4m3x2(f23);
+            const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(f01, e4m3x2_to_f16x2(h01)));
+            const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(f23, e4m3x2_to_f16x2(h23)));
             pk[wq] = h01 | (static_cast<uint32_t>(h23) << 16);
             pl[wq] = l01 | (static_cast<uint32_t>(l23) << 16);
           }
