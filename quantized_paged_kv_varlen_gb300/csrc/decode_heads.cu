@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (o & 1) it1 = it; else it0 = it;
       return it.b < 0 ? 0 : htiles(it, nt);
     };
-    RingSched q{0, 0, 0, 0, 0, 0, 0, false};
+    RingSched q{0, 0, 0, 0, 0, 0, 0, false, 2};
     q.ntl0 = open_item(0);
     if (q.ntl0 > 0) {
       while (true) {
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!is_qk) mbar_arrive(&sh.desc_free[o & 1]);   // the QK side releases by commit
         return it.b < 0 ? 0 : htiles(it, nt);
       };
-      RingSched q{0, 0, 0, 0, 0, 0, 0, false};
+      RingSched q{0, 0, 0, 0, 0, 0, 0, false, 2};
       q.ntl0 = open_item(0);
       if (q.ntl0 > 0) {
         while (true) {

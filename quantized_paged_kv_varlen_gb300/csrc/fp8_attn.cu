@@ -8,7 +8,7 @@
 //
 // One persistent CTA per SM, 10 warps:
 //   warp 0     TMA loads: the work item's 128-row Q tile, then its K and V
-//              tiles in the ring order K(0) K(1) | K(2) V(0) | K(3) V(1) ...
+//              tiles in the ring order K(0) K(1) K(2) | V(0) K(3) | V(1) ...
 //   warp 1     tcgen05 MMAs, one issuing lane:
 //                S[128 q x 128 k] = Q[128 x D] . K_tile[128 x D]^T   (FP8)
 //                O[128 q x D]   += P[128 q x 128 k] . V_tile[128 k x D]
@@ -16,15 +16,16 @@
 //              wrote it over the first 64 columns of its S buffer as two
 //              E4M3 terms hi + lo (K = 256: hi rows, then lo rows, each
 //              against the same V tile), about 8 significant bits;
-//   warps 2-5  online softmax, one thread per query row (TMEM lane), so row
-//              maxima and sums need no shuffles; the running maximum moves
-//              only when a tile beats it by more than 2^8, then the thread
-//              rescales its own O row; at the end of a work item the same
-//              threads write O / l * vd as bf16 and the lse.
-// S and O are double-buffered in TMEM (4 x 128 columns), so QK of the next
-// tile overlaps the softmax and the next item's tiles overlap the epilogue.
-// Six warps keep at most two per SM sub-partition, leaving each softmax
-// thread room for its whole 128-logit row in registers.
+//   warps 2-9  online softmax, two threads per query row (TMEM lane): warps
+//              2-5 take the row's keys [0, 64), warps 6-9 keys [64, 128);
+//              the pair combines its maxima through shared memory at a
+//              64-thread named barrier.  The running maximum moves only
+//              when a tile beats it by more than 2^8, then the row's O is
+//              rescaled.  At the end of a work item the same threads write
+//              O / l * vd as bf16 and the lse.
+// TMEM holds three S buffers and O (4 x 128 columns): QK runs up to three
+// tiles ahead of PV (K tiles three ahead of V in the ring), so S(t+1) and
+// S(t+2) are computed while the softmax works on tile t.
 //
 // Work: a unit is the pair of q tiles (t, n-1-t) of one (batch, head), so
 // every unit costs the same number of causal K/V tiles; units are dealt to
@@ -41,15 +42,16 @@ namespace {
 
 constexpr int kT = 128;             // q rows per tile = keys per tile = MMA M and N
 constexpr int kD = 128;             // head dim
-constexpr int kThreads = 192;       // 6 warps: at most 2 per SM sub-partition
-constexpr int kWarpLoad = 0, kWarpMma = 1;   // softmax + epilogue: warps 2..5
-constexpr int kSoftmax = 128;
+constexpr int kThreads = 320;       // 10 warps
+constexpr int kWarpLoad = 0, kWarpMma = 1;   // softmax + epilogue: warps 2..9
+constexpr int kSoftmax = 256;       // two threads per query row
 constexpr int kStages = 10;         // K/V ring, 16 KB each
 constexpr int kTileBytes = kT * kD; // one E4M3 tile
 constexpr int kSmem = (2 + kStages) * kTileBytes + 1024;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint32_t kColS = 0;       // S buffers: columns [0, 128), [128, 256)
-constexpr uint32_t kColO = 256;     // O buffers: columns [256, 384), [384, 512)
+constexpr int kSBufs = 3;           // S ring in TMEM: QK(t) waits only for PV(t-3)
+constexpr uint32_t kColS = 0;       // S buffers: columns [0, 128), [128, 256), [256, 384)
+constexpr uint32_t kColO = 384;     // O: columns [384, 512)
 
 struct AttnArgs {
   int B, Sq, Sk, Hq, Hkv, G;
@@ -69,10 +71,12 @@ struct AttnArgs {
 struct Shared {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full[2], q_free[2];
-  uint64_t s_full[2], p_ready[2];
-  uint64_t pv_done;            // one phase per PV step
-  uint64_t o_full[2], o_free[2];
+  uint64_t s_full[kSBufs], p_ready[kSBufs];
+  uint64_t pv_done[2];         // PV step t completes a phase of pv_done[t & 1]
+  uint64_t o_full, o_free;      // one phase per work item
   uint64_t mma_done;
+  float pmax[2][2][kT];        // [tile parity][column half][row] partial row maxima
+  float psum[2][kT];           // [column half][row] partial softmax denominators
   uint32_t tmem_base;
   int abort;
 };
@@ -164,12 +168,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sh.q_full[d], 1);
       mbar_init(&sh.q_free[d], 1);
-      mbar_init(&sh.s_full[d], 1);
-      mbar_init(&sh.p_ready[d], kSoftmax);
-      mbar_init(&sh.o_full[d], 1);
-      mbar_init(&sh.o_free[d], kSoftmax);
     }
-    mbar_init(&sh.pv_done, 1);
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(&sh.s_full[b], 1);
+      mbar_init(&sh.p_ready[b], kSoftmax);
+    }
+    mbar_init(&sh.o_full, 1);
+    mbar_init(&sh.o_free, kSoftmax);
+    mbar_init(&sh.pv_done[0], 1);
+    mbar_init(&sh.pv_done[1], 1);
     mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
     fence_mbar_init();
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pos;
         return true;
       };
-      RingSched q{0, 0, 0, 0, 0, 0, 0, false};
+      RingSched q{0, 0, 0, 0, 0, 0, 0, false, 3};
       q.ntl0 = open_item(0);
       if (q.ntl0 > 0) {
         while (true) {
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int pos = 0, st = 0, pvc = 0;
       auto qk = [&](int o, int j, int ntl) -> bool {
-        const int sb = st & 1;
+        const int sb = st % kSBufs;
         const int s = pos % kStages;
         if (!awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err)) return false;
         tc_fence_after_sync();
@@ -273,10 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto pv = [&](int o, int j, int ntl) -> bool {
-        const int sb = pvc & 1;
+        const int sb = pvc % kSBufs;
         const int s = pos % kStages;
-        if (j == 0 && !awaitb(&sh.o_free[o & 1], ((o >> 1) & 1) ^ 1, sh, a.err)) return false;
-        if (!awaitb(&sh.p_ready[sb], (pvc >> 1) & 1, sh, a.err) ||
+        // O is single-buffered: item o-1's epilogue has read it
+        if (j == 0 && !awaitb(&sh.o_free, (o & 1) ^ 1, sh, a.err)) return false;
+        if (!awaitb(&sh.p_ready[sb], (pvc / kSBufs) & 1, sh, a.err) ||
             !awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err))
           return false;
         tc_fence_after_sync();
@@ -285,16 +293,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // against the same V rows
 #pragma unroll
         for (int kk = 0; kk < 2 * kT / 32; ++kk)
-          tc_mma_f8_tmem_a(tmem + kColO + (o & 1) * kD, tmem + kColS + sb * kT + 8 * kk,
+          tc_mma_f8_tmem_a(tmem + kColO, tmem + kColS + sb * kT + 8 * kk,
                            db0 + (32 * kD / 16) * (kk & 3), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.empty[s]);
-        tc_commit(&sh.pv_done);
-        if (j == ntl - 1) tc_commit(&sh.o_full[o & 1]);
+        tc_commit(&sh.pv_done[pvc & 1]);
+        if (j == ntl - 1) tc_commit(&sh.o_full);
         ++pos;
         ++pvc;
         return true;
       };
-      RingSched q{0, 0, 0, 0, 0, 0, 0, false};
+      RingSched q{0, 0, 0, 0, 0, 0, 0, false, 3};
       q.ntl0 = open_item(0);
       if (q.ntl0 > 0) {
         while (true) {
@@ -317,16 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------- softmax
-    const int sw = warp & 3;
+    // ---------------------------------------------- softmax and epilogue
+    // Two threads per query row: warps 2-5 take columns [0, 64), warps
+    // 6-9 columns [64, 128) of the same TMEM lanes; a row's pair meets at a
+    // 64-thread named barrier to combine the row maximum.
+    const int sw = warp & 3;                      // TMEM lane quarter
+    const int half = (warp - 2) >> 2;             // column half
     const int r = sw * 32 + lane;                 // tile row = TMEM lane
+    const uint32_t bar_id = 1 + sw;               // the pair's named barrier
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
     Items it;
     it.start();
     int st = 0;
-    int o = 0;
-    for (; it.valid(a); ++o) {
-      const int d = o & 1;
+    for (int o = 0; it.valid(a); ++o) {
       int b, h, qt;
       it.get(a, b, h, qt);
       it.advance(a);
@@ -340,41 +351,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lim = a.causal ? min(a.Sk - 1, row + a.Sk - a.Sq) : a.Sk - 1;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkv; ++j) {
-        const int sb = st & 1;
-        awaitb(&sh.s_full[sb], (st >> 1) & 1, sh, a.err);
+        const int sb = st % kSBufs;
+        awaitb(&sh.s_full[sb], (st / kSBufs) & 1, sh, a.err);
         __syncwarp();   // converged before the .sync.aligned TMEM accesses
         tc_fence_after_sync();
         const uint32_t srow = tmem + lane_base + kColS + sb * kT;
-        const int climit = lim - j * kT;            // columns c <= climit are visible
-        const bool whole = climit >= kT - 1;
-        // ---- the row's 128 logits, one TMEM round trip
-        uint32_t v0[32], v1[32], v2[32], v3[32];
-        tmem_ld32(srow, v0);
-        tmem_ld32(srow + 32, v1);
-        tmem_ld32(srow + 64, v2);
-        tmem_ld32(srow + 96, v3);
+        const int climit = lim - j * kT - 64 * half;   // this half's columns c <= climit are visible
+        const bool whole = climit >= 63;
+        uint32_t v0[32], v1[32];
+        tmem_ld32(srow + 64 * half, v0);
+        tmem_ld32(srow + 64 * half + 32, v1);
         tmem_ld_wait();
         // raw logits; masked keys -inf (sc > 0, so max and order carry over)
-        float x[kT];
+        float x[64];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           x[i] = __uint_as_float(v0[i]);
           x[32 + i] = __uint_as_float(v1[i]);
-          x[64 + i] = __uint_as_float(v2[i]);
-          x[96 + i] = __uint_as_float(v3[i]);
         }
         if (!whole) {
 #pragma unroll
-          for (int c = 0; c < kT; ++c)
+          for (int c = 0; c < 64; ++c)
             if (c > climit) x[c] = -INFINITY;
         }
         float xm = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kT; ++c) xm = fmaxf(xm, x[c]);
-        const float mx = xm * sc;   // the tile maximum in log2 units
+        for (int c = 0; c < 64; ++c) xm = fmaxf(xm, x[c]);
+        sh.pmax[st & 1][half][r] = xm;
+        named_barrier(bar_id, 64);
+        xm = fmaxf(xm, sh.pmax[st & 1][half ^ 1][r]);
+        const float mx = xm * sc;   // the row's tile maximum in log2 units
         // ---- running maximum, moved only by more than 2^8; then O is
-        // rescaled.  The decision is per row, the TMEM access warp-wide (the
-        // tcgen05.ld/st forms are .sync.aligned): rows that keep their
+        // rescaled.  Both threads of a row take the same decision; the
+        // TMEM access is warp-wide (.sync.aligned), rows that keep their
         // maximum use the factor 1.
         float f = 1.f;
         bool need = false;
@@ -387,69 +396,71 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
         }
         if (__any_sync(0xffffffffu, need)) {
-          // the previous PV of this item must have finished writing O
-          awaitb(&sh.pv_done, (st - 1) & 1, sh, a.err);
+          // the previous PV of this item must have finished writing O.  Up
+          // to two PV steps can be in flight here (S(t) landing implies only
+          // PV(t-3) done), hence two barriers taken in turn.
+          awaitb(&sh.pv_done[(st - 1) & 1], ((st - 1) >> 1) & 1, sh, a.err);
           __syncwarp();
           tc_fence_after_sync();
-          const uint32_t orow = tmem + lane_base + kColO + d * kD;
+          const uint32_t orow = tmem + lane_base + kColO + 64 * half;
 #pragma unroll 1
-          for (int c4 = 0; c4 < kD / 32; ++c4) {
+          for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t w[32];
-            tmem_ld32(orow + 32 * c4, w);
+            tmem_ld32(orow + 32 * c2, w);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * f);
-            tmem_st32(orow + 32 * c4, w);
+            tmem_st32(orow + 32 * c2, w);
             tmem_st_wait();
           }
         }
         // ---- P = 2^(x sc - m) as two E4M3 terms hi + lo (about 8
         // significant bits, built in f16x2), packed four keys per column
-        float ls = 0.f;
         const float nm = m > -INFINITY ? -m : 0.f;   // a row that sees no key gets p = 0
+        uint32_t pk[16], pl[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {   // keys [64 half, 64 half + 64)
-          uint32_t pk[16], pl[16];
+        for (int wq = 0; wq < 16; ++wq) {
+          float p[4];
 #pragma unroll
-          for (int wq = 0; wq < 16; ++wq) {
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              p[e] = fast_exp2(fmaf(x[64 * half + 4 * wq + e], sc, nm));
-              ls += p[e];
-            }
-            const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
-            const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
-            const uint16_t h01 = f16x2_to_e4m3x2(f01);
-            const uint16_t h23 = f16x2_to_e4m3x2(f23);
-            const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(f01, e4m3x2_to_f16x2(h01)));
-            const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(f23, e4m3x2_to_f16x2(h23)));
-            pk[wq] = h01 | (static_cast<uint32_t>(h23) << 16);
-            pl[wq] = l01 | (static_cast<uint32_t>(l23) << 16);
+          for (int e = 0; e < 4; ++e) {
+            p[e] = fast_exp2(fmaf(x[4 * wq + e], sc, nm));
+            l += p[e];
           }
-          tmem_st16(srow + 16 * half, pk);        // columns [0, 32): hi terms
-          tmem_st16(srow + 32 + 16 * half, pl);   // columns [32, 64): lo terms
+          const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
+          const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
+          const uint16_t h01 = f16x2_to_e4m3x2(f01);
+          const uint16_t h23 = f16x2_to_e4m3x2(f23);
+          const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(f01, e4m3x2_to_f16x2(h01)));
+          const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(f23, e4m3x2_to_f16x2(h23)));
+          pk[wq] = h01 | (static_cast<uint32_t>(h23) << 16);
+          pl[wq] = l01 | (static_cast<uint32_t>(l23) << 16);
         }
-        l += ls;
+        tmem_st16(srow + 16 * half, pk);        // columns [0, 32): hi terms
+        tmem_st16(srow + 32 + 16 * half, pl);   // columns [32, 64): lo terms
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(&sh.p_ready[sb]);
         ++st;
       }
-      // ---- epilogue: O / l * vd -> bf16 and lse, once the item's last PV
-      // has landed; then the O buffer is free for item o+2
+      // ---- the row's denominator: this half's partial sum plus the other's
+      sh.psum[half][r] = l;
+      named_barrier(bar_id, 64);
+      const float lt = l + sh.psum[half ^ 1][r];
+      named_barrier(bar_id, 64);   // psum may be rewritten at the next item
+      // ---- epilogue: this half's 64 columns of O / l * vd -> bf16, and the
+      // lse, once the item's last PV has landed; then O is free for item o+2
       const float vd = __ldg(a.vd + b * a.Hkv + hk);
-      const float so = l > 0.f ? vd / l : 0.f;
-      awaitb(&sh.o_full[d], (o >> 1) & 1, sh, a.err);
+      const float so = lt > 0.f ? vd / lt : 0.f;
+      awaitb(&sh.o_full, o & 1, sh, a.err);
       __syncwarp();
       tc_fence_after_sync();
       const bool write = row < a.Sq;
-      uint16_t* out = a.o + ((static_cast<size_t>(b) * a.Sq + row) * a.Hq + h) * kD;
-      const uint32_t orow = tmem + lane_base + kColO + d * kD;
+      uint16_t* out = a.o + ((static_cast<size_t>(b) * a.Sq + row) * a.Hq + h) * kD + 64 * half;
+      const uint32_t orow = tmem + lane_base + kColO + 64 * half;
 #pragma unroll 1
-      for (int c4 = 0; c4 < kD / 32; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t v[32];
-        tmem_ld32(orow + 32 * c4, v);
+        tmem_ld32(orow + 32 * c2, v);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
@@ -459,20 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = *reinterpret_cast<const uint32_t*>(&t);
         }
         if (write) {
-          uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c4);
+          uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c2);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(&sh.o_free[d]);
-      if (write && a.lse != nullptr)
+      mbar_arrive(&sh.o_free);
+      if (write && half == 0 && a.lse != nullptr)
         a.lse[(static_cast<size_t>(b) * a.Sq + row) * a.Hq + h] =
-            l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
     }
   }
-
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kWarpMma) {

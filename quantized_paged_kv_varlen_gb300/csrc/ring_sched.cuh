@@ -4,12 +4,13 @@
 
 namespace qpkv {
 
-// K tiles run up to two tiles ahead of V tiles and at most one work item
-// ahead; every party walking the schedule sees the same stage order.
+// K tiles run up to maxlead tiles ahead of V tiles and at most one work
+// item ahead; every party walking the schedule sees the same stage order.
 struct RingSched {
   int ko, kj, vo, vj, lead;
   int ntl0, ntl1;   // tiles of the items in flight, by parity
   bool kdone;
+  int maxlead;
   __device__ __forceinline__ int ntl(int o) const { return (o & 1) ? ntl1 : ntl0; }
   __device__ __forceinline__ void set_ntl(int o, int n) {
     if (o & 1) ntl1 = n; else ntl0 = n;
@@ -25,7 +26,7 @@ __device__ __forceinline__ int ring_next(RingSched& q, Open&& open) {
     ++q.vo;
     q.vj = 0;
   }
-  if (!q.kdone && q.lead < 2) {
+  if (!q.kdone && q.lead < q.maxlead) {
     if (q.kj < q.ntl(q.ko)) return kStepK;
     if (q.ko == q.vo) {
       const int n = open(q.ko + 1);
