@@ -9,7 +9,8 @@
 // One persistent CTA per SM, 10 warps:
 //   warp 0     TMA loads: the work item's 128-row Q tile, then its K and V
 //              tiles in the ring order K(0) K(1) K(2) | V(0) K(3) | V(1) ...
-//   warp 1     tcgen05 MMAs, one issuing lane:
+//   warps 1, 10  tcgen05 MMAs, one issuing lane each (QK on warp 1, PV on
+//              warp 10):
 //                S[128 q x 128 k] = Q[128 x D] . K_tile[128 x D]^T   (FP8)
 //                O[128 q x D]   += P[128 q x 128 k] . V_tile[128 k x D]
 //              P is read straight from tensor memory, where the softmax
@@ -42,8 +43,8 @@ namespace {
 
 constexpr int kT = 128;             // q rows per tile = keys per tile = MMA M and N
 constexpr int kD = 128;             // head dim
-constexpr int kThreads = 320;       // 10 warps
-constexpr int kWarpLoad = 0, kWarpMma = 1;   // softmax + epilogue: warps 2..9
+constexpr int kThreads = 352;       // 11 warps
+constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpPv = 10;   // softmax + epilogue: warps 2..9
 constexpr int kSoftmax = 256;       // two threads per query row
 constexpr int kStages = 10;         // K/V ring, 16 KB each
 constexpr int kTileBytes = kT * kD; // one E4M3 tile
@@ -72,9 +73,9 @@ struct Shared {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full[2], q_free[2];
   uint64_t s_full[kSBufs], p_ready[kSBufs];
-  uint64_t pv_done[2];         // PV step t completes a phase of pv_done[t & 1]
+  uint64_t pv_done[kSBufs];    // PV step t completes a phase of pv_done[t % 3]
   uint64_t o_full, o_free;      // one phase per work item
-  uint64_t mma_done;
+  uint64_t mma_done[2];         // QK and PV issuers' MMAs complete
   float pmax[2][2][kT];        // [tile parity][column half][row] partial row maxima
   float psum[2][kT];           // [column half][row] partial softmax denominators
   uint32_t tmem_base;
@@ -175,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sh.o_full, 1);
     mbar_init(&sh.o_free, kSoftmax);
-    mbar_init(&sh.pv_done[0], 1);
-    mbar_init(&sh.pv_done[1], 1);
-    mbar_init(&sh.mma_done, 1);
+    for (int b = 0; b < kSBufs; ++b) mbar_init(&sh.pv_done[b], 1);
+    mbar_init(&sh.mma_done[0], 1);
+    mbar_init(&sh.mma_done[1], 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -241,8 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain(&sh.full[i % kStages], (i / kStages) & 1, a.err);
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || warp == kWarpPv) {
     // -------------------------------------------------------------- MMA
+    // Lane 0 of warp 1 issues the QK MMAs, lane 0 of warp 10 the PV MMAs;
+    // both walk the ring schedule and skip the other side's stages.  QK(t)
+    // overwrites the S buffer that held P(t-3), so it first waits for
+    // PV(t-3) to complete.
+    const bool is_qk = warp == kWarpMma;
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, kT, kT);
       const uint32_t idesc_pv = make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, kT, kD);
@@ -258,13 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b, h, qt;
         it.get(a, b, h, qt);
         it.advance(a);
-        if (!awaitb(&sh.q_full[o & 1], (o >> 1) & 1, sh, a.err)) return -1;
+        if (is_qk && !awaitb(&sh.q_full[o & 1], (o >> 1) & 1, sh, a.err)) return -1;
         return kv_tiles(a, qt);
       };
       int pos = 0, st = 0, pvc = 0;
       auto qk = [&](int o, int j, int ntl) -> bool {
         const int sb = st % kSBufs;
         const int s = pos % kStages;
+        if (st >= kSBufs &&
+            !awaitb(&sh.pv_done[sb], ((st - kSBufs) / kSBufs) & 1, sh, a.err))   // PV(st - 3) done
+          return false;
         if (!awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err)) return false;
         tc_fence_after_sync();
         const uint64_t da0 = qdesc0 + static_cast<uint64_t>(((o & 1) * kTileBytes) >> 4);
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_f8_tmem_a(tmem + kColO, tmem + kColS + sb * kT + 8 * kk,
                            db0 + (32 * kD / 16) * (kk & 3), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.empty[s]);
-        tc_commit(&sh.pv_done[pvc & 1]);
+        tc_commit(&sh.pv_done[sb]);
         if (j == ntl - 1) tc_commit(&sh.o_full);
         ++pos;
         ++pvc;
@@ -308,11 +317,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (true) {
           const int step = ring_next(q, open_item);
           if (step == kStepK) {
-            if (!qk(q.ko, q.kj, q.ntl(q.ko))) break;
+            if (is_qk) {
+              if (!qk(q.ko, q.kj, q.ntl(q.ko))) break;
+            } else {
+              ++pos;
+            }
             ++q.kj;
             ++q.lead;
           } else if (step == kStepV) {
-            if (!pv(q.vo, q.vj, q.ntl(q.vo))) break;
+            if (!is_qk) {
+              if (!pv(q.vo, q.vj, q.ntl(q.vo))) break;
+            } else {
+              ++pos;
+            }
             ++q.vj;
             --q.lead;
           } else {
@@ -320,11 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_commit(&sh.mma_done);
-      drain(&sh.mma_done, 0, a.err);
+      // every MMA issued here completes before TMEM is released
+      tc_commit(&sh.mma_done[is_qk ? 0 : 1]);
+      drain(&sh.mma_done[is_qk ? 0 : 1], 0, a.err);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kWarpPv) {
     // ---------------------------------------------- softmax and epilogue
     // Two threads per query row: warps 2-5 take columns [0, 64), warps
     // 6-9 columns [64, 128) of the same TMEM lanes; a row's pair meets at a
@@ -396,10 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
         }
         if (__any_sync(0xffffffffu, need)) {
-          // the previous PV of this item must have finished writing O.  Up
-          // to two PV steps can be in flight here (S(t) landing implies only
-          // PV(t-3) done), hence two barriers taken in turn.
-          awaitb(&sh.pv_done[(st - 1) & 1], ((st - 1) >> 1) & 1, sh, a.err);
+          // the previous PV of this item must have finished writing O (PV
+          // steps t-1 and t-2 may still be in flight; t+2 cannot be done)
+          awaitb(&sh.pv_done[(st - 1) % kSBufs], ((st - 1) / kSBufs) & 1, sh, a.err);
           __syncwarp();
           tc_fence_after_sync();
           const uint32_t orow = tmem + lane_base + kColO + 64 * half;
