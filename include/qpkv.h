@@ -53,6 +53,7 @@ typedef int32_t qpkv_status;
 #define QPKV_DEV_ERR_TIMEOUT 1   /* an internal pipeline wait gave up after ~2 s */
 #define QPKV_DEV_ERR_BAD_PAGE 2  /* a block_table entry outside [0, num_pages) was skipped */
 #define QPKV_DEV_ERR_BAD_INDEX 4 /* a sparse index outside [0, L_kv) was skipped */
+#define QPKV_DEV_ERR_BAD_LENGTH 8 /* a sequence length does not fit the arrays described; skipped */
 
 /* Text of a status code (static storage, never NULL). */
 const char* qpkv_status_string(qpkv_status status);
@@ -62,7 +63,8 @@ int32_t qpkv_version(void);
 
 /* sizeof of the parameter structs below, so that bindings in other
  * languages can check their mirror of the layout:
- * which = 0 -> qpkv_write_params.  Unknown `which` returns 0. */
+ * which = 0 -> qpkv_write_params, 1 -> qpkv_prefill_params.  Unknown
+ * `which` returns 0. */
 size_t qpkv_struct_size(int32_t which);
 
 /* -------------------------------------------------------------- RoPE table
@@ -292,6 +294,81 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
                               const float* k_descale, const float* v_descale,
                               float softmax_scale, int32_t causal, void* o, float* lse,
                               int32_t* error_word, void* stream);
+
+/* ------------------------------------------------- varlen prefill (INT8 QK)
+ * Causal varlen prefill over a paged cache in the layout QPKV_WRITE_INT8_
+ * BLOCK128_ROPE writes ("[Feature] Sage Attention Support Varlen & write kv
+ * cache BF16/FP16", Description items 1-3; "KvQuantSparseFlashAttention"
+ * README 计算公式, 参数说明 rows actual_seq_lengths_query /
+ * actual_seq_lengths_kv / block_table / sparse_mode):
+ *   logit(i, j) = sm_scale * sq[b, i/128, h] * sk[b, j/128, hk] * (q8_i . k8_j)
+ *   o_i = sum_j softmax_j(logit(i, .)) * v_j       (v bf16, no scale)
+ *   lse_i = ln sum_j exp(logit(i, j))
+ * Query i of sequence b (0-based, L_q = its row count) sees key j iff
+ * j < L_kv[b] and, when causal, j <= i + L_kv[b] - L_q (bottom-right).  The
+ * kv head of q head h is h / (Hq / Hkv).  Rows that see no key get o = 0
+ * and lse = -inf.
+ *
+ * Arrays (device; the caller owns all memory):
+ *   cu_seqlens_q  int32 [B] inclusive prefix sums; sequence b owns q/o rows
+ *                 [cu[b-1], cu[b]) (cu[-1] = 0), cu[B-1] <= num_tokens
+ *   seqlens_kv    int32 [B] tokens in the cache per sequence (L_kv)
+ *   block_table   int32 [B, bt_stride]: key j lives at pool row
+ *                 block_table[b][j / page_size] * page_size + j % page_size;
+ *                 entries past L_kv are never read
+ *   q             int8 [T, Hq, 128] codes (TND), q_block_scale fp32 [B,
+ *                 num_blocks, Hq] (query block of row i is i / 128)
+ *   k_pool        int8 [P, page_size, Hkv, 128], k_block_scale fp32
+ *                 [B, num_blocks, Hkv] (key block of key j is j / 128)
+ *   v_pool        bf16 [P, page_size, Hkv, 128]
+ *   o             bf16 [T, Hq, 128]; lse fp32 [T, Hq] or NULL
+ *   workspace     qpkv_prefill_workspace_bytes(B, T, Hq) bytes of device
+ *                 memory, overwritten by every call (the call's work order)
+ *   error_word    int32 or NULL: QPKV_DEV_ERR_BAD_PAGE (a block_table entry
+ *                 outside [0, P) read as zeros), QPKV_DEV_ERR_BAD_LENGTH (a
+ *                 sequence whose lengths exceed num_blocks * 128, the
+ *                 block_table row or num_tokens: its rows are zeroed),
+ *                 QPKV_DEV_ERR_TIMEOUT.
+ * Supported: head_dim 128, page_size a multiple of 16 that divides 128 or
+ * is a multiple of 128, Hq % Hkv == 0.  q, k_pool, v_pool, o 16-byte
+ * aligned.  sm_scale <= 0 selects 1/sqrt(128).
+ * Errors: INVALID_ARG (null required pointer, negative or zero sizes,
+ * misaligned pointer), UNSUPPORTED (head_dim, page_size, head grouping),
+ * WORKSPACE_TOO_SMALL, CUDA (launch). */
+typedef struct qpkv_prefill_params {
+  int32_t num_seqs;      /* B */
+  int32_t num_tokens;    /* T: rows of q, o, lse */
+  int32_t num_heads_q;   /* Hq */
+  int32_t num_heads_kv;  /* Hkv */
+  int32_t head_dim;      /* 128 */
+  int32_t page_size;
+  int32_t num_pages;     /* P */
+  int32_t bt_stride;     /* row stride of block_table */
+  int32_t num_blocks;    /* dim 1 of q_block_scale / k_block_scale */
+  int32_t causal;
+  float sm_scale;
+  int32_t pad0;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqlens_kv;
+  const int32_t* block_table;
+  const void* q;
+  const float* q_block_scale;
+  const void* k_pool;
+  const float* k_block_scale;
+  const void* v_pool;
+  void* o;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* error_word;
+} qpkv_prefill_params;
+
+/* Device workspace bytes qpkv_prefill_paged needs for num_seqs sequences of
+ * num_tokens query rows in total and num_heads_q query heads (0 for a
+ * negative argument). */
+size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads_q);
+
+qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* params, void* stream);
 
 #ifdef __cplusplus
 }

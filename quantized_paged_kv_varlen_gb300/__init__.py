@@ -62,6 +62,18 @@ class WriteParams(ctypes.Structure):
             "q_block_scale", "slot_mapping", "error_word")]
 
 
+
+class PrefillParams(ctypes.Structure):
+    """Mirror of ``qpkv_prefill_params`` (include/qpkv.h)."""
+    _fields_ = [(n, _i32) for n in (
+        "num_seqs", "num_tokens", "num_heads_q", "num_heads_kv", "head_dim", "page_size",
+        "num_pages", "bt_stride", "num_blocks", "causal")] + [
+        ("sm_scale", ctypes.c_float), ("pad0", _i32)] + [
+        (n, _p) for n in (
+            "cu_seqlens_q", "seqlens_kv", "block_table", "q", "q_block_scale", "k_pool",
+            "k_block_scale", "v_pool", "o", "lse", "workspace")] + [
+        ("workspace_bytes", ctypes.c_size_t), ("error_word", _p)]
+
 def _declare(lib):
     S = ctypes.c_size_t
     P64 = ctypes.POINTER(ctypes.c_int64)
@@ -85,6 +97,8 @@ def _declare(lib):
                                       _i32, _p, _i32, ctypes.c_float, _p, _p, _p, _p]),
         "qpkv_fp8_attn_fwd": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p,
                                      ctypes.c_float, _i32, _p, _p, _p, _p]),
+        "qpkv_prefill_workspace_bytes": (S, [_i32, _i32, _i32]),
+        "qpkv_prefill_paged": (_i32, [ctypes.POINTER(PrefillParams), _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -398,4 +412,62 @@ def fp8_attn_fwd(q, k, v, q_descale, k_descale, v_descale, softmax_scale=None, c
                                  float(softmax_scale) if softmax_scale else 0.0,
                                  1 if causal else 0, _ptr(out), _ptr(lse), _ptr(error_word),
                                  _stream()), "qpkv_fp8_attn_fwd")
+    return out
+
+
+def prefill_workspace(num_seqs, num_tokens, num_heads_q, device="cuda"):
+    """A device workspace large enough for ``prefill_paged`` on num_seqs
+    sequences of num_tokens query rows and num_heads_q heads."""
+    torch = _torch()
+    n = int(load().qpkv_prefill_workspace_bytes(int(num_seqs), int(num_tokens), int(num_heads_q)))
+    return torch.empty(((n + 15) // 16) * 16, dtype=torch.uint8, device=device)
+
+
+def prefill_paged(q8, q_block_scale, k_pool, k_block_scale, v_pool, block_table, cu_seqlens_q,
+                  seqlens_kv, sm_scale=None, causal=True, out=None, lse=None, workspace=None,
+                  error_word=None):
+    """Varlen prefill with INT8 Q/K (block-128 scales) and bf16 V over a paged
+    cache: q8 int8 [T, Hq, 128]; k_pool int8 / v_pool bf16 [P, ps, Hkv, 128];
+    scales fp32 [B, NB, H]; returns bf16 O [T, Hq, 128] (``lse`` fp32 [T, Hq]
+    filled when given)."""
+    torch = _torch()
+    lib = load()
+    _need(q8, "q8", torch.int8, 3)
+    _need(k_pool, "k_pool", torch.int8, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(q_block_scale, "q_block_scale", torch.float32, 3)
+    _need(k_block_scale, "k_block_scale", torch.float32, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(seqlens_kv, "seqlens_kv", torch.int32, 1)
+    T, Hq, D = q8.shape
+    P, ps, Hkv, _ = k_pool.shape
+    B = cu_seqlens_q.shape[0]
+    if tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("v_pool must match k_pool's shape")
+    if seqlens_kv.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("seqlens_kv / block_table must have one row per sequence")
+    NB = q_block_scale.shape[1]
+    if tuple(q_block_scale.shape) != (B, NB, Hq) or tuple(k_block_scale.shape) != (B, NB, Hkv):
+        raise ValueError("block scales must be [B, NB, Hq] and [B, NB, Hkv]")
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = prefill_workspace(B, T, Hq, q8.device)
+    prm = PrefillParams()
+    prm.num_seqs, prm.num_tokens, prm.num_heads_q, prm.num_heads_kv = B, T, Hq, Hkv
+    prm.head_dim, prm.page_size, prm.num_pages = D, ps, P
+    prm.bt_stride = block_table.shape[1]
+    prm.num_blocks = NB
+    prm.causal = 1 if causal else 0
+    prm.sm_scale = float(sm_scale) if sm_scale else 0.0
+    prm.cu_seqlens_q, prm.seqlens_kv = _ptr(cu_seqlens_q), _ptr(seqlens_kv)
+    prm.block_table, prm.q, prm.q_block_scale = _ptr(block_table), _ptr(q8), _ptr(q_block_scale)
+    prm.k_pool, prm.k_block_scale, prm.v_pool = _ptr(k_pool), _ptr(k_block_scale), _ptr(v_pool)
+    prm.o, prm.lse = _ptr(out), _ptr(lse)
+    prm.workspace, prm.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    prm.error_word = _ptr(error_word)
+    _check(lib.qpkv_prefill_paged(ctypes.byref(prm), _stream()), "qpkv_prefill_paged")
     return out

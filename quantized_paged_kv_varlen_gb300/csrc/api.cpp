@@ -190,6 +190,7 @@ int32_t qpkv_version(void) { return 100; }
 size_t qpkv_struct_size(int32_t which) {
   switch (which) {
     case 0: return sizeof(qpkv_write_params);
+    case 1: return sizeof(qpkv_prefill_params);
     default: return 0;
   }
 }
@@ -399,6 +400,37 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
                                         num_kv_heads, head_dim, q_descale, k_descale, v_descale,
                                         softmax_scale, causal, o, lse, error_word,
                                         static_cast<cudaStream_t>(stream), &status);
+  if (status != QPKV_OK) return static_cast<qpkv_status>(status);
+  return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
+}
+
+size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads_q) {
+  if (num_seqs < 0 || num_tokens < 0 || num_heads_q < 0) return 0;
+  return prefill_workspace_bytes(num_seqs, num_tokens, num_heads_q);
+}
+
+qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* p, void* stream) {
+  if (p == nullptr) return QPKV_ERR_INVALID_ARG;
+  if (p->num_seqs < 0 || p->num_tokens < 0 || p->num_heads_q <= 0 || p->num_heads_kv <= 0 ||
+      p->num_pages <= 0 || p->bt_stride <= 0 || p->num_blocks <= 0 || p->page_size <= 0)
+    return QPKV_ERR_INVALID_ARG;
+  const int ps = p->page_size;
+  if (p->head_dim != 128 || p->num_heads_q % p->num_heads_kv != 0 || ps % 16 != 0 ||
+      (128 % ps != 0 && ps % 128 != 0))
+    return QPKV_ERR_UNSUPPORTED;
+  if (p->num_seqs == 0 || p->num_tokens == 0) return QPKV_OK;
+  if (p->cu_seqlens_q == nullptr || p->seqlens_kv == nullptr || p->block_table == nullptr ||
+      p->q == nullptr || p->q_block_scale == nullptr || p->k_pool == nullptr ||
+      p->k_block_scale == nullptr || p->v_pool == nullptr || p->o == nullptr ||
+      p->workspace == nullptr)
+    return QPKV_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->k_pool) || !aligned16(p->v_pool) || !aligned16(p->o) ||
+      !aligned16(p->workspace))
+    return QPKV_ERR_INVALID_ARG;
+  if (p->workspace_bytes < prefill_workspace_bytes(p->num_seqs, p->num_tokens, p->num_heads_q))
+    return QPKV_ERR_WORKSPACE_TOO_SMALL;
+  int status = QPKV_OK;
+  const cudaError_t e = launch_prefill_int8(*p, static_cast<cudaStream_t>(stream), &status);
   if (status != QPKV_OK) return static_cast<qpkv_status>(status);
   return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
 }

@@ -46,7 +46,7 @@ constexpr int kD = 128;             // head dim
 constexpr int kThreads = 352;       // 11 warps
 constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpPv = 10;   // softmax + epilogue: warps 2..9
 constexpr int kSoftmax = 256;       // two threads per query row
-constexpr int kStages = 10;         // K/V ring, 16 KB each
+constexpr int kStages = 8;         // K/V ring, 16 KB each
 constexpr int kTileBytes = kT * kD; // one E4M3 tile
 constexpr int kSmem = (2 + kStages) * kTileBytes + 1024;
 constexpr float kRescaleLog2 = 8.0f;

@@ -68,6 +68,10 @@ cudaError_t launch_fp8_attn(const void* q, const void* k, const void* v, int B, 
                             const float* v_descale, float softmax_scale, int causal, void* o,
                             float* lse, int32_t* error_word, cudaStream_t stream, int* status);
 
+// Varlen INT8-QK paged prefill (prefill_int8.cu).
+size_t prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads_q);
+cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t stream, int* status);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
                            void* base, const uint64_t* dims, const uint64_t* strides_bytes,

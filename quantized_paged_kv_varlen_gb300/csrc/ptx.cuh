@@ -16,6 +16,7 @@ constexpr long long kWaitTimeoutCycles = 4000000000ll;
 constexpr int kDevErrTimeout = 1;     // an mbarrier wait ran out
 constexpr int kDevErrBadPage = 2;     // block_table entry outside [0, num_pages)
 constexpr int kDevErrBadIndex = 4;    // sparse index outside [0, L_kv)
+constexpr int kDevErrBadLength = 8;   // sequence lengths exceed the described arrays
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -237,6 +238,18 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, f16/bf16 operands; A is K-major in
+// tensor memory (one row per lane, two 16-bit elements per column).
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

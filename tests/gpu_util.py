@@ -7,6 +7,9 @@ import numpy as np
 # with P in bf16 / fp32 (the FP8-P bound is looser); LSE absolute.
 ATOL_MAX = 2e-3
 BF16_REL = 2.0 ** -8
+# The stated bound with P in bf16 (max-abs 1e-2), used where a row may see
+# only a few keys: bf16 rounding of P then moves O by up to ~2^-9 |v|.
+ATOL_P_BF16 = 1e-2
 REL_L2 = 5e-3
 REL_L2_FP8_P = 2e-2
 LSE_ATOL = 1e-3

@@ -38,6 +38,7 @@ def test_every_declared_symbol_is_exported(qlib):
 def test_struct_mirror_and_strings(qlib):
     q, lib = qlib
     assert lib.qpkv_struct_size(0) == ctypes.sizeof(q.WriteParams)
+    assert lib.qpkv_struct_size(1) == ctypes.sizeof(q.PrefillParams)
     assert lib.qpkv_struct_size(99) == 0
     assert lib.qpkv_status_string(0) == b"ok"
     assert lib.qpkv_status_string(3) == b"workspace too small"
@@ -194,6 +195,43 @@ def test_write_cache_rejects_before_launch(qlib):
     p.mode = 2                       # MLA needs head_dim 576
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
 
+
+
+def test_prefill_rejects_before_launch(qlib):
+    q, lib = qlib
+    assert lib.qpkv_prefill_paged(None, None) == 1
+    assert lib.qpkv_prefill_workspace_bytes(8, 1000, 4) >= 4 * (1 + 5 * 8) + 32 * 4 * (4 + 8)
+    assert lib.qpkv_prefill_workspace_bytes(-1, 10, 4) == 0
+    p = q.PrefillParams()
+    fake = 0x100000
+    for n in ("cu_seqlens_q", "seqlens_kv", "block_table", "q", "q_block_scale", "k_pool",
+              "k_block_scale", "v_pool", "o", "workspace"):
+        setattr(p, n, fake)
+    p.num_seqs, p.num_tokens, p.num_heads_q, p.num_heads_kv = 2, 300, 4, 2
+    p.head_dim, p.page_size, p.num_pages, p.bt_stride, p.num_blocks = 128, 64, 10, 5, 3
+    p.causal = 1
+    p.workspace_bytes = lib.qpkv_prefill_workspace_bytes(2, 300, 4)
+    p.head_dim = 64
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
+    p.head_dim = 128
+    for ps in (24, 48, 192):       # not a multiple of 16 dividing 128 or of 128
+        p.page_size = ps
+        assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
+    p.page_size = 64
+    p.num_heads_kv = 3             # 4 q heads do not group over 3 kv heads
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
+    p.num_heads_kv = 2
+    p.v_pool = fake + 8
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 1
+    p.v_pool = fake
+    p.workspace_bytes = 8
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 3
+    p.workspace_bytes = lib.qpkv_prefill_workspace_bytes(2, 300, 4)
+    p.num_blocks = 0
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 1
+    p.num_blocks = 3
+    p.num_tokens = 0               # nothing to do: OK without touching memory
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 0
 
 def test_binding_raises_without_library(tmp_path):
     import quantized_paged_kv_varlen_gb300 as q

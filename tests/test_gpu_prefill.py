@@ -1,0 +1,216 @@
+"""GPU parity: the Sage-style INT8 cache write (bit-exact) and the varlen
+INT8-QK paged prefill against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oatt
+from oracle import cache as ocache
+from oracle import rope as orope
+from quantized_paged_kv_varlen_gb300 import synth
+from tests.gpu_util import ATOL_P_BF16, assert_attention_close, assert_lse_close, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _u32(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+# --------------------------------------------------------- INT8 cache write
+
+def _gpu_write(lib, q, k, v, lengths, bt, P, ps, cos, sin):
+    """GPU RoPE + block-INT8 write of whole sequences; tables are inputs."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = len(lengths)
+    nb = max(1, (int(max(lengths)) + 127) // 128)
+    k_pool = torch.full((P, ps, Hkv, D), 99, dtype=torch.int8, device=DEV)
+    v_pool = torch.full((P, ps, Hkv, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ks = torch.full((B, nb, Hkv), float("nan"), dtype=torch.float32, device=DEV)
+    qs = torch.full((B, nb, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    q8 = torch.full((T, Hq, D), 99, dtype=torch.int8, device=DEV)
+    slots = torch.full((T,), -1, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cu = _t(synth.inclusive_prefix(lengths))
+    lib.write_cache_int8_block128_rope(
+        _t(q).to(torch.bfloat16), _t(k).to(torch.bfloat16), _t(v).to(torch.bfloat16), cu, _t(bt),
+        int(max(lengths)), _t(cos), _t(sin), k_pool, v_pool, ks, q8, qs, slot_mapping=slots,
+        error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return dict(k_pool=k_pool, v_pool=v_pool, ks=ks, qs=qs, q8=q8, slots=slots, cu=cu, nb=nb)
+
+
+def test_write_cache_int8_bit_exact(lib):
+    lengths = np.array([1, 130, 300], dtype=np.int32)
+    wl = synth.varlen_prefill(seed=11, H=4, page_size=64, lengths=lengths)
+    Hkv = 2
+    k, v = wl.k[:, :Hkv], wl.v[:, :Hkv]
+    cos, sin = orope.cos_sin_table(512, 128, wl.theta)
+    d = _gpu_write(lib, wl.q, k, v, lengths, wl.block_table, wl.num_pages, 64, cos, sin)
+    P, ps, D = wl.num_pages, 64, 128
+    kp0 = np.full((P, ps, Hkv, D), 99, np.int8)
+    vp0 = np.full((P, ps, Hkv, D), 0x7FC0, np.uint16)
+    kp, vp, kscale, q8, qscale, slots = ocache.write_int8_block128_rope(
+        wl.q, k, v, wl.cu_seqlens, wl.block_table, ps, cos, sin, d["nb"], kp0, vp0)
+    assert np.array_equal(d["slots"].cpu().numpy(), slots)
+    got_k = d["k_pool"].cpu().numpy().reshape(P * ps, Hkv, D)
+    got_v = d["v_pool"].cpu().view(torch.int16).numpy().view(np.uint16).reshape(P * ps, Hkv, D)
+    assert np.array_equal(got_k[slots], kp.reshape(P * ps, Hkv, D)[slots])
+    assert np.array_equal(got_v[slots], vp.reshape(P * ps, Hkv, D)[slots])
+    assert np.array_equal(d["q8"].cpu().numpy(), q8)
+    # scales of the blocks a sequence has; the rest stay as the caller left them
+    for b, L in enumerate(lengths):
+        n = (int(L) + 127) // 128
+        assert np.array_equal(_u32(d["ks"].cpu().numpy()[b, :n]), _u32(kscale[b, :n]))
+        assert np.array_equal(_u32(d["qs"].cpu().numpy()[b, :n]), _u32(qscale[b, :n]))
+
+
+def test_rope_table_matches_oracle(lib):
+    """The library's table (double precision on the device, rounded to
+    float) against the oracle's numpy float64 table: equal or 1 ulp apart."""
+    cos, sin = lib.rope_table(1.0e4, 4096, 128)
+    ocos, osin = orope.cos_sin_table(4096, 128, 1.0e4)
+    for g, w in ((cos.cpu().numpy(), ocos), (sin.cpu().numpy(), osin)):
+        du = np.abs(_u32(g).astype(np.int64) - _u32(w).astype(np.int64))
+        same_sign = np.sign(g) == np.sign(w)
+        assert np.all((du <= 1) | (~same_sign & (np.abs(g) < 1e-6)))
+        assert np.mean(du == 0) > 0.99
+
+
+# ------------------------------------------------------------------ prefill
+
+def _random_case(seed, Lq, Lk, Hq, Hkv, ps, qmag=3.0, kmag=3.0):
+    """Random INT8 Q/K codes with block scales and bf16 V in a permuted pool."""
+    rng = np.random.default_rng((seed, 77))
+    Lq = np.asarray(Lq, dtype=np.int32)
+    Lk = np.asarray(Lk, dtype=np.int32)
+    B, T = len(Lq), int(Lq.sum())
+    nb = max(1, (int(max(Lq.max(), Lk.max())) + 127) // 128)
+    q8 = rng.integers(-127, 128, (T, Hq, 128), dtype=np.int8)
+    qs = (rng.uniform(0.5, 1.5, (B, nb, Hq)) * qmag / 127).astype(np.float32)
+    bt, P = synth.page_tables(rng, Lk, ps, extra_pages=2)
+    k_pool = rng.integers(-127, 128, (P, ps, Hkv, 128), dtype=np.int8)
+    ks = (rng.uniform(0.5, 1.5, (B, nb, Hkv)) * kmag / 127).astype(np.float32)
+    v_bits = ocache.bf16_bits(synth.bf16_normal(rng, (P, ps, Hkv, 128)))
+    return dict(q8=q8, qs=qs, k_pool=k_pool, ks=ks, v_bits=v_bits, bt=bt,
+                cu=synth.inclusive_prefix(Lq), Lk=Lk)
+
+
+def _run_prefill(lib, c, causal, scale=None):
+    T, Hq, _ = c["q8"].shape
+    lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.full((T, Hq, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    v_pool = _t(c["v_bits"].view(np.int16)).view(torch.bfloat16)
+    lib.prefill_paged(_t(c["q8"]), _t(c["qs"]), _t(c["k_pool"]), _t(c["ks"]), v_pool, _t(c["bt"]),
+                      _t(c["cu"]), _t(c["Lk"]), sm_scale=scale, causal=causal, out=out, lse=lse,
+                      error_word=err)
+    torch.cuda.synchronize()
+    return bf16_to_f64(out), lse.cpu().numpy().astype(np.float64), int(err.item())
+
+
+def _oracle(c, causal, scale=1.0 / np.sqrt(128.0), rows=None):
+    return oatt.paged_prefill_int8(c["q8"], c["qs"], c["k_pool"], c["ks"], c["v_bits"], c["bt"],
+                                   c["cu"], c["Lk"], scale, causal, rows=rows)
+
+
+@pytest.mark.parametrize("Lq,Lk,Hq,Hkv,ps,causal", [
+    ([1, 130, 300], [1, 130, 300], 2, 2, 64, True),        # ragged tails, one-token sequence
+    ([200, 0, 385], [200, 0, 385], 4, 2, 16, True),        # an empty sequence, GQA 2:1
+    ([77, 128, 1], [300, 128, 513], 4, 1, 32, True),       # cached prefix: L_q < L_kv
+    ([300, 50], [40, 0], 2, 2, 64, True),                  # L_q > L_kv: leading rows see nothing
+    ([130, 257], [390, 100], 2, 1, 128, False),            # no mask
+    ([600], [600], 2, 2, 256, True),                       # pages longer than a tile
+    ([640, 520], [640, 520], 1, 1, 64, True),              # several q tiles: pairs (0,4) (1,3) (2)
+])
+def test_prefill_shapes(lib, Lq, Lk, Hq, Hkv, ps, causal):
+    c = _random_case(sum(Lq) + 7 * ps, Lq, Lk, Hq, Hkv, ps)
+    got_o, got_lse, err = _run_prefill(lib, c, causal)
+    assert err == 0
+    want_o, want_lse = _oracle(c, causal)
+    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_lse_close(got_lse, want_lse)
+    none = np.isneginf(want_lse)
+    assert np.all(got_o[none] == 0.0)
+
+
+def test_prefill_zero_scale_blocks(lib):
+    """A key block and a query block whose scale is 0 (all-zero input
+    blocks): their logits are exactly 0 and nothing turns into NaN."""
+    c = _random_case(5, [300], [300], 2, 2, 64)
+    c["ks"][0, 1, :] = 0.0
+    c["qs"][0, 2, 1] = 0.0
+    got_o, got_lse, err = _run_prefill(lib, c, True)
+    assert err == 0
+    want_o, want_lse = _oracle(c, True)
+    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_lse_close(got_lse, want_lse)
+
+
+def test_prefill_running_max_jumps(lib):
+    """Key scales grow 4x per block: later tiles beat the running maximum by
+    far more than 2^8 and the accumulated O rows are rescaled (the lse stays
+    near 1.5e3, where one fp32 ulp is well inside the 1e-3 bound)."""
+    c = _random_case(9, [700], [700], 2, 2, 64, kmag=0.5)
+    c["ks"][0] *= (4.0 ** np.arange(c["ks"].shape[1]))[:, None].astype(np.float32)
+    got_o, got_lse, err = _run_prefill(lib, c, True)
+    assert err == 0
+    want_o, want_lse = _oracle(c, True)
+    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_lse_close(got_lse, want_lse)
+
+
+def test_prefill_bad_page_sets_error_word(lib):
+    """A block_table entry outside the pool is read as zeros and flagged."""
+    c = _random_case(3, [256], [256], 1, 1, 64)
+    P = c["k_pool"].shape[0]
+    c["bt"][0, 1] = P + 5
+    _, _, err = _run_prefill(lib, c, True)
+    assert err & 2
+
+
+def test_prefill_full_size_sampled(lib):
+    """8 sequences, L ~ U{256..4096}, 32 heads, page 64: the GPU writes the
+    cache and runs the prefill (the benchmark's launch); the oracle rebuilds
+    two sequences' caches from the same bf16 draws and checks sampled rows."""
+    wl = synth.varlen_prefill(0)
+    lengths = wl.lengths
+    cos, sin = orope.cos_sin_table(int(lengths.max()), 128, wl.theta)
+    d = _gpu_write(lib, wl.q, wl.k, wl.v, lengths, wl.block_table, wl.num_pages, 64, cos, sin)
+    T, H = wl.q.shape[0], wl.H
+    lse = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lk = _t(lengths)
+    out = lib.prefill_paged(d["q8"], d["qs"], d["k_pool"], d["ks"], d["v_pool"], _t(wl.block_table),
+                            d["cu"], lk, causal=True, lse=lse, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    begin = np.concatenate([[0], np.cumsum(lengths)[:-1]])
+    for b in (int(np.argmax(lengths)), int(np.argmin(lengths))):
+        L = int(lengths[b])
+        sl = slice(int(begin[b]), int(begin[b]) + L)
+        npg = (L + 63) // 64
+        bt1 = np.arange(npg, dtype=np.int32)[None]
+        kp, vp, kscale, q8, qscale, _ = ocache.write_int8_block128_rope(
+            wl.q[sl], wl.k[sl], wl.v[sl], np.array([L], np.int32), bt1, 64, cos, sin,
+            (L + 127) // 128, np.zeros((npg, 64, H, 128), np.int8),
+            np.zeros((npg, 64, H, 128), np.uint16))
+        toks = sorted({0, 1, 127, 128, L // 2, L - 2, L - 1})
+        rows = [(t, h) for t in toks for h in (0, 13, 31)]
+        want_o, want_lse = oatt.paged_prefill_int8(q8, qscale, kp, kscale, vp, bt1,
+                                                   np.array([L], np.int32), np.array([L], np.int32),
+                                                   wl.scale, True, rows=rows)
+        ti = np.array([t for t, _ in rows])
+        hi = np.array([h for _, h in rows])
+        got_o = bf16_to_f64(out[torch.from_numpy(begin[b] + ti).long(), torch.from_numpy(hi).long()])
+        got_l = lse[torch.from_numpy(begin[b] + ti).long(), torch.from_numpy(hi).long()]
+        assert_attention_close(got_o, want_o[ti, hi], atol=ATOL_P_BF16)
+        assert_lse_close(got_l.cpu().numpy().astype(np.float64), want_lse[ti, hi])
