@@ -63,8 +63,8 @@ int32_t qpkv_version(void);
 
 /* sizeof of the parameter structs below, so that bindings in other
  * languages can check their mirror of the layout:
- * which = 0 -> qpkv_write_params, 1 -> qpkv_prefill_params.  Unknown
- * `which` returns 0. */
+ * which = 0 -> qpkv_write_params, 1 -> qpkv_prefill_params,
+ * 2 -> qpkv_mla_params.  Unknown `which` returns 0. */
 size_t qpkv_struct_size(int32_t which);
 
 /* -------------------------------------------------------------- RoPE table
@@ -369,6 +369,66 @@ typedef struct qpkv_prefill_params {
 size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads_q);
 
 qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* params, void* stream);
+
+/* ------------------------------------------------ MLA-absorb sparse decode
+ * ("KvQuantSparseFlashAttention" README, 计算公式; 参数说明 rows query, key,
+ * value, sparse_indices, block_table, actual_seq_lengths_query,
+ * actual_seq_lengths_kv, sparse_mode, scale_value; attention_mode 2 with
+ * the combined cache row, quant_scale_repo_mode 1):
+ *   for query token t (sequence b, row i of its L_q rows) and q head h the
+ *   keys are the entries of sparse_indices[t, 0, :] before the first -1,
+ *   logical token positions of sequence b mapped through block_table
+ *   (pool row block_table[b][id / block_size] * block_size + id % block_size);
+ *   sparse_mode 3 also drops ids above i + L_kv - L_q.  A cache row is 656
+ *   bytes: 512 INT8 nope codes, 64 bf16 rope values, 4 fp32 scales (nope
+ *   tile k = dims 128k..128k+127), the layout QPKV_WRITE_MLA_ROW writes.
+ *   K = [code * scale || rope] (576), V = code * scale (512);
+ *   o[t, h] = softmax(scale_value * q[t, h] . K^T) . V (bf16 [T, Hq, 512]),
+ *   lse[t, h] = ln sum exp(logits); no visible key: o = 0, lse = -inf.
+ * The nope is dequantised to bf16 (code * scale rounded once) for both
+ * products; the logits and the softmax are fp32, P enters PV as bf16.
+ *
+ * Arrays (device): q bf16 [T, Hq, 576]; kv_pool u8 [P, block_size, 1, 656];
+ * sparse_indices int32 [T, 1, sparse_size]; block_table int32 [B,
+ * bt_stride]; seqlens_kv int32 [B]; cu_seqlens_q int32 [B] inclusive prefix
+ * sums; o bf16 [T, Hq, 512]; lse fp32 [T, Hq] or NULL; workspace of
+ * qpkv_mla_workspace_bytes(T, sparse_size) bytes (overwritten).
+ * error_word bits: QPKV_DEV_ERR_BAD_INDEX (an id outside [0, L_kv) before
+ * the first -1, skipped), QPKV_DEV_ERR_BAD_PAGE, QPKV_DEV_ERR_TIMEOUT.
+ * Supported: 1 <= Hq <= 128, head_dim_qk 576, head_dim_v 512, sparse_mode
+ * 0 or 3, sparse_block_size 1.  q, kv_pool, o, workspace 16-byte aligned.
+ * scale <= 0 selects 1/sqrt(576).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
+typedef struct qpkv_mla_params {
+  int32_t num_seqs;      /* B */
+  int32_t num_tokens;    /* T: query tokens (rows of q, o, lse) */
+  int32_t num_heads_q;   /* Hq, at most 128 */
+  int32_t head_dim_qk;   /* 576 */
+  int32_t head_dim_v;    /* 512 */
+  int32_t block_size;    /* tokens per cache block */
+  int32_t num_blocks;    /* P */
+  int32_t bt_stride;
+  int32_t sparse_size;   /* entries per sparse_indices row */
+  int32_t sparse_mode;   /* 0 or 3 */
+  float scale;
+  int32_t pad0;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seqlens_kv;
+  const int32_t* block_table;
+  const void* q;
+  const void* kv_pool;
+  const int32_t* sparse_indices;
+  void* o;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* error_word;
+} qpkv_mla_params;
+
+/* Device workspace bytes qpkv_mla_sparse_decode needs (0 for negative sizes). */
+size_t qpkv_mla_workspace_bytes(int32_t num_tokens, int32_t sparse_size);
+
+qpkv_status qpkv_mla_sparse_decode(const qpkv_mla_params* params, void* stream);
 
 #ifdef __cplusplus
 }

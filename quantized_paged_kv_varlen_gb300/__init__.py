@@ -74,6 +74,18 @@ class PrefillParams(ctypes.Structure):
             "k_block_scale", "v_pool", "o", "lse", "workspace")] + [
         ("workspace_bytes", ctypes.c_size_t), ("error_word", _p)]
 
+
+class MlaParams(ctypes.Structure):
+    """Mirror of ``qpkv_mla_params`` (include/qpkv.h)."""
+    _fields_ = [(n, _i32) for n in (
+        "num_seqs", "num_tokens", "num_heads_q", "head_dim_qk", "head_dim_v", "block_size",
+        "num_blocks", "bt_stride", "sparse_size", "sparse_mode")] + [
+        ("scale", ctypes.c_float), ("pad0", _i32)] + [
+        (n, _p) for n in (
+            "cu_seqlens_q", "seqlens_kv", "block_table", "q", "kv_pool", "sparse_indices", "o",
+            "lse", "workspace")] + [
+        ("workspace_bytes", ctypes.c_size_t), ("error_word", _p)]
+
 def _declare(lib):
     S = ctypes.c_size_t
     P64 = ctypes.POINTER(ctypes.c_int64)
@@ -99,6 +111,8 @@ def _declare(lib):
                                      ctypes.c_float, _i32, _p, _p, _p, _p]),
         "qpkv_prefill_workspace_bytes": (S, [_i32, _i32, _i32]),
         "qpkv_prefill_paged": (_i32, [ctypes.POINTER(PrefillParams), _p]),
+        "qpkv_mla_workspace_bytes": (S, [_i32, _i32]),
+        "qpkv_mla_sparse_decode": (_i32, [ctypes.POINTER(MlaParams), _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -470,4 +484,53 @@ def prefill_paged(q8, q_block_scale, k_pool, k_block_scale, v_pool, block_table,
     prm.workspace, prm.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     prm.error_word = _ptr(error_word)
     _check(lib.qpkv_prefill_paged(ctypes.byref(prm), _stream()), "qpkv_prefill_paged")
+    return out
+
+
+def mla_workspace(num_tokens, sparse_size, device="cuda"):
+    """A device workspace large enough for ``mla_sparse_decode``."""
+    torch = _torch()
+    n = int(load().qpkv_mla_workspace_bytes(int(num_tokens), int(sparse_size)))
+    return torch.empty(((n + 15) // 16) * 16, dtype=torch.uint8, device=device)
+
+
+def mla_sparse_decode(q, kv_pool, sparse_indices, block_table, seqlens_kv, cu_seqlens_q,
+                      scale=None, sparse_mode=0, out=None, lse=None, workspace=None,
+                      error_word=None):
+    """MLA-absorb sparse decode: q bf16 [T, Hq, 576]; kv_pool u8 [P, bs, 1, 656];
+    sparse_indices int32 [T, 1, S]; returns bf16 O [T, Hq, 512] (``lse`` fp32
+    [T, Hq] filled when given)."""
+    torch = _torch()
+    lib = load()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kv_pool, "kv_pool", torch.uint8, 4)
+    _need(sparse_indices, "sparse_indices", torch.int32, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seqlens_kv, "seqlens_kv", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    T, Hq, Dqk = q.shape
+    P, bs, one, W = kv_pool.shape
+    if one != 1 or W != PAGE_ROW_MLA or Dqk != 576:
+        raise ValueError("kv_pool must be [P, bs, 1, 656] and q [T, Hq, 576]")
+    S = sparse_indices.shape[2]
+    if sparse_indices.shape[0] != T:
+        raise ValueError("sparse_indices must be [T, 1, S]")
+    if out is None:
+        out = torch.empty((T, Hq, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = mla_workspace(T, S, q.device)
+    prm = MlaParams()
+    prm.num_seqs, prm.num_tokens, prm.num_heads_q = cu_seqlens_q.shape[0], T, Hq
+    prm.head_dim_qk, prm.head_dim_v, prm.block_size, prm.num_blocks = 576, 512, bs, P
+    prm.bt_stride, prm.sparse_size, prm.sparse_mode = block_table.shape[1], S, int(sparse_mode)
+    prm.scale = float(scale) if scale else 0.0
+    prm.cu_seqlens_q, prm.seqlens_kv, prm.block_table = (
+        _ptr(cu_seqlens_q), _ptr(seqlens_kv), _ptr(block_table))
+    prm.q, prm.kv_pool, prm.sparse_indices = _ptr(q), _ptr(kv_pool), _ptr(sparse_indices)
+    prm.o, prm.lse = _ptr(out), _ptr(lse)
+    prm.workspace, prm.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    prm.error_word = _ptr(error_word)
+    _check(lib.qpkv_mla_sparse_decode(ctypes.byref(prm), _stream()), "qpkv_mla_sparse_decode")
     return out

@@ -191,6 +191,7 @@ size_t qpkv_struct_size(int32_t which) {
   switch (which) {
     case 0: return sizeof(qpkv_write_params);
     case 1: return sizeof(qpkv_prefill_params);
+    case 2: return sizeof(qpkv_mla_params);
     default: return 0;
   }
 }
@@ -431,6 +432,34 @@ qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* p, void* stream) {
     return QPKV_ERR_WORKSPACE_TOO_SMALL;
   int status = QPKV_OK;
   const cudaError_t e = launch_prefill_int8(*p, static_cast<cudaStream_t>(stream), &status);
+  if (status != QPKV_OK) return static_cast<qpkv_status>(status);
+  return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
+}
+
+size_t qpkv_mla_workspace_bytes(int32_t num_tokens, int32_t sparse_size) {
+  if (num_tokens < 0 || sparse_size < 0) return 0;
+  return mla_workspace_bytes(num_tokens, sparse_size);
+}
+
+qpkv_status qpkv_mla_sparse_decode(const qpkv_mla_params* p, void* stream) {
+  if (p == nullptr) return QPKV_ERR_INVALID_ARG;
+  if (p->num_seqs <= 0 || p->num_tokens < 0 || p->num_heads_q <= 0 || p->block_size <= 0 ||
+      p->num_blocks <= 0 || p->bt_stride <= 0 || p->sparse_size <= 0)
+    return QPKV_ERR_INVALID_ARG;
+  if (p->head_dim_qk != 576 || p->head_dim_v != 512 || p->num_heads_q > 128 ||
+      (p->sparse_mode != 0 && p->sparse_mode != 3))
+    return QPKV_ERR_UNSUPPORTED;
+  if (p->num_tokens == 0) return QPKV_OK;
+  if (p->cu_seqlens_q == nullptr || p->seqlens_kv == nullptr || p->block_table == nullptr ||
+      p->q == nullptr || p->kv_pool == nullptr || p->sparse_indices == nullptr || p->o == nullptr ||
+      p->workspace == nullptr)
+    return QPKV_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->kv_pool) || !aligned16(p->o) || !aligned16(p->workspace))
+    return QPKV_ERR_INVALID_ARG;
+  if (p->workspace_bytes < mla_workspace_bytes(p->num_tokens, p->sparse_size))
+    return QPKV_ERR_WORKSPACE_TOO_SMALL;
+  int status = QPKV_OK;
+  const cudaError_t e = launch_mla_sparse(*p, static_cast<cudaStream_t>(stream), &status);
   if (status != QPKV_OK) return static_cast<qpkv_status>(status);
   return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
 }

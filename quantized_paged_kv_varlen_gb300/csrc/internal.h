@@ -72,6 +72,10 @@ cudaError_t launch_fp8_attn(const void* q, const void* k, const void* v, int B, 
 size_t prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads_q);
 cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t stream, int* status);
 
+// MLA-absorb sparse decode (mla_sparse.cu).
+size_t mla_workspace_bytes(int num_tokens, int sparse_size);
+cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int* status);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
                            void* base, const uint64_t* dims, const uint64_t* strides_bytes,

@@ -243,3 +243,29 @@ def mla_sparse(seed: int = 0, B: int = 32, QN: int = 128, lo: int = 32768,
         idx[b, 0, :n] = rng.permutation(int(lengths[b]))[:n]
     return MlaWorkload(seed, B, QN, lengths, block_size, bt, P, q, idx,
                        1.0 / np.sqrt(576.0))
+
+
+def mla_sparse_device(seed: int, device, B: int = 32, QN: int = 128, lo: int = 32768,
+                      hi: int = 65536, block_size: int = 64, topk: int = 2048,
+                      sparse_size: int = 2048):
+    """Full-size MLA inputs with the bulk made on the GPU: lengths, the page
+    permutation and the sparse ids from numpy (seed, 6); q [B, QN, 576] and
+    the cache rows' values kv [sum L, 576] as N(0,1) draws of a seeded torch
+    device generator, rounded to bf16.  Returns a dict of device tensors
+    (and the host lengths / block table)."""
+    import torch
+    rng = np.random.default_rng((seed, 6))
+    lengths = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    bt, P = page_tables(rng, lengths, block_size)
+    idx = np.full((B, 1, sparse_size), -1, dtype=np.int32)
+    for b in range(B):
+        n = min(topk, int(lengths[b]), sparse_size)
+        idx[b, 0, :n] = rng.permutation(int(lengths[b]))[:n]
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 6)
+    q = torch.randn((B, QN, 576), generator=g, device=device).to(torch.bfloat16)
+    kv = torch.randn((int(lengths.sum()), 576), generator=g, device=device).to(torch.bfloat16)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return dict(lengths=lengths, block_table=bt, num_pages=P, block_size=block_size, q=q, kv=kv,
+                idx=dev(idx), bt=dev(bt), lk=dev(lengths), cu_kv=dev(inclusive_prefix(lengths)),
+                cu_q=dev(np.arange(1, B + 1, dtype=np.int32)), scale=1.0 / np.sqrt(576.0))

@@ -39,6 +39,7 @@ def test_struct_mirror_and_strings(qlib):
     q, lib = qlib
     assert lib.qpkv_struct_size(0) == ctypes.sizeof(q.WriteParams)
     assert lib.qpkv_struct_size(1) == ctypes.sizeof(q.PrefillParams)
+    assert lib.qpkv_struct_size(2) == ctypes.sizeof(q.MlaParams)
     assert lib.qpkv_struct_size(99) == 0
     assert lib.qpkv_status_string(0) == b"ok"
     assert lib.qpkv_status_string(3) == b"workspace too small"
@@ -232,6 +233,41 @@ def test_prefill_rejects_before_launch(qlib):
     p.num_blocks = 3
     p.num_tokens = 0               # nothing to do: OK without touching memory
     assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 0
+
+
+def test_mla_rejects_before_launch(qlib):
+    q, lib = qlib
+    assert lib.qpkv_mla_sparse_decode(None, None) == 1
+    assert lib.qpkv_mla_workspace_bytes(32, 2048) >= 32 * 128 * 2048 * 6
+    assert lib.qpkv_mla_workspace_bytes(-1, 2048) == 0
+    p = q.MlaParams()
+    fake = 0x100000
+    for n in ("cu_seqlens_q", "seqlens_kv", "block_table", "q", "kv_pool", "sparse_indices", "o",
+              "workspace"):
+        setattr(p, n, fake)
+    p.num_seqs, p.num_tokens, p.num_heads_q, p.head_dim_qk, p.head_dim_v = 2, 2, 128, 576, 512
+    p.block_size, p.num_blocks, p.bt_stride, p.sparse_size = 64, 10, 5, 256
+    p.workspace_bytes = lib.qpkv_mla_workspace_bytes(2, 256)
+    p.head_dim_qk = 192
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 2
+    p.head_dim_qk = 576
+    p.num_heads_q = 256            # more heads than one MMA tile
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 2
+    p.num_heads_q = 128
+    p.sparse_mode = 1
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 2
+    p.sparse_mode = 3
+    p.kv_pool = fake + 4
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 1
+    p.kv_pool = fake
+    p.workspace_bytes = 64
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 3
+    p.workspace_bytes = lib.qpkv_mla_workspace_bytes(2, 256)
+    p.sparse_size = 0
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 1
+    p.sparse_size = 256
+    p.num_tokens = 0
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 0
 
 def test_binding_raises_without_library(tmp_path):
     import quantized_paged_kv_varlen_gb300 as q
