@@ -15,7 +15,7 @@
 // stream-ordered kernels:
 //   mla_prep     sparse ids -> pool rows (block_table lookup; -1 for ids
 //                after the first -1, outside [0, L_kv), or hidden by
-//                sparse_mode 3), per token
+//                sparse_mode 3), and a bulk L2 prefetch of every listed row
 //   mla_qk       one CTA per (token, 512 keys): Q and dequantised-K chunks
 //                of 64 dims stream through shared memory (TMA for Q, eight
 //                converter warps gather and dequantise the rows), S for the
@@ -82,6 +82,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// One whole cache row into L2 (656 bytes, 16-byte aligned): the gathers
+// later read it in pieces, which from DRAM would be single sectors.
+__device__ __forceinline__ void prefetch_row_l2(const void* p) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(kRow)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -113,12 +121,13 @@ __device__ __forceinline__ void dequant16(const uint4& w, float s, uint4& p0, ui
 
 
 // ----------------------------------------------------------------- prep
-// One block per query token: the first -1 ends its list; every listed id
+// Blocks (token, 256-entry slice): the first -1 of the token's list (found
+// by every block of the token) ends it; every listed id
 // becomes a pool row (or -1: past the list, outside [0, L_kv) - flagged -,
 // hidden by the right-down causal rule of sparse_mode 3, or on a page id
 // outside the pool - flagged).
 __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
-  const int t = static_cast<int>(blockIdx.x);
+  const int t = static_cast<int>(blockIdx.x), j0 = static_cast<int>(blockIdx.y) * 256;
   __shared__ int first_neg;
   if (threadIdx.x == 0) first_neg = a.S;
   __syncthreads();
@@ -137,7 +146,8 @@ __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
   const int begin = b > 0 ? a.cu_q[b - 1] : 0;
   const int Lq = a.cu_q[b] - begin, i = t - begin, Lk = a.lk[b];
   int32_t* out = a.rows + static_cast<size_t>(t) * a.Sp;
-  for (int j = threadIdx.x; j < a.Sp; j += blockDim.x) {
+  {
+    const int j = j0 + static_cast<int>(threadIdx.x);
     int r = -1;
     if (has_seq && j < nv) {
       const int id = ids[j];
@@ -151,7 +161,8 @@ __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
           r = pg * a.bs + id % a.bs;
       }
     }
-    out[j] = r;
+    if (r >= 0) prefetch_row_l2(a.pool + static_cast<size_t>(r) * kRow);
+    if (j < a.Sp) out[j] = r;
   }
 }
 
@@ -617,7 +628,7 @@ cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int
     *status = QPKV_ERR_CUDA;
     return cudaErrorInvalidValue;
   }
-  mla_prep_kernel<<<T, 256, 0, stream>>>(a);
+  mla_prep_kernel<<<dim3(T, Sp / 256 + (Sp % 256 ? 1 : 0)), 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmem);
