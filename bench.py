@@ -244,6 +244,19 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def peaks_all():
+    """hbm_gbs and bf16_tflops from MEASURED_PEAKS.json, else the fallbacks."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    out = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        out["hbm_gbs"] = float(p.get("hbm_gbs", out["hbm_gbs"]))
+        out["bf16_tflops"] = float(p.get("bf16_tflops", out["bf16_tflops"]))
+        out["source"] = "measured"
+    return out
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def cpu_worker(seconds, n_req):
@@ -461,7 +474,124 @@ def run_qpkv(args):
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if world == 1 and not args.no_extras:
+        line["also"] = run_extras(device)
     print(json.dumps(line), flush=True)
+
+
+def _median_ms(fn, iters, flush=None):
+    """Median CUDA-event time of fn() on the current stream (L2 flushed
+    before each run when `flush` is given)."""
+    import torch
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def run_extras(device, iters=10):
+    """The other hot paths at their full sizes, timed alone: dense FP8
+    causal attention (B=4, S=8192, H=32, D=128), the varlen INT8-QK paged
+    prefill (8 sequences, L ~ U{256..4096}, 32 heads, page 64) and the
+    MLA-absorb sparse decode (B=32, 128 heads, 2048 ids of L ~ U{32768..65536})."""
+    import numpy as np
+    import torch
+    import quantized_paged_kv_varlen_gb300 as q
+    from quantized_paged_kv_varlen_gb300 import synth
+    pk = peaks_all()
+    bf16, fp8 = pk["bf16_tflops"], 2.0 * pk["bf16_tflops"]
+    out = {}
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    # dense FP8, causal
+    B4, S4, H4, D4 = 4, 8192, 32, 128
+    q8, k8, v8, qd, kd, vd = synth.dense_fp8_device(0, B4, S4, H4, D4, device)
+    o4 = torch.empty((B4, S4, H4, D4), dtype=torch.bfloat16, device=device)
+    f4 = lambda: q.fp8_attn_fwd(q8, k8, v8, qd, kd, vd, causal=True, out=o4, error_word=err)
+    for _ in range(3):
+        f4()
+    ms = _median_ms(f4, iters)
+    flops = 2.0 * B4 * H4 * D4 * S4 * (S4 + 1)
+    tf = flops / (ms / 1e3) / 1e12
+    out["fp8_attn_causal"] = {
+        "workload": f"dense FP8 causal B={B4} S={S4} H={H4} D={D4} (BSND e4m3, per-(b,h) descales)",
+        "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8, "unit": "TFLOP/s",
+                     "frac": tf / fp8, "peak_source": "measured bf16_tflops x 2 (fp8 nominal ratio)"}}
+    del q8, k8, v8, o4
+
+    # varlen INT8-QK paged prefill (cache written by the library)
+    wl = synth.varlen_prefill(0)
+    L = wl.lengths
+    T, H, D = wl.q.shape
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    cos, sin = q.rope_table(wl.theta, int(L.max()), 128)
+    nb = wl.num_blocks
+    k_pool = torch.zeros((wl.num_pages, wl.page_size, H, D), dtype=torch.int8, device=device)
+    v_pool = torch.zeros((wl.num_pages, wl.page_size, H, D), dtype=torch.bfloat16, device=device)
+    ks = torch.zeros((len(L), nb, H), dtype=torch.float32, device=device)
+    qs = torch.zeros_like(ks)
+    q8p = torch.zeros((T, H, D), dtype=torch.int8, device=device)
+    cu, bt, lk = t(synth.inclusive_prefix(L)), t(wl.block_table), t(L)
+    qb, kb, vb = (t(x).to(torch.bfloat16) for x in (wl.q, wl.k, wl.v))
+    wr = lambda: q.write_cache_int8_block128_rope(qb, kb, vb, cu, bt, int(L.max()), cos, sin,
+                                                  k_pool, v_pool, ks, q8p, qs, error_word=err)
+    wr()
+    op = torch.empty((T, H, D), dtype=torch.bfloat16, device=device)
+    wsp = q.prefill_workspace(len(L), T, H, device)
+    fp = lambda: q.prefill_paged(q8p, qs, k_pool, ks, v_pool, bt, cu, lk, causal=True, out=op,
+                                 workspace=wsp, error_word=err)
+    for _ in range(3):
+        fp()
+    ms = _median_ms(fp, iters)
+    ms_w = _median_ms(wr, iters)
+    flops = float(sum(4.0 * D * H * int(x) * (int(x) + 1) / 2 for x in L))
+    tf = flops / (ms / 1e3) / 1e12
+    out["int8_prefill_varlen"] = {
+        "workload": f"varlen causal prefill {len(L)} seqs L={L.tolist()} H={H} D={D} page 64, "
+                    "INT8 Q/K block-128 scales, bf16 V",
+        "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops, "write_cache_ms": ms_w,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": tf / bf16, "peak_source": "measured bf16_tflops (f16/bf16 MMAs)"}}
+    del k_pool, v_pool, q8p, qb, kb, vb, op
+
+    # MLA-absorb sparse decode
+    d = synth.mla_sparse_device(0, device)
+    pool = torch.empty((d["num_pages"], 64, 1, 656), dtype=torch.uint8, device=device)
+    q.write_cache_mla(d["kv"], d["cu_kv"], d["bt"], pool, error_word=err)
+    om = torch.empty((32, 128, 512), dtype=torch.bfloat16, device=device)
+    wsm = q.mla_workspace(32, 2048, device)
+    fm = lambda: q.mla_sparse_decode(d["q"], pool, d["idx"], d["bt"], d["lk"], d["cu_q"],
+                                     scale=d["scale"], out=om, workspace=wsm, error_word=err)
+    for _ in range(3):
+        fm()
+    ms = _median_ms(fm, iters * 2, flush=flush)
+    flops = 32.0 * 128 * 2048 * 2 * (576 + 512)
+    row_bytes = 32 * 2048 * 656 + 32 * 128 * 576 * 2 + 32 * 128 * 512 * 2 + 32 * 2048 * 4
+    tf = flops / (ms / 1e3) / 1e12
+    gbs = row_bytes / (ms / 1e3) / 1e9
+    out["mla_sparse_decode"] = {
+        "workload": "MLA-absorb sparse decode B=32 QN=128 D=576/512, 2048 ids of "
+                    "L~U{32768..65536}, block 64, INT8 nope + bf16 rope rows",
+        "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops, "gb_per_s": gbs,
+        "l2": "flushed (256 MB write) before each run",
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": tf / bf16, "hbm_frac": gbs / pk["hbm_gbs"],
+                     "peak_source": "measured bf16_tflops; hbm_frac of measured hbm_gbs"}}
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the extra workloads")
+    return out
 
 
 def set_batch(n):
@@ -482,6 +612,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["qpkv", "reference"], default="qpkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the dense FP8, INT8 prefill and MLA decode measurements")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up for at least this long so clocks settle")
