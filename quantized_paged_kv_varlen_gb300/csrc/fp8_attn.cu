@@ -14,8 +14,7 @@
 //                S[128 q x 128 k] = Q[128 x D] . K_tile[128 x D]^T   (FP8)
 //                O[128 q x D]   += P[128 q x 128 k] . V_tile[128 k x D]
 //              P is read straight from tensor memory, where the softmax
-//              wrote it over the first 64 columns of its S buffer as two
-//              E4M3 terms hi + lo (K = 256: hi rows, then lo rows, each
+//              wrote it into a P buffer as two E4M3 terms hi + lo (K = 256: hi rows, then lo rows, each
 //              against the same V tile), about 8 significant bits;
 //   warps 2-9  online softmax, two threads per query row (TMEM lane): warps
 //              2-5 take the row's keys [0, 64), warps 6-9 keys [64, 128);
@@ -24,9 +23,10 @@
 //              when a tile beats it by more than 2^8, then the row's O is
 //              rescaled.  At the end of a work item the same threads write
 //              O / l * vd as bf16 and the lse.
-// TMEM holds three S buffers and O (4 x 128 columns): QK runs up to three
-// tiles ahead of PV (K tiles three ahead of V in the ring), so S(t+1) and
-// S(t+2) are computed while the softmax works on tile t.
+// TMEM holds two S buffers, two P buffers (64 columns each) and O: QK(t)
+// waits only for the softmax to have read S(t-2), and the softmax writes
+// P(t) once PV(t-2) has read that P buffer, so the in-order tensor pipe
+// never holds QK back behind a late PV.
 //
 // Work: a unit is the pair of q tiles (t, n-1-t) of one (batch, head), so
 // every unit costs the same number of causal K/V tiles; units are dealt to
@@ -50,8 +50,10 @@ constexpr int kStages = 8;         // K/V ring, 16 KB each
 constexpr int kTileBytes = kT * kD; // one E4M3 tile
 constexpr int kSmem = (2 + kStages) * kTileBytes + 1024;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kSBufs = 3;           // S ring in TMEM: QK(t) waits only for PV(t-3)
-constexpr uint32_t kColS = 0;       // S buffers: columns [0, 128), [128, 256), [256, 384)
+constexpr int kSBufs = 2;           // S ring in TMEM: QK(t) waits for the softmax to read S(t-2)
+constexpr int kPBufs = 2;           // P ring in TMEM: P(t) waits for PV(t-2)
+constexpr uint32_t kColS = 0;       // S buffers: columns [0, 128), [128, 256)
+constexpr uint32_t kColP = 256;     // P buffers: columns [256, 320), [320, 384)
 constexpr uint32_t kColO = 384;     // O: columns [384, 512)
 
 struct AttnArgs {
@@ -72,8 +74,9 @@ struct AttnArgs {
 struct Shared {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full[2], q_free[2];
-  uint64_t s_full[kSBufs], p_ready[kSBufs];
-  uint64_t pv_done[kSBufs];    // PV step t completes a phase of pv_done[t % 3]
+  uint64_t s_full[kSBufs], s_free[kSBufs];   // QK(t) written / read by the softmax
+  uint64_t p_ready[kPBufs];
+  uint64_t pv_done[kPBufs];    // PV step t completes a phase of pv_done[t % 2]
   uint64_t o_full, o_free;      // one phase per work item
   uint64_t mma_done[2];         // QK and PV issuers' MMAs complete
   float pmax[2][2][kT];        // [tile parity][column half][row] partial row maxima
@@ -172,11 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&sh.s_full[b], 1);
+      mbar_init(&sh.s_free[b], kSoftmax);
+    }
+    for (int b = 0; b < kPBufs; ++b) {
       mbar_init(&sh.p_ready[b], kSoftmax);
     }
     mbar_init(&sh.o_full, 1);
     mbar_init(&sh.o_free, kSoftmax);
-    for (int b = 0; b < kSBufs; ++b) mbar_init(&sh.pv_done[b], 1);
+    for (int b = 0; b < kPBufs; ++b) mbar_init(&sh.pv_done[b], 1);
     mbar_init(&sh.mma_done[0], 1);
     mbar_init(&sh.mma_done[1], 1);
     sh.abort = 0;
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = st % kSBufs;
         const int s = pos % kStages;
         if (st >= kSBufs &&
-            !awaitb(&sh.pv_done[sb], ((st - kSBufs) / kSBufs) & 1, sh, a.err))   // PV(st - 3) done
+            !awaitb(&sh.s_free[sb], ((st - kSBufs) / kSBufs) & 1, sh, a.err))   // S(st - 2) read
           return false;
         if (!awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err)) return false;
         tc_fence_after_sync();
@@ -289,11 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto pv = [&](int o, int j, int ntl) -> bool {
-        const int sb = pvc % kSBufs;
+        const int sb = pvc % kPBufs;
         const int s = pos % kStages;
         // O is single-buffered: item o-1's epilogue has read it
         if (j == 0 && !awaitb(&sh.o_free, (o & 1) ^ 1, sh, a.err)) return false;
-        if (!awaitb(&sh.p_ready[sb], (pvc / kSBufs) & 1, sh, a.err) ||
+        if (!awaitb(&sh.p_ready[sb], (pvc / kPBufs) & 1, sh, a.err) ||
             !awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err))
           return false;
         tc_fence_after_sync();
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // against the same V rows
 #pragma unroll
         for (int kk = 0; kk < 2 * kT / 32; ++kk)
-          tc_mma_f8_tmem_a(tmem + kColO, tmem + kColS + sb * kT + 8 * kk,
+          tc_mma_f8_tmem_a(tmem + kColO, tmem + kColP + sb * 64 + 8 * kk,
                            db0 + (32 * kD / 16) * (kk & 3), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.empty[s]);
         tc_commit(&sh.pv_done[sb]);
@@ -380,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(srow + 64 * half, v0);
         tmem_ld32(srow + 64 * half + 32, v1);
         tmem_ld_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sh.s_free[sb]);   // QK(st + 2) may overwrite this S buffer
         // raw logits; masked keys -inf (sc > 0, so max and order carry over)
         float x[64];
 #pragma unroll
@@ -392,9 +400,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 64; ++c)
             if (c > climit) x[c] = -INFINITY;
         }
-        float xm = -INFINITY;
+        // row maximum in eight independent chains (a single chain of 64
+        // dependent max operations is latency-bound)
+        float xm8[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) xm = fmaxf(xm, x[c]);
+        for (int i = 0; i < 8; ++i) xm8[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < 64; ++c) xm8[c & 7] = fmaxf(xm8[c & 7], x[c]);
+        float xm = fmaxf(fmaxf(fmaxf(xm8[0], xm8[1]), fmaxf(xm8[2], xm8[3])),
+                         fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
         sh.pmax[st & 1][half][r] = xm;
         named_barrier(bar_id, 64);
         xm = fmaxf(xm, sh.pmax[st & 1][half ^ 1][r]);
@@ -415,8 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (__any_sync(0xffffffffu, need)) {
           // the previous PV of this item must have finished writing O (PV
-          // steps t-1 and t-2 may still be in flight; t+2 cannot be done)
-          awaitb(&sh.pv_done[(st - 1) % kSBufs], ((st - 1) / kSBufs) & 1, sh, a.err);
+          // step t-1 may still be in flight; t+1 cannot be done)
+          awaitb(&sh.pv_done[(st - 1) % kPBufs], ((st - 1) / kPBufs) & 1, sh, a.err);
           __syncwarp();
           tc_fence_after_sync();
           const uint32_t orow = tmem + lane_base + kColO + 64 * half;
@@ -435,13 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // significant bits, built in f16x2), packed four keys per column
         const float nm = m > -INFINITY ? -m : 0.f;   // a row that sees no key gets p = 0
         uint32_t pk[16], pl[16];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sum chains
 #pragma unroll
         for (int wq = 0; wq < 16; ++wq) {
           float p[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             p[e] = fast_exp2(fmaf(x[4 * wq + e], sc, nm));
-            l += p[e];
+            ls[e] += p[e];
           }
           const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
           const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
@@ -452,11 +467,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[wq] = h01 | (static_cast<uint32_t>(h23) << 16);
           pl[wq] = l01 | (static_cast<uint32_t>(l23) << 16);
         }
-        tmem_st16(srow + 16 * half, pk);        // columns [0, 32): hi terms
-        tmem_st16(srow + 32 + 16 * half, pl);   // columns [32, 64): lo terms
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // the P buffer of step st was read by PV(st - 2)
+        const int pb = st % kPBufs;
+        if (st >= kPBufs) {
+          awaitb(&sh.pv_done[pb], ((st - kPBufs) / kPBufs) & 1, sh, a.err);
+          __syncwarp();
+          tc_fence_after_sync();
+        }
+        const uint32_t prow = tmem + lane_base + kColP + pb * 64;
+        tmem_st16(prow + 16 * half, pk);        // columns [0, 32): hi terms
+        tmem_st16(prow + 32 + 16 * half, pl);   // columns [32, 64): lo terms
         tmem_st_wait();
         tc_fence_before_sync();
-        mbar_arrive(&sh.p_ready[sb]);
+        mbar_arrive(&sh.p_ready[pb]);
         ++st;
       }
       // ---- the row's denominator: this half's partial sum plus the other's
