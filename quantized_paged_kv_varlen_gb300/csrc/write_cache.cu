@@ -126,11 +126,18 @@ __device__ __forceinline__ void rope_quant_block(const uint16_t* __restrict__ sr
       float a[8], bb[8];
       load_bf16x8(src_row + half * 32 + c * 8, a);
       load_bf16x8(src_row + 64 + half * 32 + c * 8, bb);
+      // this chunk's 8 cos / sin values: two 16-byte loads each
+      const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * 64 +
+                                                         half * 32 + c * 8);
+      const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * 64 +
+                                                         half * 32 + c * 8);
+      const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+      const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int i = half * 32 + c * 8 + j;
-        const float cs = __ldg(cos_t + static_cast<size_t>(pos) * 64 + i);
-        const float sn = __ldg(sin_t + static_cast<size_t>(pos) * 64 + i);
+        const float cs = cv[j];
+        const float sn = sv[j];
         const float r1 = __fsub_rn(__fmul_rn(a[j], cs), __fmul_rn(bb[j], sn));
         const float r2 = __fadd_rn(__fmul_rn(bb[j], cs), __fmul_rn(a[j], sn));
         y1[c * 8 + j] = r1;
