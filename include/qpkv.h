@@ -329,6 +329,12 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
  *                 sequence whose lengths exceed num_blocks * 128, the
  *                 block_table row or num_tokens: its rows are zeroed),
  *                 QPKV_DEV_ERR_TIMEOUT.
+ * Ragged K/V (flashinfer's BatchPrefillWithRaggedKVCache layout, "[Refactor]
+ * Unify JIT/Customization/AOT mode", Batch Prefill): with cu_seqlens_kv set,
+ * k_pool is int8 [num_kv_tokens, Hkv, 128] and v_pool bf16 [num_kv_tokens,
+ * Hkv, 128], sequence b's keys are rows [cu_kv[b-1], cu_kv[b]) and L_kv[b]
+ * = cu_kv[b] - cu_kv[b-1]; block_table, seqlens_kv, page_size and
+ * num_pages are not used (block_table and seqlens_kv may be NULL).
  * Supported: head_dim 128, page_size a multiple of 16 that divides 128 or
  * is a multiple of 128, Hq % Hkv == 0.  q, k_pool, v_pool, o 16-byte
  * aligned.  sm_scale <= 0 selects 1/sqrt(128).
@@ -347,9 +353,10 @@ typedef struct qpkv_prefill_params {
   int32_t num_blocks;    /* dim 1 of q_block_scale / k_block_scale */
   int32_t causal;
   float sm_scale;
-  int32_t pad0;
+  int32_t num_kv_tokens;  /* ragged K/V only: rows of k_pool / v_pool */
   const int32_t* cu_seqlens_q;
   const int32_t* seqlens_kv;
+  const int32_t* cu_seqlens_kv;  /* NULL: paged K/V; else ragged, inclusive prefix sums [B] */
   const int32_t* block_table;
   const void* q;
   const float* q_block_scale;
@@ -369,6 +376,24 @@ typedef struct qpkv_prefill_params {
 size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads_q);
 
 qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* params, void* stream);
+
+/* ------------------------------------------------------ CSR page description
+ * flashinfer's CSR description of a paged cache ("[Refactor] Unify
+ * JIT/Customization/AOT mode", Batch Decode/Prefill: paged_kv_indptr,
+ * paged_kv_indices, paged_kv_last_page_len) -> this library's block_table
+ * rows and per-request lengths, on the host:
+ *   block_table[b][i] = indices[indptr[b] + i] for i < n_b = indptr[b+1] - indptr[b]
+ *   seqlens[b] = (n_b - 1) * page_size + last_page_len[b]   (0 when n_b = 0)
+ * Entries of block_table past n_b are set to -1.  Host arrays: indptr [B+1],
+ * indices [indptr[B]], last_page_len [B], block_table_out [B, bt_stride],
+ * seqlens_out [B] (caller-allocated).
+ * Errors: INVALID_ARG (null pointer, B < 0, page_size < 1, indptr not
+ * starting at 0 or decreasing, n_b > bt_stride, last_page_len[b] outside
+ * [1, page_size] for n_b > 0, a length above INT32_MAX). */
+qpkv_status qpkv_csr_to_block_table(const int32_t* indptr, const int32_t* indices,
+                                    const int32_t* last_page_len, int32_t batch,
+                                    int32_t page_size, int32_t bt_stride,
+                                    int32_t* block_table_out, int32_t* seqlens_out);
 
 /* ------------------------------------------------ MLA-absorb sparse decode
  * ("KvQuantSparseFlashAttention" README, 计算公式; 参数说明 rows query, key,

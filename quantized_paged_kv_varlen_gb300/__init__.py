@@ -68,9 +68,9 @@ class PrefillParams(ctypes.Structure):
     _fields_ = [(n, _i32) for n in (
         "num_seqs", "num_tokens", "num_heads_q", "num_heads_kv", "head_dim", "page_size",
         "num_pages", "bt_stride", "num_blocks", "causal")] + [
-        ("sm_scale", ctypes.c_float), ("pad0", _i32)] + [
+        ("sm_scale", ctypes.c_float), ("num_kv_tokens", _i32)] + [
         (n, _p) for n in (
-            "cu_seqlens_q", "seqlens_kv", "block_table", "q", "q_block_scale", "k_pool",
+            "cu_seqlens_q", "seqlens_kv", "cu_seqlens_kv", "block_table", "q", "q_block_scale", "k_pool",
             "k_block_scale", "v_pool", "o", "lse", "workspace")] + [
         ("workspace_bytes", ctypes.c_size_t), ("error_word", _p)]
 
@@ -111,6 +111,7 @@ def _declare(lib):
                                      ctypes.c_float, _i32, _p, _p, _p, _p]),
         "qpkv_prefill_workspace_bytes": (S, [_i32, _i32, _i32]),
         "qpkv_prefill_paged": (_i32, [ctypes.POINTER(PrefillParams), _p]),
+        "qpkv_csr_to_block_table": (_i32, [_p, _p, _p, _i32, _i32, _i32, _p, _p]),
         "qpkv_mla_workspace_bytes": (S, [_i32, _i32]),
         "qpkv_mla_sparse_decode": (_i32, [ctypes.POINTER(MlaParams), _p]),
     }
@@ -439,28 +440,43 @@ def prefill_workspace(num_seqs, num_tokens, num_heads_q, device="cuda"):
 
 def prefill_paged(q8, q_block_scale, k_pool, k_block_scale, v_pool, block_table, cu_seqlens_q,
                   seqlens_kv, sm_scale=None, causal=True, out=None, lse=None, workspace=None,
-                  error_word=None):
-    """Varlen prefill with INT8 Q/K (block-128 scales) and bf16 V over a paged
-    cache: q8 int8 [T, Hq, 128]; k_pool int8 / v_pool bf16 [P, ps, Hkv, 128];
-    scales fp32 [B, NB, H]; returns bf16 O [T, Hq, 128] (``lse`` fp32 [T, Hq]
+                  error_word=None, cu_seqlens_kv=None):
+    """Varlen prefill with INT8 Q/K (block-128 scales) and bf16 V: q8 int8
+    [T, Hq, 128]; a paged cache k_pool int8 / v_pool bf16 [P, ps, Hkv, 128]
+    with block_table and seqlens_kv, or (cu_seqlens_kv given) ragged K/V
+    [T_kv, Hkv, 128] with inclusive prefix sums of the kv lengths; scales
+    fp32 [B, NB, H]; returns bf16 O [T, Hq, 128] (``lse`` fp32 [T, Hq]
     filled when given)."""
     torch = _torch()
     lib = load()
+    ragged = cu_seqlens_kv is not None
     _need(q8, "q8", torch.int8, 3)
-    _need(k_pool, "k_pool", torch.int8, 4)
-    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(k_pool, "k_pool", torch.int8, 3 if ragged else 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 3 if ragged else 4)
     _need(q_block_scale, "q_block_scale", torch.float32, 3)
     _need(k_block_scale, "k_block_scale", torch.float32, 3)
-    _need(block_table, "block_table", torch.int32, 2)
     _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
-    _need(seqlens_kv, "seqlens_kv", torch.int32, 1)
     T, Hq, D = q8.shape
-    P, ps, Hkv, _ = k_pool.shape
     B = cu_seqlens_q.shape[0]
     if tuple(v_pool.shape) != tuple(k_pool.shape):
         raise ValueError("v_pool must match k_pool's shape")
-    if seqlens_kv.shape[0] != B or block_table.shape[0] != B:
-        raise ValueError("seqlens_kv / block_table must have one row per sequence")
+    prm = PrefillParams()
+    if ragged:
+        _need(cu_seqlens_kv, "cu_seqlens_kv", torch.int32, 1)
+        if cu_seqlens_kv.shape[0] != B:
+            raise ValueError("cu_seqlens_kv must have one entry per sequence")
+        T_kv, Hkv, _ = k_pool.shape
+        prm.num_kv_tokens = T_kv
+        prm.cu_seqlens_kv = _ptr(cu_seqlens_kv)
+        prm.page_size, prm.num_pages, prm.bt_stride = 128, 1, 1
+    else:
+        _need(block_table, "block_table", torch.int32, 2)
+        _need(seqlens_kv, "seqlens_kv", torch.int32, 1)
+        P, ps, Hkv, _ = k_pool.shape
+        if seqlens_kv.shape[0] != B or block_table.shape[0] != B:
+            raise ValueError("seqlens_kv / block_table must have one row per sequence")
+        prm.page_size, prm.num_pages, prm.bt_stride = ps, P, block_table.shape[1]
+        prm.seqlens_kv, prm.block_table = _ptr(seqlens_kv), _ptr(block_table)
     NB = q_block_scale.shape[1]
     if tuple(q_block_scale.shape) != (B, NB, Hq) or tuple(k_block_scale.shape) != (B, NB, Hkv):
         raise ValueError("block scales must be [B, NB, Hq] and [B, NB, Hkv]")
@@ -470,21 +486,39 @@ def prefill_paged(q8, q_block_scale, k_pool, k_block_scale, v_pool, block_table,
         _need(lse, "lse", torch.float32, 2)
     if workspace is None:
         workspace = prefill_workspace(B, T, Hq, q8.device)
-    prm = PrefillParams()
     prm.num_seqs, prm.num_tokens, prm.num_heads_q, prm.num_heads_kv = B, T, Hq, Hkv
-    prm.head_dim, prm.page_size, prm.num_pages = D, ps, P
-    prm.bt_stride = block_table.shape[1]
+    prm.head_dim = D
     prm.num_blocks = NB
     prm.causal = 1 if causal else 0
     prm.sm_scale = float(sm_scale) if sm_scale else 0.0
-    prm.cu_seqlens_q, prm.seqlens_kv = _ptr(cu_seqlens_q), _ptr(seqlens_kv)
-    prm.block_table, prm.q, prm.q_block_scale = _ptr(block_table), _ptr(q8), _ptr(q_block_scale)
+    prm.cu_seqlens_q = _ptr(cu_seqlens_q)
+    prm.q, prm.q_block_scale = _ptr(q8), _ptr(q_block_scale)
     prm.k_pool, prm.k_block_scale, prm.v_pool = _ptr(k_pool), _ptr(k_block_scale), _ptr(v_pool)
     prm.o, prm.lse = _ptr(out), _ptr(lse)
     prm.workspace, prm.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     prm.error_word = _ptr(error_word)
     _check(lib.qpkv_prefill_paged(ctypes.byref(prm), _stream()), "qpkv_prefill_paged")
     return out
+
+
+def csr_to_block_table(indptr, indices, last_page_len, page_size, bt_stride=None):
+    """flashinfer's CSR page description (numpy int32 arrays) -> (block_table
+    int32 [B, bt_stride], seqlens int32 [B]), computed by the library."""
+    import numpy as np
+    lib = load()
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    last = np.ascontiguousarray(last_page_len, dtype=np.int32)
+    B = len(indptr) - 1
+    if bt_stride is None:
+        bt_stride = max(1, int(np.max(np.diff(indptr))) if B > 0 else 1)
+    bt = np.empty((B, bt_stride), dtype=np.int32)
+    lens = np.empty(B, dtype=np.int32)
+    st = lib.qpkv_csr_to_block_table(indptr.ctypes.data, indices.ctypes.data if indices.size else None,
+                                     last.ctypes.data, B, int(page_size), int(bt_stride),
+                                     bt.ctypes.data, lens.ctypes.data)
+    _check(st, "qpkv_csr_to_block_table")
+    return bt, lens
 
 
 def mla_workspace(num_tokens, sparse_size, device="cuda"):

@@ -1,6 +1,7 @@
 // The extern "C" boundary: argument checks, the host decode planner, tensor
 // maps, and dispatch to the kernel launchers.  No exception leaves this file;
 // no allocation, free or synchronisation happens here.
+#include <climits>
 #include <cstdint>
 #include <algorithm>
 #include <cstring>
@@ -412,18 +413,23 @@ size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_
 
 qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* p, void* stream) {
   if (p == nullptr) return QPKV_ERR_INVALID_ARG;
+  const bool ragged = p->cu_seqlens_kv != nullptr;
   if (p->num_seqs < 0 || p->num_tokens < 0 || p->num_heads_q <= 0 || p->num_heads_kv <= 0 ||
-      p->num_pages <= 0 || p->bt_stride <= 0 || p->num_blocks <= 0 || p->page_size <= 0)
+      p->num_blocks <= 0)
+    return QPKV_ERR_INVALID_ARG;
+  if (ragged ? p->num_kv_tokens < 0
+             : (p->num_pages <= 0 || p->bt_stride <= 0 || p->page_size <= 0))
     return QPKV_ERR_INVALID_ARG;
   const int ps = p->page_size;
-  if (p->head_dim != 128 || p->num_heads_q % p->num_heads_kv != 0 || ps % 16 != 0 ||
-      (128 % ps != 0 && ps % 128 != 0))
-    return QPKV_ERR_UNSUPPORTED;
+  if (p->head_dim != 128 || p->num_heads_q % p->num_heads_kv != 0) return QPKV_ERR_UNSUPPORTED;
+  if (!ragged && (ps % 16 != 0 || (128 % ps != 0 && ps % 128 != 0))) return QPKV_ERR_UNSUPPORTED;
   if (p->num_seqs == 0 || p->num_tokens == 0) return QPKV_OK;
-  if (p->cu_seqlens_q == nullptr || p->seqlens_kv == nullptr || p->block_table == nullptr ||
-      p->q == nullptr || p->q_block_scale == nullptr || p->k_pool == nullptr ||
-      p->k_block_scale == nullptr || p->v_pool == nullptr || p->o == nullptr ||
-      p->workspace == nullptr)
+  if (p->cu_seqlens_q == nullptr || p->q == nullptr || p->q_block_scale == nullptr ||
+      p->k_block_scale == nullptr || p->o == nullptr || p->workspace == nullptr)
+    return QPKV_ERR_INVALID_ARG;
+  if (!ragged && (p->seqlens_kv == nullptr || p->block_table == nullptr))
+    return QPKV_ERR_INVALID_ARG;
+  if ((!ragged || p->num_kv_tokens > 0) && (p->k_pool == nullptr || p->v_pool == nullptr))
     return QPKV_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->k_pool) || !aligned16(p->v_pool) || !aligned16(p->o) ||
       !aligned16(p->workspace))
@@ -434,6 +440,32 @@ qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* p, void* stream) {
   const cudaError_t e = launch_prefill_int8(*p, static_cast<cudaStream_t>(stream), &status);
   if (status != QPKV_OK) return static_cast<qpkv_status>(status);
   return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
+}
+
+qpkv_status qpkv_csr_to_block_table(const int32_t* indptr, const int32_t* indices,
+                                    const int32_t* last_page_len, int32_t batch,
+                                    int32_t page_size, int32_t bt_stride,
+                                    int32_t* block_table_out, int32_t* seqlens_out) {
+  if (batch < 0 || page_size < 1 || bt_stride < 0) return QPKV_ERR_INVALID_ARG;
+  if (indptr == nullptr || (batch > 0 && (last_page_len == nullptr || seqlens_out == nullptr)))
+    return QPKV_ERR_INVALID_ARG;
+  if (batch > 0 && bt_stride > 0 && block_table_out == nullptr) return QPKV_ERR_INVALID_ARG;
+  if (indptr[0] != 0) return QPKV_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t n = static_cast<int64_t>(indptr[b + 1]) - indptr[b];
+    if (n < 0 || n > bt_stride) return QPKV_ERR_INVALID_ARG;
+    if (n > 0 && indices == nullptr) return QPKV_ERR_INVALID_ARG;
+    if (n > 0 && (last_page_len[b] < 1 || last_page_len[b] > page_size)) return QPKV_ERR_INVALID_ARG;
+    const int64_t len = n > 0 ? (n - 1) * page_size + last_page_len[b] : 0;
+    if (len > INT32_MAX) return QPKV_ERR_INVALID_ARG;
+  }
+  for (int b = 0; b < batch; ++b) {
+    const int n = indptr[b + 1] - indptr[b];
+    for (int i = 0; i < bt_stride; ++i)
+      block_table_out[static_cast<size_t>(b) * bt_stride + i] = i < n ? indices[indptr[b] + i] : -1;
+    seqlens_out[b] = n > 0 ? (n - 1) * page_size + last_page_len[b] : 0;
+  }
+  return QPKV_OK;
 }
 
 size_t qpkv_mla_workspace_bytes(int32_t num_tokens, int32_t sparse_size) {

@@ -73,6 +73,7 @@ constexpr uint32_t kColO = 384;         // O: columns [384, 512)
 
 struct PArgs {
   int B, T, Hq, Hkv, G, ps, P, bt_stride, NB, causal;
+  int ragged, T_kv;     // ragged K/V: rows [T_kv, Hkv, D] addressed from the unit record
   int rows_box, nbox;   // page rows per TMA box, boxes per 128-key tile
   float scale_log2;     // softmax scale * log2(e)
   const int32_t* cu_q;  // [B] inclusive prefix sums
@@ -171,12 +172,14 @@ __device__ __forceinline__ void q_tile_range(int Lq, int Lk, int causal, int& qt
 
 struct Tile {
   int b, h, qt, begin, Lq, Lk, nkv;
+  int kvb;   // ragged K/V: the sequence's first row
 };
 
 // Workspace: int32 [0] unit count, [1, 1 + 4B) the sequences in cost order
 // (kWs* fields), [1 + 4B, 1 + 5B) their costs; from byte offset
 // units_offset(B) one 32-byte record per unit in that order:
-//   {b, h, qt_a, qt_b (-1 when the unit has one q tile), begin, Lq, Lk, 0}.
+//   {b, h, qt_a, qt_b (-1 when the unit has one q tile), begin, Lq, Lk,
+//    first K/V row (ragged K/V; 0 for a paged cache)}.
 __host__ __device__ __forceinline__ size_t units_offset(int B) {
   return ((static_cast<size_t>(1 + (kWsStride + 1) * static_cast<size_t>(B)) * 4 + 15) / 16) * 16;
 }
@@ -210,6 +213,7 @@ struct Items {
     t.begin = r1.x;
     t.Lq = r1.y;
     t.Lk = r1.z;
+    t.kvb = r1.w;
     t.nkv = kv_tiles_of(t.Lq, t.Lk, t.qt, a.causal);
   }
   __device__ __forceinline__ void advance() {
@@ -277,6 +281,7 @@ constexpr int kNoKey = -2147483647 - 1;
 struct BoxIds {
   int i0, i1, i2, i3, i4, i5, i6, i7;
   __device__ __forceinline__ void load(const PArgs& a, const Tile& t, int j) {
+    if (a.ragged) return;   // rows follow from the sequence's first row
     const int32_t* row = a.bt + static_cast<size_t>(t.b) * a.bt_stride;
     const int k0 = j * kT;
     auto one = [&](int i) -> int {
@@ -361,8 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // pool row of box i of key tile j; keys past L_kv and bad page ids read
   // rows past the pool's end, which the copy fills with zeros
-  const int oob = a.P * a.ps;
-  auto page_row = [&](const BoxIds& ids, int i, int j) -> int {
+  const int oob = a.ragged ? a.T_kv : a.P * a.ps;
+  auto page_row = [&](const Tile& t, const BoxIds& ids, int i, int j) -> int {
+    if (a.ragged) {
+      const int key0 = j * kT + i * a.rows_box;
+      return key0 < t.Lk ? t.kvb + key0 : oob;
+    }
     const int id = ids.get(i);
     if (id == kNoKey) return oob;
     if (id < 0 || id >= a.P) {
@@ -404,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int i = 0; i < a.nbox; ++i)
             tma_load_3d(dst + i * a.rows_box * 128, &k_map, &sh.k8_full[s], 0, t.h / a.G,
-                        page_row(ids, i, ld.j));
+                        page_row(ld.t, ids, i, ld.j));
         }
         ++ipos;
         ld.next(a);
@@ -520,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile& t = vw.t;
 #pragma unroll 1
         for (int i = 0; i < a.nbox; ++i) {
-          const int row = page_row(vids, i, vw.j);
+          const int row = page_row(vw.t, vids, i, vw.j);
           uint8_t* dst = smem + kOffV + s * kH16Tile + i * a.rows_box * 128;
           tma_load_3d(dst, &v_map, &sh.v_full[s], 0, t.h / a.G, row);
           tma_load_3d(dst + kHalf, &v_map, &sh.v_full[s], 64, t.h / a.G, row);
@@ -803,8 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct PrepArgs {
   int B, T, Hq, NB, causal, ps, bt_stride;
+  int ragged, T_kv;
   const int32_t* cu_q;
   const int32_t* lk;
+  const int32_t* cu_kv;   // ragged K/V: inclusive prefix sums of L_kv
   int32_t* ws;   // [0] units, [1, 1 + 4B) table, [1 + 4B, 1 + 5B) costs
   uint16_t* o;
   float* lse;
@@ -818,10 +829,12 @@ __device__ __forceinline__ bool seq_info(const PrepArgs& p, int b, int& begin, i
   begin = b > 0 ? p.cu_q[b - 1] : 0;
   const int end = p.cu_q[b];
   Lq = end - begin;
-  Lk = p.lk[b];
+  const int kvb = p.ragged ? (b > 0 ? p.cu_kv[b - 1] : 0) : 0;
+  Lk = p.ragged ? p.cu_kv[b] - kvb : p.lk[b];
+  const bool kv_ok = p.ragged ? kvb >= 0 && p.cu_kv[b] <= p.T_kv
+                              : static_cast<long long>(Lk) <= static_cast<long long>(p.bt_stride) * p.ps;
   const bool ok = begin >= 0 && Lq >= 0 && end <= p.T && Lk >= 0 &&
-                  (Lq + kT - 1) / kT <= p.NB && (Lk + kT - 1) / kT <= p.NB &&
-                  static_cast<long long>(Lk) <= static_cast<long long>(p.bt_stride) * p.ps;
+                  (Lq + kT - 1) / kT <= p.NB && (Lk + kT - 1) / kT <= p.NB && kv_ok;
   int nqt = 0;
   qt_lo = 0;
   if (ok) q_tile_range(Lq, Lk, p.causal, qt_lo, nqt);
@@ -900,9 +913,11 @@ __global__ void __launch_bounds__(256) prefill_units_kernel(const PrepArgs p) {
   const int pairs = (nqv + 1) >> 1;
   const int tt = local % pairs;
   const int begin = b > 0 ? p.cu_q[b - 1] : 0;
+  const int kvb = p.ragged ? (b > 0 ? p.cu_kv[b - 1] : 0) : 0;
+  const int Lk = p.ragged ? p.cu_kv[b] - kvb : p.lk[b];
   int4* rec = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(p.ws) + units_offset(p.B)) + 2 * u;
   rec[0] = make_int4(b, local / pairs, qt_lo + tt, nqv - 1 - tt != tt ? qt_lo + nqv - 1 - tt : -1);
-  rec[1] = make_int4(begin, p.cu_q[b] - begin, p.lk[b], 0);
+  rec[1] = make_int4(begin, p.cu_q[b] - begin, Lk, kvb);
 }
 
 // Upper bound of the unit count: sum_b ceil(ceil(L_b / 128) / 2) per head is
@@ -921,9 +936,13 @@ size_t prefill_workspace_bytes(int num_seqs, int num_tokens, int num_heads_q) {
 cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t stream, int* status) {
   *status = QPKV_OK;
   if (p.num_seqs == 0 || p.num_tokens == 0) return cudaSuccess;
-  const int ps = p.page_size;
+  const bool ragged = p.cu_seqlens_kv != nullptr;
+  const int ps = ragged ? kT : p.page_size;
   const int rows_box = ps < kT ? ps : kT;
   PrepArgs pa;
+  pa.ragged = ragged ? 1 : 0;
+  pa.T_kv = p.num_kv_tokens;
+  pa.cu_kv = p.cu_seqlens_kv;
   pa.B = p.num_seqs;
   pa.T = p.num_tokens;
   pa.Hq = p.num_heads_q;
@@ -945,12 +964,14 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   prefill_units_kernel<<<static_cast<unsigned>((umax + 255) / 256), 256, 0, stream>>>(pa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (ragged && p.num_kv_tokens == 0) return cudaSuccess;   // no keys: the prep pass wrote every row
 
   // q [T, Hq, D] int8, pools [P * ps, Hkv, D] (int8 K, bf16 V) as 3-D maps
   // (d, head, row); a box is 128 q rows / one page's rows of one head
   const uint64_t D = kD, T = static_cast<uint64_t>(p.num_tokens);
   const uint64_t Hq = static_cast<uint64_t>(p.num_heads_q), Hkv = static_cast<uint64_t>(p.num_heads_kv);
-  const uint64_t rows = static_cast<uint64_t>(p.num_pages) * ps;
+  const uint64_t rows = ragged ? static_cast<uint64_t>(p.num_kv_tokens)
+                               : static_cast<uint64_t>(p.num_pages) * ps;
   CUtensorMap qm, km, vm;
   const uint64_t qdims[3] = {D, Hq, T}, qstr[2] = {D, Hq * D};
   const uint64_t kdims[3] = {D, Hkv, rows}, kstr[2] = {D, Hkv * D};
@@ -979,6 +1000,8 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   a.bt_stride = p.bt_stride;
   a.NB = p.num_blocks;
   a.causal = p.causal ? 1 : 0;
+  a.ragged = ragged ? 1 : 0;
+  a.T_kv = p.num_kv_tokens;
   a.rows_box = rows_box;
   a.nbox = kT / rows_box;
   a.scale_log2 = (p.sm_scale > 0.f ? p.sm_scale : 1.0f / sqrtf(static_cast<float>(kD))) * kLog2e;

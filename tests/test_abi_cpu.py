@@ -269,6 +269,63 @@ def test_mla_rejects_before_launch(qlib):
     p.num_tokens = 0
     assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 0
 
+
+def test_csr_to_block_table(qlib):
+    """flashinfer's CSR page description -> block_table rows and lengths."""
+    q, lib = qlib
+    indptr = np.array([0, 3, 3, 5], np.int32)
+    indices = np.array([7, 2, 9, 4, 1], np.int32)
+    last = np.array([16, 5, 1], np.int32)
+    bt, lens = q.csr_to_block_table(indptr, indices, last, 16, bt_stride=4)
+    assert bt.tolist() == [[7, 2, 9, -1], [-1, -1, -1, -1], [4, 1, -1, -1]]
+    assert lens.tolist() == [48, 0, 17]
+    # round trip from a random block table
+    rng = np.random.default_rng(4)
+    L = rng.integers(0, 400, 20).astype(np.int32)
+    n = (L + 15) // 16
+    ptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    ids = rng.permutation(int(ptr[-1])).astype(np.int32)
+    lastp = np.where(n > 0, L - (n - 1) * 16, 1).astype(np.int32)
+    bt2, lens2 = q.csr_to_block_table(ptr, ids, lastp, 16)
+    assert np.array_equal(lens2, L)
+    for b in range(20):
+        assert np.array_equal(bt2[b, :n[b]], ids[ptr[b]:ptr[b + 1]])
+        assert np.all(bt2[b, n[b]:] == -1)
+    # rejected descriptions
+    def bad(ip, ix, lp, stride=4):
+        arrs = [np.ascontiguousarray(x, np.int32) for x in (ip, ix, lp)]
+        outs = [np.zeros((len(ip) - 1) * stride, np.int32), np.zeros(len(ip) - 1, np.int32)]
+        return lib.qpkv_csr_to_block_table(arrs[0].ctypes.data, arrs[1].ctypes.data,
+                                           arrs[2].ctypes.data, len(ip) - 1, 16, stride,
+                                           outs[0].ctypes.data, outs[1].ctypes.data)
+    assert bad([0, 2], [1, 2], [0]) == 1          # last page holds no token
+    assert bad([0, 2], [1, 2], [17]) == 1         # more than a page
+    assert bad([0, 3, 2], [1, 2, 3], [1, 1]) == 1 # decreasing indptr
+    assert bad([1, 3], [1, 2, 3], [1]) == 1       # indptr not starting at 0
+    assert bad([0, 5], [1, 2, 3, 4, 5], [1]) == 1  # more pages than the row holds
+    assert bad([0, 2], [1, 2], [3]) == 0
+
+
+def test_prefill_ragged_rejects_before_launch(qlib):
+    q, lib = qlib
+    p = q.PrefillParams()
+    fake = 0x100000
+    for n in ("cu_seqlens_q", "cu_seqlens_kv", "q", "q_block_scale", "k_pool", "k_block_scale",
+              "v_pool", "o", "workspace"):
+        setattr(p, n, fake)
+    p.num_seqs, p.num_tokens, p.num_heads_q, p.num_heads_kv = 2, 300, 4, 2
+    p.head_dim, p.num_blocks, p.num_kv_tokens, p.causal = 128, 3, 500, 1
+    p.workspace_bytes = lib.qpkv_prefill_workspace_bytes(2, 300, 4)
+    p.page_size = 24                # ignored with ragged K/V
+    p.num_kv_tokens = -1
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 1
+    p.num_kv_tokens = 500
+    p.k_pool = None
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 1
+    p.k_pool = fake
+    p.num_tokens = 0
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 0
+
 def test_binding_raises_without_library(tmp_path):
     import quantized_paged_kv_varlen_gb300 as q
     saved = q._lib

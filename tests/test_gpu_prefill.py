@@ -142,6 +142,45 @@ def test_prefill_shapes(lib, Lq, Lk, Hq, Hkv, ps, causal):
     assert np.all(got_o[none] == 0.0)
 
 
+
+@pytest.mark.parametrize("Lq,Lk,Hq,Hkv,causal", [
+    ([1, 130, 300], [1, 130, 300], 2, 2, True),      # sequences back to back, ragged tails
+    ([77, 128, 1], [300, 128, 513], 4, 1, True),     # cached prefixes, GQA 4:1
+    ([300, 50], [40, 0], 2, 2, True),                # rows that see nothing, an empty sequence
+    ([130, 257], [390, 100], 2, 2, False),           # no mask
+])
+def test_prefill_ragged_kv(lib, Lq, Lk, Hq, Hkv, causal):
+    """Ragged (non-paged) K/V: sequence b's keys are rows [cu[b-1], cu[b]) of
+    one packed tensor.  The oracle sees the same rows as a page-size-1 pool
+    whose block table points at them."""
+    rng = np.random.default_rng((sum(Lk), 23))
+    Lq, Lk = np.asarray(Lq, np.int32), np.asarray(Lk, np.int32)
+    B, T, Tkv = len(Lq), int(Lq.sum()), int(Lk.sum())
+    nb = max(1, (int(max(Lq.max(), Lk.max())) + 127) // 128)
+    q8 = rng.integers(-127, 128, (T, Hq, 128), dtype=np.int8)
+    qs = (rng.uniform(0.5, 1.5, (B, nb, Hq)) * 3.0 / 127).astype(np.float32)
+    k8 = rng.integers(-127, 128, (max(Tkv, 1), Hkv, 128), dtype=np.int8)
+    ks = (rng.uniform(0.5, 1.5, (B, nb, Hkv)) * 3.0 / 127).astype(np.float32)
+    v_bits = ocache.bf16_bits(synth.bf16_normal(rng, (max(Tkv, 1), Hkv, 128)))
+    cu_kv = synth.inclusive_prefix(Lk)
+    kvb = np.concatenate([[0], cu_kv[:-1]]).astype(np.int32)
+    bt = np.full((B, max(1, int(Lk.max()))), -1, np.int32)
+    for b in range(B):
+        bt[b, :Lk[b]] = kvb[b] + np.arange(Lk[b])
+    cu_q = synth.inclusive_prefix(Lq)
+    lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    v_t = _t(v_bits[:Tkv].view(np.int16)).view(torch.bfloat16)
+    out = lib.prefill_paged(_t(q8), _t(qs), _t(k8[:Tkv]), _t(ks), v_t, None, _t(cu_q), None,
+                            causal=causal, lse=lse, error_word=err, cu_seqlens_kv=_t(cu_kv))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want_o, want_lse = oatt.paged_prefill_int8(q8, qs, k8.reshape(-1, 1, Hkv, 128), ks,
+                                               v_bits.reshape(-1, 1, Hkv, 128), bt, cu_q, Lk,
+                                               1.0 / np.sqrt(128.0), causal)
+    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
+
 def test_prefill_zero_scale_blocks(lib):
     """A key block and a query block whose scale is 0 (all-zero input
     blocks): their logits are exactly 0 and nothing turns into NaN."""
