@@ -563,7 +563,19 @@ def run_extras(device, iters=10):
         "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops, "write_cache_ms": ms_w,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s",
                      "frac": tf / bf16, "peak_source": "measured bf16_tflops (f16/bf16 MMAs)"}}
-    del k_pool, v_pool, q8p, qb, kb, vb, op
+    # the same prefill over ragged (packed, non-paged) K/V of the same sizes
+    gk = torch.Generator(device=device)
+    gk.manual_seed(13)
+    k_rag = torch.randint(-127, 128, (T, H, D), generator=gk, dtype=torch.int8, device=device)
+    v_rag = torch.randn((T, H, D), generator=gk, device=device).to(torch.bfloat16)
+    fr = lambda: q.prefill_paged(q8p, qs, k_rag, ks, v_rag, None, cu, None, causal=True, out=op,
+                                 workspace=wsp, error_word=err, cu_seqlens_kv=cu)
+    for _ in range(3):
+        fr()
+    ms_r = _median_ms(fr, iters)
+    out["int8_prefill_varlen"]["ragged_kv_ms"] = ms_r
+    out["int8_prefill_varlen"]["ragged_kv_tflops"] = flops / (ms_r / 1e3) / 1e12
+    del k_pool, v_pool, q8p, qb, kb, vb, op, k_rag, v_rag
 
     # MLA-absorb sparse decode
     d = synth.mla_sparse_device(0, device)
