@@ -20,10 +20,11 @@
 //                of 64 dims stream through shared memory (TMA for Q, eight
 //                converter warps gather and dequantise the rows), S for the
 //                four 128-key tiles accumulates in tensor memory; the
-//                epilogue writes the scaled logits (log2 units) and each
-//                tile's row maximum and sum of exponentials
-//   mla_softmax  per (token, head) row: the row's maximum and sum from the
-//                tile statistics, P = 2^(x - M) / L as bf16, and the lse
+//                epilogue (12 warps) writes P_tile = 2^(x - m) as bf16 with
+//                each tile's row maximum m and sum
+//   mla_softmax  per (token, head) row: the row's maximum M and sum L from
+//                the tile statistics, P = P_tile * 2^(m - M) / L in place,
+//                and the lse
 //   mla_pv       one CTA per (token, 128 output columns = one scale tile):
 //                P chunks by TMA, V chunks dequantised by the converter
 //                warps, O[128 x 128] in tensor memory, bf16 out.
@@ -56,9 +57,8 @@ struct MlaArgs {
   const int32_t* idx;       // [T, 1, S]
   const uint8_t* pool;      // [P * bs, 656]
   int32_t* rows;            // [T, Sp] pool row per key, -1 = masked
-  float* sx;                // [T, 128, Sp] logits in log2 units
   float* stats;             // [T, 128, Sp / 128, 2] tile (max, sum)
-  uint16_t* p;              // [T, 128, Sp] bf16
+  uint16_t* p;              // [T, 128, Sp] bf16: 2^(x - m_tile), then the normalised P
   uint16_t* o;              // [T, QN, 512] bf16
   float* lse;               // [T, QN] or null
   int* err;
@@ -306,20 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh.k_full[s]);
       }
     }
-  } else {
+  }
+  if (warp >= kConv0) {
     // ----------------------------------------------------------- epilogue
-    // One thread per head row: the scaled logits of each 128-key tile
-    // (masked keys -inf) go to the workspace with the tile's row maximum
-    // and sum of 2^(x - max).
-    const int sw = warp & 3, r = sw * 32 + lane;
+    // Warps 2-13 (the converters join once their units are done): quarter
+    // warp & 3 of the head rows, tiles {0, 3}, {1}, {2} by (warp - 2) / 4.
+    // Per tile and head row: m = the row maximum of the scaled logits
+    // (masked keys -inf), P_tile = 2^(x - m) in bf16 and l = sum P_tile to
+    // the workspace.
+    const int sw = warp & 3, part = (warp - kConv0) >> 2, r = sw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
     wait_bar(&sh.s_full, 0, a.err);
     __syncwarp();
     tc_fence_after_sync();
     const int32_t* rws = a.rows + static_cast<size_t>(t) * a.Sp + key0;
-    float* xrow = a.sx + (static_cast<size_t>(t) * kQN + r) * a.Sp + key0;
+    uint16_t* prow = a.p + (static_cast<size_t>(t) * kQN + r) * a.Sp + key0;
     const int ntile = a.Sp / 128;
-    for (int n = 0; n < nt; ++n) {
+    for (int n = part; n < nt; n += 3) {
       float m = -INFINITY;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -327,38 +330,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + 128 * n + 32 * cc, v);
         tmem_ld_wait();
         const int kb0 = 128 * n + 32 * cc;
-        float x[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const int4 rr = __ldg(reinterpret_cast<const int4*>(rws + kb0 + i));
-          x[i] = rr.x >= 0 ? __uint_as_float(v[i]) * a.scale_log2 : -INFINITY;
-          x[i + 1] = rr.y >= 0 ? __uint_as_float(v[i + 1]) * a.scale_log2 : -INFINITY;
-          x[i + 2] = rr.z >= 0 ? __uint_as_float(v[i + 2]) * a.scale_log2 : -INFINITY;
-          x[i + 3] = rr.w >= 0 ? __uint_as_float(v[i + 3]) * a.scale_log2 : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          *reinterpret_cast<float4*>(xrow + kb0 + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
-          m = fmaxf(m, fmaxf(fmaxf(x[i], x[i + 1]), fmaxf(x[i + 2], x[i + 3])));
+          m = fmaxf(m, fmaxf(fmaxf(rr.x >= 0 ? __uint_as_float(v[i]) : -INFINITY,
+                                   rr.y >= 0 ? __uint_as_float(v[i + 1]) : -INFINITY),
+                             fmaxf(rr.z >= 0 ? __uint_as_float(v[i + 2]) : -INFINITY,
+                                   rr.w >= 0 ? __uint_as_float(v[i + 3]) : -INFINITY)));
         }
       }
+      m = m > -INFINITY ? m * a.scale_log2 : -INFINITY;   // scale_log2 > 0 keeps the order
+      const float nm = m > -INFINITY ? -m : 0.f;
       float l = 0.f;
-      if (m > -INFINITY) {
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + 128 * n + 32 * cc, v);
-          tmem_ld_wait();
-          const int kb0 = 128 * n + 32 * cc;
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + 128 * n + 32 * cc, v);
+        tmem_ld_wait();
+        const int kb0 = 128 * n + 32 * cc;
+        uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const int4 rr = __ldg(reinterpret_cast<const int4*>(rws + kb0 + i));
-            l += (rr.x >= 0 ? fast_exp2(__uint_as_float(v[i]) * a.scale_log2 - m) : 0.f) +
-                 (rr.y >= 0 ? fast_exp2(__uint_as_float(v[i + 1]) * a.scale_log2 - m) : 0.f) +
-                 (rr.z >= 0 ? fast_exp2(__uint_as_float(v[i + 2]) * a.scale_log2 - m) : 0.f) +
-                 (rr.w >= 0 ? fast_exp2(__uint_as_float(v[i + 3]) * a.scale_log2 - m) : 0.f);
-          }
+        for (int i = 0; i < 32; i += 4) {
+          const int4 rr = __ldg(reinterpret_cast<const int4*>(rws + kb0 + i));
+          const float p0 = rr.x >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i]), a.scale_log2, nm)) : 0.f;
+          const float p1 = rr.y >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), a.scale_log2, nm)) : 0.f;
+          const float p2 = rr.z >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i + 2]), a.scale_log2, nm)) : 0.f;
+          const float p3 = rr.w >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i + 3]), a.scale_log2, nm)) : 0.f;
+          l += (p0 + p1) + (p2 + p3);
+          const __nv_bfloat162 b0 = __floats2bfloat162_rn(p0, p1);
+          const __nv_bfloat162 b1 = __floats2bfloat162_rn(p2, p3);
+          pk[i / 2] = *reinterpret_cast<const uint32_t*>(&b0);
+          pk[i / 2 + 1] = *reinterpret_cast<const uint32_t*>(&b1);
         }
+        uint4* dst = reinterpret_cast<uint4*>(prow + kb0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
       float* st = a.stats + ((static_cast<size_t>(t) * kQN + r) * ntile + (key0 / 128 + n)) * 2;
       st[0] = m;
@@ -374,37 +380,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------- softmax
-// One block per (token, head) row: M and L from the tile statistics, then
-// P = 2^(x - M) / L in bf16, eight keys per thread and step.
-__global__ void __launch_bounds__(256) mla_softmax_kernel(const MlaArgs a) {
-  const int row = static_cast<int>(blockIdx.x);   // t * 128 + h
+// One warp per (token, head) row, eight rows per block: M and L from the
+// tile statistics (warp reductions), then P = P_tile * 2^(m_tile - M) / L
+// in place (bf16), eight keys per lane and step, and the lse.
+__global__ void __launch_bounds__(256) mla_softmax_kernel(const MlaArgs a, int nrows) {
+  const int lane = threadIdx.x & 31;
+  const int row = static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5);   // t * 128 + h
+  if (row >= nrows) return;
   const int ntile = a.Sp / 128;
   const float* st = a.stats + static_cast<size_t>(row) * ntile * 2;
   float M = -INFINITY;
-  for (int i = 0; i < ntile; ++i) M = fmaxf(M, st[2 * i]);
+  for (int i = lane; i < ntile; i += 32) M = fmaxf(M, st[2 * i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f;
   if (M > -INFINITY)
-    for (int i = 0; i < ntile; ++i)
+    for (int i = lane; i < ntile; i += 32)
       if (st[2 * i] > -INFINITY) L += st[2 * i + 1] * exp2f(st[2 * i] - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  const float nm = M > -INFINITY ? -M : 0.f;
-  const float* x = a.sx + static_cast<size_t>(row) * a.Sp;
   uint16_t* pr = a.p + static_cast<size_t>(row) * a.Sp;
-  for (int j = 8 * threadIdx.x; j < a.Sp; j += 8 * blockDim.x) {
-    const float4 x0 = *reinterpret_cast<const float4*>(x + j);
-    const float4 x1 = *reinterpret_cast<const float4*>(x + j + 4);
-    const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-    uint32_t w[4];
+  for (int j = 8 * lane; j < a.Sp; j += 256) {
+    const float mt = st[2 * (j / 128)];
+    const float f = mt > -INFINITY ? exp2f(mt - M) * inv : 0.f;
+    uint4 w = *reinterpret_cast<const uint4*>(pr + j);
+    uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 b2 = __floats2bfloat162_rn(fast_exp2(v[2 * i] + nm) * inv,
-                                                      fast_exp2(v[2 * i + 1] + nm) * inv);
-      w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[i]));
+      const __nv_bfloat162 o = __floats2bfloat162_rn(x.x * f, x.y * f);
+      ww[i] = *reinterpret_cast<const uint32_t*>(&o);
     }
-    *reinterpret_cast<uint4*>(pr + j) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(pr + j) = w;
   }
   const int t = row / kQN, h = row % kQN;
-  if (threadIdx.x == 0 && a.lse != nullptr && h < a.QN)
+  if (lane == 0 && a.lse != nullptr && h < a.QN)
     a.lse[static_cast<size_t>(t) * a.QN + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
@@ -563,15 +574,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct MlaLayout {
-  size_t rows, sx, stats, p, total;
+  size_t rows, stats, p, total;
 };
 
 MlaLayout mla_layout(int T, int Sp) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   MlaLayout l;
   l.rows = 0;
-  l.sx = up(static_cast<size_t>(T) * Sp * 4);
-  l.stats = l.sx + up(static_cast<size_t>(T) * kQN * Sp * 4);
+  l.stats = up(static_cast<size_t>(T) * Sp * 4);
   l.p = l.stats + up(static_cast<size_t>(T) * kQN * (Sp / 128) * 8);
   l.total = l.p + up(static_cast<size_t>(T) * kQN * Sp * 2);
   return l;
@@ -608,7 +618,6 @@ cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int
   a.idx = p.sparse_indices;
   a.pool = static_cast<const uint8_t*>(p.kv_pool);
   a.rows = reinterpret_cast<int32_t*>(ws + lay.rows);
-  a.sx = reinterpret_cast<float*>(ws + lay.sx);
   a.stats = reinterpret_cast<float*>(ws + lay.stats);
   a.p = reinterpret_cast<uint16_t*>(ws + lay.p);
   a.o = static_cast<uint16_t*>(p.o);
@@ -637,7 +646,7 @@ cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int
   mla_qk_kernel<<<T * ngroups, kThreads, kQkSmem, stream>>>(qm, a, ngroups);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mla_softmax_kernel<<<T * kQN, 256, 0, stream>>>(a);
+  mla_softmax_kernel<<<(T * kQN + 7) / 8, 256, 0, stream>>>(a, T * kQN);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(mla_pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvSmem);
