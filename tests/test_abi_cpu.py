@@ -238,7 +238,7 @@ def test_prefill_rejects_before_launch(qlib):
 def test_mla_rejects_before_launch(qlib):
     q, lib = qlib
     assert lib.qpkv_mla_sparse_decode(None, None) == 1
-    assert lib.qpkv_mla_workspace_bytes(32, 2048) >= 32 * 128 * 2048 * 6
+    assert lib.qpkv_mla_workspace_bytes(32, 2048) >= 32 * 128 * 2048 * 2 + 32 * 2048 * 4
     assert lib.qpkv_mla_workspace_bytes(-1, 2048) == 0
     p = q.MlaParams()
     fake = 0x100000
