@@ -94,7 +94,14 @@ class ClockSampler:
     def summary(self, t0, t1):
         rows = [r for t, r in self.rows if len(r) >= 9]
         inside = [r for t, r in self.rows if t0 <= t <= t1 and len(r) >= 9]
+        window = "timed region"
+        if not inside:   # region shorter than the sampling interval: nearest samples
+            inside = [r for t, r in self.rows if t0 - 0.2 <= t <= t1 + 0.2 and len(r) >= 9]
+            window = "timed region +- 200 ms"
         use = inside if inside else rows
+        if not inside:
+            window = "whole run"
+        n_inside = len([1 for t, r in self.rows if t0 <= t <= t1 and len(r) >= 9])
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
 
@@ -112,7 +119,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": num(use[0][2]), "reasons": sorted(reasons),
-                "samples": len(use), "samples_in_timed_region": len(inside),
+                "samples": len(use), "samples_in_timed_region": n_inside, "window": window,
                 "power_w_max": max((num(r[3]) or 0.0) for r in use)}
 
 
@@ -620,7 +627,7 @@ def main():
         return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["qpkv", "reference"], default="qpkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
