@@ -336,7 +336,7 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
  * = cu_kv[b] - cu_kv[b-1]; block_table, seqlens_kv, page_size and
  * num_pages are not used (block_table and seqlens_kv may be NULL).
  * Supported: head_dim 128, page_size a multiple of 16 that divides 128 or
- * is a multiple of 128, Hq % Hkv == 0.  q, k_pool, v_pool, o 16-byte
+ * is a multiple of 128 up to 16384, Hq <= 32768, Hq % Hkv == 0.  q, k_pool, v_pool, o 16-byte
  * aligned.  sm_scale <= 0 selects 1/sqrt(128).
  * Errors: INVALID_ARG (null required pointer, negative or zero sizes,
  * misaligned pointer), UNSUPPORTED (head_dim, page_size, head grouping),

@@ -422,7 +422,9 @@ qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* p, void* stream) {
     return QPKV_ERR_INVALID_ARG;
   const int ps = p->page_size;
   if (p->head_dim != 128 || p->num_heads_q % p->num_heads_kv != 0) return QPKV_ERR_UNSUPPORTED;
-  if (!ragged && (ps % 16 != 0 || (128 % ps != 0 && ps % 128 != 0))) return QPKV_ERR_UNSUPPORTED;
+  if (!ragged && (ps % 16 != 0 || (128 % ps != 0 && ps % 128 != 0) || ps > 16384))
+    return QPKV_ERR_UNSUPPORTED;
+  if (p->num_heads_q > 32768) return QPKV_ERR_UNSUPPORTED;
   if (p->num_seqs == 0 || p->num_tokens == 0) return QPKV_OK;
   if (p->cu_seqlens_q == nullptr || p->q == nullptr || p->q_block_scale == nullptr ||
       p->k_block_scale == nullptr || p->o == nullptr || p->workspace == nullptr)

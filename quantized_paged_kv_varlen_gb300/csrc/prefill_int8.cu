@@ -75,6 +75,14 @@ struct PArgs {
   int B, T, Hq, Hkv, G, ps, P, bt_stride, NB, causal;
   int ragged, T_kv;     // ragged K/V: rows [T_kv, Hkv, D] addressed from the unit record
   int rows_box, nbox;   // page rows per TMA box, boxes per 128-key tile
+  // key tile j, box i -> block_table entry and row offset in the page, with
+  // no division on the device (an integer division by a runtime value runs
+  // through the MUFU pipe, which the softmax keeps busy):
+  //   page_size <= 128: entry j * nbox + i, offset 0;
+  //   page_size = 128 m, m > 1: entry j / m = umulhi(j, m_magic), offset
+  //   (j - entry * m) * 128, m_magic = ceil(2^32 / m) (exact while j * m < 2^32)
+  int m;
+  unsigned m_magic;
   float scale_log2;     // softmax scale * log2(e)
   const int32_t* cu_q;  // [B] inclusive prefix sums
   const int32_t* lk;    // [B]
@@ -102,6 +110,7 @@ struct Shared {
   float pair[2][kT];      // [column half][row]: a row's partial maxima / sums
   uint32_t tmem_base;
   int abort;
+  int kring[6], vring[6];   // IdRing slots of the K and V copy issuers
 };
 
 // Bounded mbarrier wait: the first probe is inline, the polling loop is one
@@ -171,15 +180,15 @@ __device__ __forceinline__ void q_tile_range(int Lq, int Lk, int causal, int& qt
 }
 
 struct Tile {
-  int b, h, qt, begin, Lq, Lk, nkv;
+  int b, h, hk, qt, begin, Lq, Lk, nkv;   // hk = h / (Hq / Hkv)
   int kvb;   // ragged K/V: the sequence's first row
 };
 
 // Workspace: int32 [0] unit count, [1, 1 + 4B) the sequences in cost order
 // (kWs* fields), [1 + 4B, 1 + 5B) their costs; from byte offset
 // units_offset(B) one 32-byte record per unit in that order:
-//   {b, h, qt_a, qt_b (-1 when the unit has one q tile), begin, Lq, Lk,
-//    first K/V row (ragged K/V; 0 for a paged cache)}.
+//   {b, h | kv head << 16, qt_a, qt_b (-1 when the unit has one q tile),
+//    begin, Lq, Lk, first K/V row (ragged K/V; 0 for a paged cache)}.
 __host__ __device__ __forceinline__ size_t units_offset(int B) {
   return ((static_cast<size_t>(1 + (kWsStride + 1) * static_cast<size_t>(B)) * 4 + 15) / 16) * 16;
 }
@@ -208,7 +217,8 @@ struct Items {
   __device__ __forceinline__ bool valid() const { return unit < total; }
   __device__ __forceinline__ void get(const PArgs& a, Tile& t) const {
     t.b = r0.x;
-    t.h = r0.y;
+    t.h = r0.y & 0xFFFF;
+    t.hk = r0.y >> 16;
     t.qt = second ? r0.w : r0.z;
     t.begin = r1.x;
     t.Lq = r1.y;
@@ -274,26 +284,42 @@ __device__ __forceinline__ void convert_half(const uint8_t* src, uint8_t* dst, i
   }
 }
 
-// The block_table entries of a key tile's TMA boxes (at most 8), loaded
-// together one tile before they are needed and kept in registers (the
-// loads complete in the background); kNoKey marks a box past L_kv.
-constexpr int kNoKey = -2147483647 - 1;
-struct BoxIds {
-  int i0, i1, i2, i3, i4, i5, i6, i7;
-  __device__ __forceinline__ void load(const PArgs& a, const Tile& t, int j) {
-    if (a.ragged) return;   // rows follow from the sequence's first row
-    const int32_t* row = a.bt + static_cast<size_t>(t.b) * a.bt_stride;
-    const int k0 = j * kT;
-    auto one = [&](int i) -> int {
-      const int key0 = k0 + i * a.rows_box;
-      return (i < a.nbox && key0 < t.Lk) ? __ldg(row + key0 / a.ps) : kNoKey;
-    };
-    i0 = one(0); i1 = one(1); i2 = one(2); i3 = one(3);
-    i4 = one(4); i5 = one(5); i6 = one(6); i7 = one(7);
+// Page ids of the first two TMA boxes of key tiles j, j + 1, j + 2 of one
+// walk, in a 3-slot shared-memory ring filled by 4-byte cp.async copies two
+// tiles before the tile is issued, so issuing a copy never waits on a
+// block_table load.  One walk per issuing thread; each fetch() closes one
+// cp.async group, and a fetch is issued for every position after the first
+// two of a work item, so when position j is issued only the group of j + 1
+// can still be in flight.  Boxes 2..7 (pages shorter than 64 rows) are read
+// directly when the tile is issued.
+__device__ __forceinline__ int bt_entry(const PArgs& a, int j, int i) {
+  return a.m == 1 ? j * a.nbox + i : static_cast<int>(__umulhi(static_cast<unsigned>(j), a.m_magic));
+}
+__device__ __forceinline__ int page_offset(const PArgs& a, int j, int e) {
+  return a.m == 1 ? 0 : (j - e * a.m) * kT;
+}
+
+struct IdRing {
+  int* slot;   // shared [3][2]
+  __device__ __forceinline__ void fetch(const PArgs& a, const Tile& t, int j) const {
+    if (!a.ragged && j < t.nkv) {
+      const int32_t* row = a.bt + static_cast<size_t>(t.b) * a.bt_stride;
+      const int nb = a.nbox < 2 ? a.nbox : 2;
+      for (int i = 0; i < nb; ++i) {
+        const int key0 = j * kT + i * a.rows_box;
+        if (key0 < t.Lk) cp_async_4(slot + 2 * (j % 3) + i, row + bt_entry(a, j, i));
+      }
+    }
+    cp_async_commit();
   }
-  __device__ __forceinline__ int get(int i) const {
-    return i == 0 ? i0 : i == 1 ? i1 : i == 2 ? i2 : i == 3 ? i3
-         : i == 4 ? i4 : i == 5 ? i5 : i == 6 ? i6 : i7;
+  // the walk moved to position j of its current item (j == first: just opened)
+  __device__ __forceinline__ void advanced(const PArgs& a, const Tile& t, int j, int first) const {
+    if (j == first) {
+      fetch(a, t, 0);
+      fetch(a, t, 1);
+    } else if (j >= 1) {
+      fetch(a, t, j + 1);
+    }
   }
 };
 
@@ -367,18 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pool row of box i of key tile j; keys past L_kv and bad page ids read
   // rows past the pool's end, which the copy fills with zeros
   const int oob = a.ragged ? a.T_kv : a.P * a.ps;
-  auto page_row = [&](const Tile& t, const BoxIds& ids, int i, int j) -> int {
-    if (a.ragged) {
-      const int key0 = j * kT + i * a.rows_box;
-      return key0 < t.Lk ? t.kvb + key0 : oob;
-    }
-    const int id = ids.get(i);
-    if (id == kNoKey) return oob;
-    if (id < 0 || id >= a.P) {
-      report_error(a.err, kDevErrBadPage);
-      return oob;
-    }
-    return id * a.ps + (j * kT + i * a.rows_box) % a.ps;
+  // (paged: after cp_async_wait_but_one(), the ring holds tile j's ids)
+  auto page_row = [&](const Tile& t, const int* ring, int i, int j) -> int {
+    const int key0 = j * kT + i * a.rows_box;
+    if (key0 >= t.Lk) return oob;
+    if (a.ragged) return t.kvb + key0;
+    const int e = bt_entry(a, j, i);
+    const int id = i < 2 ? ring[2 * (j % 3) + i]
+                         : __ldg(a.bt + static_cast<size_t>(t.b) * a.bt_stride + e);
+    // an entry outside the pool reads zeros (the prep pass flags it)
+    if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.P)) return oob;
+    return id * a.ps + page_offset(a, j, e);
   };
 
   if (warp == kWarpLoad || warp == kWarpConv) {
@@ -391,14 +416,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = warp == kWarpLoad ? 0 : 1;
     const bool issuer = part == 0 && lane == 0;
     TileWalk cv, ld;
-    BoxIds ids;
+    const IdRing kr{sh.kring};
     cv.start(a, true);
     int kpos = 0, ipos = 0, c16 = 0;
     if (issuer) {
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&k_map);
       ld.start(a, true);
-      if (ld.live && ld.j >= 0) ids.load(a, ld.t, ld.j);
+      if (ld.live) kr.advanced(a, ld.t, ld.j, -1);
     }
     auto issue = [&](int upto) -> bool {
       while (ld.live && ipos <= upto) {
@@ -410,14 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ld.j < 0) {
           tma_load_3d(dst, &q_map, &sh.k8_full[s], 0, t.h, t.begin + t.qt * kT);
         } else {
+          cp_async_wait_but_one();
 #pragma unroll 1
           for (int i = 0; i < a.nbox; ++i)
-            tma_load_3d(dst + i * a.rows_box * 128, &k_map, &sh.k8_full[s], 0, t.h / a.G,
-                        page_row(ld.t, ids, i, ld.j));
+            tma_load_3d(dst + i * a.rows_box * 128, &k_map, &sh.k8_full[s], 0, t.hk,
+                        page_row(ld.t, sh.kring, i, ld.j));
         }
         ++ipos;
         ld.next(a);
-        if (ld.live && ld.j >= 0) ids.load(a, ld.t, ld.j);
+        if (ld.live) kr.advanced(a, ld.t, ld.j, -1);
       }
       return true;
     };
@@ -447,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (issuer) {
+      cp_async_wait_all();
       for (int i = ipos > kK8Stages ? ipos - kK8Stages : 0; i < ipos; ++i)
         drain(&sh.k8_full[i % kK8Stages], (i / kK8Stages) & 1, a.err);
     }
@@ -507,12 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     Items it;
     it.start(a);
     TileWalk vw;
-    BoxIds vids;
+    const IdRing vr{sh.vring};
     int vpos = 0, pvc = 0, vis = 0;
     if (lane == 0) {
       tma_prefetch_desc(&v_map);
       vw.start(a, false);
-      if (vw.live) vids.load(a, vw.t, vw.j);
+      if (vw.live) vr.advanced(a, vw.t, vw.j, 0);
     }
     // lane 0: issue the V copies of tiles up to `upto`, waiting for a free
     // stage only when `block`; false on abort
@@ -527,16 +554,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&sh.v_full[s], kH16Tile);
         const Tile& t = vw.t;
+        cp_async_wait_but_one();
 #pragma unroll 1
         for (int i = 0; i < a.nbox; ++i) {
-          const int row = page_row(vw.t, vids, i, vw.j);
+          const int row = page_row(vw.t, sh.vring, i, vw.j);
           uint8_t* dst = smem + kOffV + s * kH16Tile + i * a.rows_box * 128;
-          tma_load_3d(dst, &v_map, &sh.v_full[s], 0, t.h / a.G, row);
-          tma_load_3d(dst + kHalf, &v_map, &sh.v_full[s], 64, t.h / a.G, row);
+          tma_load_3d(dst, &v_map, &sh.v_full[s], 0, t.hk, row);
+          tma_load_3d(dst + kHalf, &v_map, &sh.v_full[s], 64, t.hk, row);
         }
         ++vis;
         vw.next(a);
-        if (vw.live) vids.load(a, vw.t, vw.j);
+        if (vw.live) vr.advanced(a, vw.t, vw.j, 0);
       }
       return true;
     };
@@ -606,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // copy lands before the CTA exits
       tc_commit(&sh.mma_done[1]);
       drain(&sh.mma_done[1], 0, a.err);
+      cp_async_wait_all();
       for (int i = vis > kVStages ? vis - kVStages : 0; i < vis; ++i)
         drain(&sh.v_full[i % kVStages], (i / kVStages) & 1, a.err);
     }
@@ -657,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Tile t;
       it.get(a, t);
       it.advance();
-      const int hk = t.h / a.G;
+      const int hk = t.hk;
       const float base =
           a.scale_log2 * __ldg(a.sq + (static_cast<size_t>(t.b) * a.NB + t.qt) * a.Hq + t.h);
       const float* skp = a.sk + static_cast<size_t>(t.b) * a.NB * a.Hkv + hk;
@@ -811,8 +840,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct PrepArgs {
-  int B, T, Hq, NB, causal, ps, bt_stride;
+  int B, T, Hq, G, NB, causal, ps, bt_stride, P;
   int ragged, T_kv;
+  const int32_t* bt;
   const int32_t* cu_q;
   const int32_t* lk;
   const int32_t* cu_kv;   // ragged K/V: inclusive prefix sums of L_kv
@@ -843,7 +873,9 @@ __device__ __forceinline__ bool seq_info(const PrepArgs& p, int b, int& begin, i
 }
 
 // Block 0: unit table in cost order.  Every block: O = 0, lse = -inf on
-// the rows of q tiles that see no key (and of sequences rejected above).
+// the rows of q tiles that see no key (and of sequences rejected above);
+// block_table entries of the pages holding keys [0, L_kv) outside the pool
+// are flagged here, once, rather than where the copies are issued.
 __global__ void __launch_bounds__(256) prefill_prep_kernel(const PrepArgs p) {
   if (blockIdx.x == 0) {
     int32_t* cost = p.ws + 1 + kWsStride * p.B;
@@ -886,6 +918,13 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const PrepArgs p) {
     const bool ok = seq_info(p, b, begin, Lq, Lk, qt_lo, nqv);
     int rows = ok ? min(Lq, qt_lo * kT) : 0;
     if (!ok && begin >= 0 && Lq > 0 && begin + Lq <= p.T) rows = Lq;
+    if (ok && !p.ragged) {
+      const int npg = (Lk + p.ps - 1) / p.ps;
+      const int32_t* row = p.bt + static_cast<size_t>(b) * p.bt_stride;
+      for (int e = threadIdx.x; e < npg; e += blockDim.x)
+        if (static_cast<unsigned>(row[e]) >= static_cast<unsigned>(p.P))
+          report_error(p.err, kDevErrBadPage);
+    }
     const int chunks = rows * p.Hq * (kD / 8);
     for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
       const int c = i % (kD / 8), rh = i / (kD / 8);
@@ -916,7 +955,9 @@ __global__ void __launch_bounds__(256) prefill_units_kernel(const PrepArgs p) {
   const int kvb = p.ragged ? (b > 0 ? p.cu_kv[b - 1] : 0) : 0;
   const int Lk = p.ragged ? p.cu_kv[b] - kvb : p.lk[b];
   int4* rec = reinterpret_cast<int4*>(reinterpret_cast<uint8_t*>(p.ws) + units_offset(p.B)) + 2 * u;
-  rec[0] = make_int4(b, local / pairs, qt_lo + tt, nqv - 1 - tt != tt ? qt_lo + nqv - 1 - tt : -1);
+  const int h = local / pairs;
+  rec[0] = make_int4(b, h | ((h / p.G) << 16), qt_lo + tt,
+                     nqv - 1 - tt != tt ? qt_lo + nqv - 1 - tt : -1);
   rec[1] = make_int4(begin, p.cu_q[b] - begin, Lk, kvb);
 }
 
@@ -946,6 +987,9 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   pa.B = p.num_seqs;
   pa.T = p.num_tokens;
   pa.Hq = p.num_heads_q;
+  pa.G = p.num_heads_q / p.num_heads_kv;
+  pa.P = p.num_pages;
+  pa.bt = p.block_table;
   pa.NB = p.num_blocks;
   pa.causal = p.causal ? 1 : 0;
   pa.ps = ps;
@@ -1004,6 +1048,8 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   a.T_kv = p.num_kv_tokens;
   a.rows_box = rows_box;
   a.nbox = kT / rows_box;
+  a.m = ps > kT ? ps / kT : 1;
+  a.m_magic = a.m > 1 ? static_cast<unsigned>(((1ull << 32) + a.m - 1) / a.m) : 0u;
   a.scale_log2 = (p.sm_scale > 0.f ? p.sm_scale : 1.0f / sqrtf(static_cast<float>(kD))) * kLog2e;
   a.cu_q = p.cu_seqlens_q;
   a.lk = p.seqlens_kv;

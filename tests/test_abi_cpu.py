@@ -215,10 +215,13 @@ def test_prefill_rejects_before_launch(qlib):
     p.head_dim = 64
     assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
     p.head_dim = 128
-    for ps in (24, 48, 192):       # not a multiple of 16 dividing 128 or of 128
+    for ps in (24, 48, 192, 32768):   # not a multiple of 16 dividing 128 or of 128, or too long
         p.page_size = ps
         assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
     p.page_size = 64
+    p.num_heads_q = 65536          # the head index is packed into 16 bits
+    assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
+    p.num_heads_q = 4
     p.num_heads_kv = 3             # 4 q heads do not group over 3 kv heads
     assert lib.qpkv_prefill_paged(ctypes.byref(p), None) == 2
     p.num_heads_kv = 2

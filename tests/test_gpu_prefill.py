@@ -129,6 +129,7 @@ def _oracle(c, causal, scale=1.0 / np.sqrt(128.0), rows=None):
     ([300, 50], [40, 0], 2, 2, 64, True),                  # L_q > L_kv: leading rows see nothing
     ([130, 257], [390, 100], 2, 1, 128, False),            # no mask
     ([600], [600], 2, 2, 256, True),                       # pages longer than a tile
+    ([900, 300], [1000, 300], 4, 2, 384, True),            # three tiles per page
     ([640, 520], [640, 520], 1, 1, 64, True),              # several q tiles: pairs (0,4) (1,3) (2)
 ])
 def test_prefill_shapes(lib, Lq, Lk, Hq, Hkv, ps, causal):
