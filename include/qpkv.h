@@ -104,6 +104,14 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
  *     bytes [0, 512) INT8 nope codes (tile i = dims 128i..128i+127 has scale
  *     absmax/127), [512, 640) the bf16 rope values, [640, 656) the 4 fp32
  *     tile scales, little-endian ("512+64*2+4*4", README row key).
+ *     With rope_cos / rope_sin (float [rope_max_pos, 32], from
+ *     qpkv_rope_table with rot_dim 64) the rope part is first rotated
+ *     (rotate-half, pairs (i, i + 32)) at the token's position and the
+ *     float32 result rounded to bf16 (nearest-even); a position outside the
+ *     tables leaves the row unwritten and sets QPKV_DEV_ERR_BAD_LENGTH.
+ *     With q (bf16 [T, Hq, 576], Hq = num_heads_q) the query rows are written
+ *     to q_out (bf16, same shape; may alias q) with their rope part rotated
+ *     the same way and the nope part copied; q requires the tables.
  *
  * Device arrays: cu_seqlens_q int32 [B] inclusive prefix sums (batch b spans
  * [cu[b-1], cu[b]), cu[-1] = 0); start_pos int32 [B] or NULL (all zero);
@@ -130,21 +138,21 @@ typedef struct qpkv_write_params {
   int32_t num_pages;      /* P, pool size, for page-id checks */
   int32_t bt_stride;      /* row stride of block_table */
   int32_t num_blocks;     /* INT8 mode: dim 1 of the block-scale arrays */
-  int32_t rope_max_pos;   /* rows of the RoPE tables (INT8 mode) */
+  int32_t rope_max_pos;   /* rows of the RoPE tables (INT8 and MLA modes) */
   const int32_t* cu_seqlens_q;
   const int32_t* start_pos;
   const int32_t* block_table;
-  const void* q;          /* bf16 [T, Hq, D] (INT8 mode) */
+  const void* q;          /* bf16 [T, Hq, D] (INT8 mode; MLA: [T, Hq, 576] or NULL) */
   const void* k;          /* bf16 [T, Hkv, D] ([T, 576] for MLA) */
   const void* v;          /* bf16 [T, Hkv, D] (not used for MLA) */
-  const float* rope_cos;  /* [rope_max_pos, D/2] (INT8 mode) */
+  const float* rope_cos;  /* [rope_max_pos, D/2] (INT8 mode; MLA: [rope_max_pos, 32] or NULL) */
   const float* rope_sin;
   void* k_pool;           /* u8 E4M3 / int8 / MLA rows */
   void* v_pool;           /* u8 E4M3 (FP8 mode) / bf16 (INT8 mode) */
   float* k_scale_pool;    /* FP8 mode [P, page_size, Hkv] */
   float* v_scale_pool;
   float* k_block_scale;   /* INT8 mode [B, num_blocks, Hkv] */
-  void* q_out;            /* INT8 mode: int8 [T, Hq, D] */
+  void* q_out;            /* INT8 mode: int8 [T, Hq, D]; MLA: bf16 [T, Hq, 576] */
   float* q_block_scale;   /* INT8 mode [B, num_blocks, Hq] */
   int32_t* slot_mapping;  /* [T] or NULL */
   int32_t* error_word;    /* device int32 or NULL */
@@ -404,7 +412,12 @@ qpkv_status qpkv_csr_to_block_table(const int32_t* indptr, const int32_t* indice
  *   keys are the entries of sparse_indices[t, 0, :] before the first -1,
  *   logical token positions of sequence b mapped through block_table
  *   (pool row block_table[b][id / block_size] * block_size + id % block_size);
- *   sparse_mode 3 also drops ids above i + L_kv - L_q.  A cache row is 656
+ *   sparse_mode 3 also drops ids above i + L_kv - L_q.  With
+ *   sparse_block_size n > 1 (block-wise sparsity, README row
+ *   sparse_block_size) an entry id names the n tokens [id * n, id * n + n)
+ *   of the sequence, which share the decision; tokens of the block at or
+ *   past L_kv are not keys, and an id with id * n >= L_kv is out of range.
+ *   A cache row is 656
  *   bytes: 512 INT8 nope codes, 64 bf16 rope values, 4 fp32 scales (nope
  *   tile k = dims 128k..128k+127), the layout QPKV_WRITE_MLA_ROW writes.
  *   K = [code * scale || rope] (576), V = code * scale (512);
@@ -417,11 +430,13 @@ qpkv_status qpkv_csr_to_block_table(const int32_t* indptr, const int32_t* indice
  * sparse_indices int32 [T, 1, sparse_size]; block_table int32 [B,
  * bt_stride]; seqlens_kv int32 [B]; cu_seqlens_q int32 [B] inclusive prefix
  * sums; o bf16 [T, Hq, 512]; lse fp32 [T, Hq] or NULL; workspace of
- * qpkv_mla_workspace_bytes(T, sparse_size) bytes (overwritten).
+ * qpkv_mla_workspace_bytes(T, sparse_size * sparse_block_size) bytes
+ * (overwritten).
  * error_word bits: QPKV_DEV_ERR_BAD_INDEX (an id outside [0, L_kv) before
  * the first -1, skipped), QPKV_DEV_ERR_BAD_PAGE, QPKV_DEV_ERR_TIMEOUT.
  * Supported: 1 <= Hq <= 128, head_dim_qk 576, head_dim_v 512, sparse_mode
- * 0 or 3, sparse_block_size 1.  q, kv_pool, o, workspace 16-byte aligned.
+ * 0 or 3, 1 <= sparse_block_size <= 128 (0 reads as 1), sparse_size *
+ * sparse_block_size <= 2^24.  q, kv_pool, o, workspace 16-byte aligned.
  * scale <= 0 selects 1/sqrt(576).
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA. */
 typedef struct qpkv_mla_params {
@@ -436,7 +451,7 @@ typedef struct qpkv_mla_params {
   int32_t sparse_size;   /* entries per sparse_indices row */
   int32_t sparse_mode;   /* 0 or 3 */
   float scale;
-  int32_t pad0;
+  int32_t sparse_block_size;   /* tokens per listed id: 1 (token-wise) .. 128; 0 = 1 */
   const int32_t* cu_seqlens_q;
   const int32_t* seqlens_kv;
   const int32_t* block_table;

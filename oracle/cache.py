@@ -22,7 +22,9 @@ Three modes:
   mla_row          one 656-byte row per token: 512 INT8 nope codes with one
                    fp32 scale per 128-wide tile, the 64-wide rope part as
                    bf16, then the 4 scales (README, 参数说明 row key:
-                   "512+64*2+4*4").
+                   "512+64*2+4*4").  Optionally the rope part (and the
+                   query's) is rotated first: rotate-half over its 64 dims,
+                   the float32 result rounded to bf16 to nearest-even.
 """
 import numpy as np
 
@@ -65,6 +67,17 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     if np.any(u & 0xFFFF):
         raise ValueError("values are not exactly representable in bf16")
     return (u >> 16).astype(np.uint16)
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bf16 (ties to even), returned
+    as float32; NaN stays NaN, infinities stay infinite."""
+    u = np.asarray(x, dtype=F32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    nan = np.isnan(np.asarray(x, dtype=F32))
+    r = np.where(nan, (u | 0x400000) >> 16 << 16, r)
+    return r.astype(np.uint32).view(F32)
 
 
 def bf16_value(bits: np.ndarray) -> np.ndarray:
@@ -190,8 +203,23 @@ def mla_unpack_rows(rows):
     return k, nope
 
 
-def write_mla_rows(kv, cu_seqlens_q, start_pos, block_table, page_size, pool):
-    """MLA combined-row write of [T, 576] tokens into pool [P, bs, 1, 656]."""
+def mla_rope(x, cu_seqlens_q, start_pos, cos, sin):
+    """Rotate the 64-wide rope part (last 64 of 576 dims) of every row of
+    x float32 [T, 576] or [T, N, 576] at its token's position; the rotated
+    values are rounded to bf16.  cos/sin: float32 [max_pos, 32]."""
+    x = np.array(x, dtype=F32)
+    _, p_of = token_positions(cu_seqlens_q, start_pos)
+    rot = rope.rotate(x[..., MLA_NOPE:], p_of, cos, sin)
+    x[..., MLA_NOPE:] = bf16_round(rot)
+    return x
+
+
+def write_mla_rows(kv, cu_seqlens_q, start_pos, block_table, page_size, pool,
+                   cos=None, sin=None):
+    """MLA combined-row write of [T, 576] tokens into pool [P, bs, 1, 656];
+    with cos/sin the rope part is rotated first (mla_rope)."""
+    if cos is not None:
+        kv = mla_rope(kv, cu_seqlens_q, start_pos, cos, sin)
     slots = slot_mapping(cu_seqlens_q, start_pos, block_table, page_size)
     P, bs, one, W = pool.shape
     pool = pool.copy().reshape(P * bs, W)

@@ -16,7 +16,10 @@ sparse_mode, and the formula under 计算公式:
   dequantised nope (512 wide), so the output is [T, Q_N, 512];
 * sparse_indices [T, 1, sparse_size] lists logical token positions of the
   request (mapped through block_table); valid entries come first, the first
-  -1 ends the list; sparse_block_size = 1 (token-wise);
+  -1 ends the list; with sparse_block_size n > 1 (row sparse_block_size,
+  block-wise sparsity) an entry names the n tokens [id*n, id*n + n) of the
+  request, which share the decision, and the tokens at or past L_kv of the
+  last block are not keys;
 * sparse_mode 3 additionally drops ids outside the right-down causal region.
 """
 import numpy as np
@@ -25,20 +28,23 @@ from . import cache
 from .attention import NEG_INF, attend_rows, page_rows
 
 
-def valid_ids(index_row, L_kv):
-    """Leading valid entries of one sparse_indices row (stop at the first -1)."""
+def valid_ids(index_row, L_kv, block=1):
+    """Token positions named by one sparse_indices row: its entries up to the
+    first -1, each covering `block` tokens (clipped to the sequence)."""
     ids = []
     for x in np.asarray(index_row).tolist():
         if x < 0:
             break
-        if x >= L_kv:
-            raise ValueError(f"sparse index {x} outside [0, {L_kv})")
-        ids.append(int(x))
+        if x * block >= L_kv:
+            raise ValueError(f"sparse index {x} outside the sequence (L = {L_kv})")
+        for o in range(block):
+            if x * block + o < L_kv:
+                ids.append(int(x) * block + o)
     return np.asarray(ids, dtype=np.int64)
 
 
 def mla_sparse_decode(q, kv_pool, sparse_indices, block_table, seqlens_kv,
-                      cu_seqlens_q, scale, sparse_mode=0, tokens=None):
+                      cu_seqlens_q, scale, sparse_mode=0, tokens=None, sparse_block_size=1):
     """q f32 [T, QN, 576] (bf16 values); kv_pool u8 [P, bs, 1, 656];
     sparse_indices int32 [T, 1, S]; returns (O f64[T, QN, 512], lse f64[T, QN]).
     ``tokens``: optional subset of query tokens to compute.
@@ -58,7 +64,7 @@ def mla_sparse_decode(q, kv_pool, sparse_indices, block_table, seqlens_kv,
             t = int(begin[b]) + i
             if t not in todo:
                 continue
-            ids = valid_ids(sparse_indices[t, 0], Lk)
+            ids = valid_ids(sparse_indices[t, 0], Lk, sparse_block_size)
             if sparse_mode == 3:
                 ids = ids[ids <= i + (Lk - Lq)]
             if ids.size == 0:

@@ -80,7 +80,7 @@ class MlaParams(ctypes.Structure):
     _fields_ = [(n, _i32) for n in (
         "num_seqs", "num_tokens", "num_heads_q", "head_dim_qk", "head_dim_v", "block_size",
         "num_blocks", "bt_stride", "sparse_size", "sparse_mode")] + [
-        ("scale", ctypes.c_float), ("pad0", _i32)] + [
+        ("scale", ctypes.c_float), ("sparse_block_size", _i32)] + [
         (n, _p) for n in (
             "cu_seqlens_q", "seqlens_kv", "block_table", "q", "kv_pool", "sparse_indices", "o",
             "lse", "workspace")] + [
@@ -260,8 +260,13 @@ def write_cache_int8_block128_rope(q, k, v, cu_seqlens, block_table, max_seqlen,
 
 
 def write_cache_mla(kv, cu_seqlens, block_table, pool, start_pos=None, slot_mapping=None,
-                    error_word=None):
-    """MLA combined-row write: kv bf16 [T, 576] -> pool u8 [P, bs, 1, 656]."""
+                    error_word=None, rope_cos=None, rope_sin=None, q=None, q_out=None):
+    """MLA combined-row write: kv bf16 [T, 576] -> pool u8 [P, bs, 1, 656].
+
+    With rope_cos / rope_sin (fp32 [max_pos, 32], ``rope_table(theta, max_pos,
+    64)``) the 64-wide rope part is rotated at each token's position first;
+    with q (bf16 [T, Hq, 576]) the rotated queries go to q_out (allocated
+    when None, may be q itself), which is returned."""
     torch = _torch()
     lib = load()
     _need(kv, "kv", torch.bfloat16, 2)
@@ -274,10 +279,29 @@ def write_cache_mla(kv, cu_seqlens, block_table, pool, start_pos=None, slot_mapp
     p.head_dim = 576
     p.k = _ptr(kv)
     p.k_pool = _ptr(pool)
+    if rope_cos is not None:
+        _need(rope_cos, "rope_cos", torch.float32, 2)
+        _need(rope_sin, "rope_sin", torch.float32, 2)
+        if rope_cos.shape[1] != 32 or tuple(rope_sin.shape) != tuple(rope_cos.shape):
+            raise ValueError("MLA RoPE tables must be [max_pos, 32]")
+        p.rope_max_pos = rope_cos.shape[0]
+        p.rope_cos, p.rope_sin = _ptr(rope_cos), _ptr(rope_sin)
+    if q is not None:
+        if rope_cos is None:
+            raise ValueError("rotating q needs the RoPE tables")
+        _need(q, "q", torch.bfloat16, 3)
+        if q.shape[0] != kv.shape[0] or q.shape[2] != 576:
+            raise ValueError("q must be [T, Hq, 576]")
+        if q_out is None:
+            q_out = torch.empty_like(q)
+        _need(q_out, "q_out", torch.bfloat16, 3)
+        p.num_heads_q = q.shape[1]
+        p.q, p.q_out = _ptr(q), _ptr(q_out)
     p.start_pos = _ptr(start_pos)
     p.slot_mapping = _ptr(slot_mapping)
     p.error_word = _ptr(error_word)
     _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(mla)")
+    return q_out
 
 
 class DecodePlan:
@@ -521,19 +545,21 @@ def csr_to_block_table(indptr, indices, last_page_len, page_size, bt_stride=None
     return bt, lens
 
 
-def mla_workspace(num_tokens, sparse_size, device="cuda"):
+def mla_workspace(num_tokens, sparse_size, device="cuda", sparse_block_size=1):
     """A device workspace large enough for ``mla_sparse_decode``."""
     torch = _torch()
-    n = int(load().qpkv_mla_workspace_bytes(int(num_tokens), int(sparse_size)))
+    n = int(load().qpkv_mla_workspace_bytes(int(num_tokens),
+                                            int(sparse_size) * max(1, int(sparse_block_size))))
     return torch.empty(((n + 15) // 16) * 16, dtype=torch.uint8, device=device)
 
 
 def mla_sparse_decode(q, kv_pool, sparse_indices, block_table, seqlens_kv, cu_seqlens_q,
                       scale=None, sparse_mode=0, out=None, lse=None, workspace=None,
-                      error_word=None):
+                      error_word=None, sparse_block_size=1):
     """MLA-absorb sparse decode: q bf16 [T, Hq, 576]; kv_pool u8 [P, bs, 1, 656];
-    sparse_indices int32 [T, 1, S]; returns bf16 O [T, Hq, 512] (``lse`` fp32
-    [T, Hq] filled when given)."""
+    sparse_indices int32 [T, 1, S] (token ids, or with sparse_block_size n > 1
+    ids of n-token blocks); returns bf16 O [T, Hq, 512] (``lse`` fp32 [T, Hq]
+    filled when given)."""
     torch = _torch()
     lib = load()
     _need(q, "q", torch.bfloat16, 3)
@@ -554,12 +580,13 @@ def mla_sparse_decode(q, kv_pool, sparse_indices, block_table, seqlens_kv, cu_se
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
     if workspace is None:
-        workspace = mla_workspace(T, S, q.device)
+        workspace = mla_workspace(T, S, q.device, sparse_block_size)
     prm = MlaParams()
     prm.num_seqs, prm.num_tokens, prm.num_heads_q = cu_seqlens_q.shape[0], T, Hq
     prm.head_dim_qk, prm.head_dim_v, prm.block_size, prm.num_blocks = 576, 512, bs, P
     prm.bt_stride, prm.sparse_size, prm.sparse_mode = block_table.shape[1], S, int(sparse_mode)
     prm.scale = float(scale) if scale else 0.0
+    prm.sparse_block_size = int(sparse_block_size)
     prm.cu_seqlens_q, prm.seqlens_kv, prm.block_table = (
         _ptr(cu_seqlens_q), _ptr(seqlens_kv), _ptr(block_table))
     prm.q, prm.kv_pool, prm.sparse_indices = _ptr(q), _ptr(kv_pool), _ptr(sparse_indices)

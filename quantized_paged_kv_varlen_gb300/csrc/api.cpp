@@ -242,6 +242,12 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
       break;
     case QPKV_WRITE_MLA_ROW:
       if (p->head_dim != 576 || p->num_heads_kv != 1) return QPKV_ERR_UNSUPPORTED;
+      if (p->rope_cos != nullptr && (p->rope_sin == nullptr || p->rope_max_pos < 1))
+        return QPKV_ERR_INVALID_ARG;
+      if (p->q != nullptr &&
+          (p->rope_cos == nullptr || p->q_out == nullptr || p->num_heads_q < 1 ||
+           !aligned16(p->q) || !aligned16(p->q_out)))
+        return QPKV_ERR_INVALID_ARG;
       break;
     default:
       return QPKV_ERR_UNSUPPORTED;
@@ -481,8 +487,12 @@ qpkv_status qpkv_mla_sparse_decode(const qpkv_mla_params* p, void* stream) {
       p->num_blocks <= 0 || p->bt_stride <= 0 || p->sparse_size <= 0)
     return QPKV_ERR_INVALID_ARG;
   if (p->head_dim_qk != 576 || p->head_dim_v != 512 || p->num_heads_q > 128 ||
-      (p->sparse_mode != 0 && p->sparse_mode != 3))
+      (p->sparse_mode != 0 && p->sparse_mode != 3) || p->sparse_block_size < 0 ||
+      p->sparse_block_size > 128)
     return QPKV_ERR_UNSUPPORTED;
+  const long long keys =
+      static_cast<long long>(p->sparse_size) * (p->sparse_block_size > 1 ? p->sparse_block_size : 1);
+  if (keys > (1ll << 24)) return QPKV_ERR_UNSUPPORTED;
   if (p->num_tokens == 0) return QPKV_OK;
   if (p->cu_seqlens_q == nullptr || p->seqlens_kv == nullptr || p->block_table == nullptr ||
       p->q == nullptr || p->kv_pool == nullptr || p->sparse_indices == nullptr || p->o == nullptr ||
@@ -490,7 +500,7 @@ qpkv_status qpkv_mla_sparse_decode(const qpkv_mla_params* p, void* stream) {
     return QPKV_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->kv_pool) || !aligned16(p->o) || !aligned16(p->workspace))
     return QPKV_ERR_INVALID_ARG;
-  if (p->workspace_bytes < mla_workspace_bytes(p->num_tokens, p->sparse_size))
+  if (p->workspace_bytes < mla_workspace_bytes(p->num_tokens, static_cast<int>(keys)))
     return QPKV_ERR_WORKSPACE_TOO_SMALL;
   int status = QPKV_OK;
   const cudaError_t e = launch_mla_sparse(*p, static_cast<cudaStream_t>(stream), &status);

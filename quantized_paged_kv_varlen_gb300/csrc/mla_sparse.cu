@@ -48,7 +48,8 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kConv0 = 2, kNConv = 8, kEpi0 = 10;
 constexpr int kConvThreads = kNConv * 32;
 
 struct MlaArgs {
-  int T, QN, Sp, S;         // tokens, q heads, padded and given sparse size
+  int T, QN, Sp, S;         // tokens, q heads, padded key count, sparse_indices row length
+  int sbs;                  // tokens per listed id (sparse_block_size)
   int bs, P, bt_stride, B, mode;
   float scale_log2;
   const int32_t* cu_q;
@@ -121,11 +122,13 @@ __device__ __forceinline__ void dequant16(const uint4& w, float s, uint4& p0, ui
 
 
 // ----------------------------------------------------------------- prep
-// Blocks (token, 256-entry slice): the first -1 of the token's list (found
-// by every block of the token) ends it; every listed id
-// becomes a pool row (or -1: past the list, outside [0, L_kv) - flagged -,
-// hidden by the right-down causal rule of sparse_mode 3, or on a page id
-// outside the pool - flagged).
+// Blocks (token, 256-key slice): the first -1 of the token's list (found
+// by every block of the token) ends it; key j is token id * sbs + j % sbs
+// of the listed id = list[j / sbs] (sbs = sparse_block_size, 1 for
+// token-wise lists) and becomes a pool row, or -1: past the list, a block
+// outside the sequence (flagged), a block token at or past L_kv, hidden by
+// the right-down causal rule of sparse_mode 3, or on a page id outside the
+// pool (flagged).
 __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
   const int t = static_cast<int>(blockIdx.x), j0 = static_cast<int>(blockIdx.y) * 256;
   __shared__ int first_neg;
@@ -148,17 +151,22 @@ __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
   int32_t* out = a.rows + static_cast<size_t>(t) * a.Sp;
   {
     const int j = j0 + static_cast<int>(threadIdx.x);
+    const int li = j / a.sbs;
     int r = -1;
-    if (has_seq && j < nv) {
-      const int id = ids[j];
-      if (id < 0 || id >= Lk || id / a.bs >= a.bt_stride) {
-        report_error(a.err, kDevErrBadIndex);
-      } else if (a.mode != 3 || id <= i + Lk - Lq) {
-        const int pg = a.bt[static_cast<size_t>(b) * a.bt_stride + id / a.bs];
+    if (has_seq && li < nv) {
+      const int id = ids[li];
+      const long long tok = static_cast<long long>(id) * a.sbs + (j - li * a.sbs);
+      const long long rows_bt = static_cast<long long>(a.bt_stride) * a.bs;
+      if (id < 0 || static_cast<long long>(id) * a.sbs >= Lk ||
+          static_cast<long long>(id) * a.sbs >= rows_bt) {
+        if (j == li * a.sbs) report_error(a.err, kDevErrBadIndex);
+      } else if (tok < Lk && tok < rows_bt && (a.mode != 3 || tok <= i + Lk - Lq)) {
+        const int kt = static_cast<int>(tok);
+        const int pg = a.bt[static_cast<size_t>(b) * a.bt_stride + kt / a.bs];
         if (pg < 0 || pg >= a.P)
           report_error(a.err, kDevErrBadPage);
         else
-          r = pg * a.bs + id % a.bs;
+          r = pg * a.bs + kt % a.bs;
       }
     }
     if (r >= 0) prefetch_row_l2(a.pool + static_cast<size_t>(r) * kRow);
@@ -598,7 +606,8 @@ size_t mla_workspace_bytes(int num_tokens, int sparse_size) {
 cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int* status) {
   *status = QPKV_OK;
   if (p.num_tokens == 0) return cudaSuccess;
-  const int T = p.num_tokens, Sp = padded_sparse(p.sparse_size);
+  const int sbs = p.sparse_block_size > 1 ? p.sparse_block_size : 1;
+  const int T = p.num_tokens, Sp = padded_sparse(p.sparse_size * sbs);
   const MlaLayout lay = mla_layout(T, Sp);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
   MlaArgs a;
@@ -606,6 +615,7 @@ cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int
   a.QN = p.num_heads_q;
   a.Sp = Sp;
   a.S = p.sparse_size;
+  a.sbs = sbs;
   a.bs = p.block_size;
   a.P = p.num_blocks;
   a.bt_stride = p.bt_stride;

@@ -224,19 +224,73 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
 
 // ------------------------------------------------------------ MLA rows
 // One warp per token: lane l quantises nope dims [16l, 16l + 16) (tile l / 8),
-// lanes 0..7 copy the 64 bf16 rope values, lanes 0/8/16/24 store the scales.
-constexpr int kMlaIn = 576, kMlaRow = 656;
+// lanes 0..7 copy the 64 bf16 rope values (with RoPE: lanes 0..3 rotate
+// the pairs (i, i + 32), i in [8l, 8l + 8)), lanes 0/8/16/24 store the scales.
+constexpr int kMlaIn = 576, kMlaRow = 656, kMlaRopeHalf = 32;
+
+// Rotate-half RoPE of one lane's 8 pairs of the 64-wide rope part: x holds
+// dims [8l, 8l + 8), y dims [32 + 8l, 32 + 8l + 8) as bf16; the float32
+// results (products and sums rounded separately) are rounded to bf16.
+__device__ __forceinline__ void mla_rope8(uint4& x, uint4& y, const float* __restrict__ cs,
+                                          const float* __restrict__ sn) {
+  float a[8], b[8];
+  const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x);
+  const uint32_t* yw = reinterpret_cast<const uint32_t*>(&y);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    a[2 * j] = bf16_bits_to_float(xw[j] & 0xFFFF);
+    a[2 * j + 1] = bf16_bits_to_float(xw[j] >> 16);
+    b[2 * j] = bf16_bits_to_float(yw[j] & 0xFFFF);
+    b[2 * j + 1] = bf16_bits_to_float(yw[j] >> 16);
+  }
+  uint32_t ox[4], oy[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float r1[2], r2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k = 2 * j + e;
+      const float c = __ldg(cs + k), s = __ldg(sn + k);
+      r1[e] = __fsub_rn(__fmul_rn(a[k], c), __fmul_rn(b[k], s));
+      r2[e] = __fadd_rn(__fmul_rn(b[k], c), __fmul_rn(a[k], s));
+    }
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(r1[0], r1[1]);
+    const __nv_bfloat162 p2 = __floats2bfloat162_rn(r2[0], r2[1]);
+    ox[j] = *reinterpret_cast<const uint32_t*>(&p1);
+    oy[j] = *reinterpret_cast<const uint32_t*>(&p2);
+  }
+  x = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+  y = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+}
+
+// Position of token t, or -1 (flagged) when it lies past the RoPE tables.
+__device__ __forceinline__ int mla_pos(const int32_t* __restrict__ cu,
+                                       const int32_t* __restrict__ start_pos, int B, int t,
+                                       int max_pos, int* err) {
+  const int b = seq_of_token(cu, B, t);
+  const int p = (start_pos ? __ldg(start_pos + b) : 0) + (t - seq_begin(cu, b));
+  if (p < 0 || p >= max_pos) {
+    report_error(err, kDevErrBadLength);
+    return -1;
+  }
+  return p;
+}
 
 __global__ void __launch_bounds__(256) write_mla_row_kernel(
     int T, int B, int ps, int num_pages, int bt_stride, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ bt,
-    const uint16_t* __restrict__ kv, uint8_t* __restrict__ pool, int32_t* __restrict__ slots,
-    int* err) {
+    const uint16_t* __restrict__ kv, const float* __restrict__ rope_cos,
+    const float* __restrict__ rope_sin, int rope_max_pos, uint8_t* __restrict__ pool,
+    int32_t* __restrict__ slots, int* err) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const int b = seq_of_token(cu, B, t);
   const int p = (start_pos ? __ldg(start_pos + b) : 0) + (t - seq_begin(cu, b));
+  if (rope_cos != nullptr && (p < 0 || p >= rope_max_pos)) {
+    if (lane == 0) report_error(err, kDevErrBadLength);
+    return;
+  }
   const int page = pool_page(bt, bt_stride, b, p, ps, num_pages, lane == 0 ? err : nullptr);
   if (page < 0) return;
   const size_t slot = static_cast<size_t>(page) * ps + (p % ps);
@@ -263,11 +317,53 @@ __global__ void __launch_bounds__(256) write_mla_row_kernel(
     }
   }
   *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-  if (lane < 8) {
-    *reinterpret_cast<uint4*>(row + 512 + lane * 16) =
-        *reinterpret_cast<const uint4*>(src + 512 + lane * 8);
+  if (rope_cos == nullptr) {
+    if (lane < 8) {
+      *reinterpret_cast<uint4*>(row + 512 + lane * 16) =
+          *reinterpret_cast<const uint4*>(src + 512 + lane * 8);
+    }
+  } else if (lane < 4) {
+    uint4 x = *reinterpret_cast<const uint4*>(src + 512 + lane * 8);
+    uint4 y = *reinterpret_cast<const uint4*>(src + 512 + kMlaRopeHalf + lane * 8);
+    const size_t tab = static_cast<size_t>(p) * kMlaRopeHalf + lane * 8;
+    mla_rope8(x, y, rope_cos + tab, rope_sin + tab);
+    *reinterpret_cast<uint4*>(row + 512 + lane * 16) = x;
+    *reinterpret_cast<uint4*>(row + 512 + 2 * kMlaRopeHalf + lane * 16) = y;
   }
   if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 640 + 4 * (lane >> 3)) = scale;
+}
+
+// The query side of the MLA RoPE: one warp per (token, head) row of 576
+// bf16; the 512 nope values are copied, the rope part rotated at the
+// token's position (q_out may alias q: each lane writes what it read).
+__global__ void __launch_bounds__(256) rope_mla_q_kernel(
+    int T, int B, int Hq, const int32_t* __restrict__ cu, const int32_t* __restrict__ start_pos,
+    const uint16_t* q, const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
+    int rope_max_pos, uint16_t* q_out, int* err) {
+  const long w = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<long>(T) * Hq) return;
+  const int t = static_cast<int>(w / Hq);
+  const int p = mla_pos(cu, start_pos, B, t, rope_max_pos, lane == 0 ? err : nullptr);
+  if (p < 0) return;
+  const uint16_t* src = q + w * kMlaIn;
+  uint16_t* dst = q_out + w * kMlaIn;
+  // nope: 1024 bytes, two 16-byte pieces per lane
+  const uint4 n0 = *reinterpret_cast<const uint4*>(src + lane * 8);
+  const uint4 n1 = *reinterpret_cast<const uint4*>(src + 256 + lane * 8);
+  uint4 x, y;
+  if (lane < 4) {
+    x = *reinterpret_cast<const uint4*>(src + 512 + lane * 8);
+    y = *reinterpret_cast<const uint4*>(src + 512 + kMlaRopeHalf + lane * 8);
+    const size_t tab = static_cast<size_t>(p) * kMlaRopeHalf + lane * 8;
+    mla_rope8(x, y, rope_cos + tab, rope_sin + tab);
+  }
+  *reinterpret_cast<uint4*>(dst + lane * 8) = n0;
+  *reinterpret_cast<uint4*>(dst + 256 + lane * 8) = n1;
+  if (lane < 4) {
+    *reinterpret_cast<uint4*>(dst + 512 + lane * 8) = x;
+    *reinterpret_cast<uint4*>(dst + 512 + kMlaRopeHalf + lane * 8) = y;
+  }
 }
 
 }  // namespace
@@ -309,8 +405,16 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
       if (grid == 0) return cudaSuccess;
       write_mla_row_kernel<<<grid, threads, 0, stream>>>(
           p.num_tokens, p.num_seqs, p.page_size, p.num_pages, p.bt_stride, p.cu_seqlens_q,
-          p.start_pos, p.block_table, static_cast<const uint16_t*>(p.k),
-          static_cast<uint8_t*>(p.k_pool), p.slot_mapping, p.error_word);
+          p.start_pos, p.block_table, static_cast<const uint16_t*>(p.k), p.rope_cos, p.rope_sin,
+          p.rope_max_pos, static_cast<uint8_t*>(p.k_pool), p.slot_mapping, p.error_word);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess || p.q == nullptr) return e;
+      const long warps = static_cast<long>(p.num_tokens) * p.num_heads_q;
+      rope_mla_q_kernel<<<static_cast<unsigned>((warps * 32 + threads - 1) / threads), threads, 0,
+                          stream>>>(p.num_tokens, p.num_seqs, p.num_heads_q, p.cu_seqlens_q,
+                                    p.start_pos, static_cast<const uint16_t*>(p.q), p.rope_cos,
+                                    p.rope_sin, p.rope_max_pos, static_cast<uint16_t*>(p.q_out),
+                                    p.error_word);
       return cudaGetLastError();
     }
     default:

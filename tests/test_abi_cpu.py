@@ -195,6 +195,13 @@ def test_write_cache_rejects_before_launch(qlib):
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1   # no RoPE tables
     p.mode = 2                       # MLA needs head_dim 576
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
+    p.head_dim = 576                 # MLA: rotating q needs the RoPE tables
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
+    p.rope_cos = fake                # ... both of them, with rows
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
+    p.rope_sin, p.rope_max_pos = fake, 64
+    p.q = fake + 8                   # misaligned query rows
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
 
 
 
@@ -269,6 +276,11 @@ def test_mla_rejects_before_launch(qlib):
     p.sparse_size = 0
     assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 1
     p.sparse_size = 256
+    p.sparse_block_size = 129      # block-wise lists: at most 128 tokens per id
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 2
+    p.sparse_block_size = 4        # the workspace then covers 4x the keys
+    assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 3
+    p.sparse_block_size = 0
     p.num_tokens = 0
     assert lib.qpkv_mla_sparse_decode(ctypes.byref(p), None) == 0
 

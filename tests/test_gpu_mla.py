@@ -74,6 +74,58 @@ def test_write_cache_mla_bit_exact(lib):
     assert np.array_equal(got, _oracle_pool(c))
 
 
+def test_write_cache_mla_rope_bit_exact(lib):
+    """RoPE on the rope part of the rows and of the queries, at positions
+    start_pos[b] + i: pool bytes and rotated queries bit-exact; q_out may be
+    q itself."""
+    from oracle import rope as orope
+    rng = np.random.default_rng(41)
+    lengths = np.array([37, 5, 90], np.int32)
+    start = np.array([3, 200, 0], np.int32)
+    bt, P = synth.page_tables(rng, lengths + start, 64, extra_pages=1)
+    kv = synth.bf16_normal(rng, (int(lengths.sum()), 576))
+    q = synth.bf16_normal(rng, (int(lengths.sum()), 8, 576))
+    cos, sin = orope.cos_sin_table(400, 64, 1.0e4)
+    cu = synth.inclusive_prefix(lengths)
+    pool = torch.full((P, 64, 1, 656), FILL, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    qd = _t(q).to(torch.bfloat16)
+    q_out = lib.write_cache_mla(_t(kv).to(torch.bfloat16), _t(cu), _t(bt), pool, start_pos=_t(start),
+                                error_word=err, rope_cos=_t(cos), rope_sin=_t(sin), q=qd, q_out=qd)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and q_out.data_ptr() == qd.data_ptr()
+    want_pool = np.full((P, 64, 1, 656), FILL, dtype=np.uint8)
+    want_pool, _ = ocache.write_mla_rows(kv, cu, start.astype(np.int64), bt, 64, want_pool, cos, sin)
+    assert np.array_equal(pool.cpu().numpy(), want_pool)
+    want_q = ocache.mla_rope(q, cu, start.astype(np.int64), cos, sin)
+    assert np.array_equal(q_out.float().cpu().numpy(), want_q)
+
+
+def test_write_cache_mla_rope_position_past_table(lib):
+    """A token whose position lies past the RoPE tables is not written and
+    flags the length error."""
+    from oracle import rope as orope
+    rng = np.random.default_rng(42)
+    lengths = np.array([4], np.int32)
+    bt, P = synth.page_tables(rng, lengths + 30, 16)
+    kv = synth.bf16_normal(rng, (4, 576))
+    cos, sin = orope.cos_sin_table(32, 64, 1.0e4)
+    pool = torch.full((P, 16, 1, 656), FILL, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.write_cache_mla(_t(kv).to(torch.bfloat16), _t(synth.inclusive_prefix(lengths)), _t(bt), pool,
+                        start_pos=_t(np.array([30], np.int32)), error_word=err,
+                        rope_cos=_t(cos), rope_sin=_t(sin))
+    torch.cuda.synchronize()
+    assert int(err.item()) & 8
+    got = pool.cpu().numpy().reshape(-1, 656)
+    want = np.full((P, 16, 1, 656), FILL, dtype=np.uint8)
+    want, slots = ocache.write_mla_rows(kv[:2], np.array([2], np.int32), np.array([30]), bt, 16, want, cos, sin)
+    assert np.array_equal(got[slots], want.reshape(-1, 656)[slots])     # positions 30, 31 written
+    untouched = np.ones(got.shape[0], bool)
+    untouched[slots] = False
+    assert np.all(got[untouched] == FILL)                                # 32, 33 not
+
+
 @pytest.mark.parametrize("lengths,qps,QN,bs,S,n,mode", [
     ([300, 700], 1, 16, 64, 256, 200, 0),         # -1 tails, ragged last tile
     ([1000, 513], 1, 128, 64, 640, 640, 0),       # full head tile, S past one 512-key group
@@ -139,3 +191,34 @@ def test_mla_full_size_sampled(lib):
             np.array([n], np.int32), np.array([1], np.int32), d["scale"])
         assert_attention_close(bf16_to_f64(out[t:t + 1]), want_o, atol=ATOL_P_BF16)
         assert_lse_close(lse[t:t + 1].cpu().numpy().astype(np.float64), want_lse)
+
+
+@pytest.mark.parametrize("lengths,qps,QN,bs,S,n_ids,sbs,mode", [
+    ([300, 701], 1, 16, 64, 80, 60, 4, 0),        # partial last block, -1 tail, S*n past 256
+    ([1000, 517], 2, 32, 64, 40, 33, 16, 3),      # two query rows, causal drop inside blocks
+    ([900, 130], 1, 128, 128, 8, 7, 128, 0),      # whole-tile blocks
+])
+def test_mla_block_sparse(lib, lengths, qps, QN, bs, S, n_ids, sbs, mode):
+    """sparse_block_size > 1: each listed id names sbs consecutive tokens."""
+    rng = np.random.default_rng((sum(lengths), sbs))
+    c = _case(sum(lengths) + sbs, lengths, qps, QN, bs, S, 0)
+    T = c["q"].shape[0]
+    idx = np.full((T, 1, S), -1, dtype=np.int32)
+    for t in range(T):
+        nblk = (int(c["lengths"][t // qps]) + sbs - 1) // sbs
+        k = min(n_ids, nblk, S)
+        idx[t, 0, :k] = rng.permutation(nblk)[:k]
+    c["idx"] = idx
+    pool = _gpu_pool(lib, c)
+    lse = torch.full((T, QN), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = lib.mla_sparse_decode(_t(c["q"]).to(torch.bfloat16), pool, _t(idx), _t(c["bt"]),
+                                _t(c["lengths"]), _t(c["cu_q"]), scale=c["scale"], sparse_mode=mode,
+                                lse=lse, error_word=err, sparse_block_size=sbs)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want_o, want_lse = omla.mla_sparse_decode(c["q"], _oracle_pool(c), idx, c["bt"], c["lengths"],
+                                              c["cu_q"], c["scale"], sparse_mode=mode,
+                                              sparse_block_size=sbs)
+    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)

@@ -291,3 +291,35 @@ def test_mla_index_list_stops_at_first_negative_and_rejects_out_of_range():
     assert mla.valid_ids([3, 1, -1, 7], 10).tolist() == [3, 1]
     with pytest.raises(ValueError):
         mla.valid_ids([3, 10], 10)
+
+
+def test_mla_block_sparse_covering_equals_dense():
+    """Block-wise lists (sparse_block_size n): listing every n-token block of
+    the sequence, in any order, is dense attention over all L tokens; a
+    single block id sees exactly its (clipped) tokens; a block starting at or
+    past L_kv is out of range."""
+    rng = np.random.default_rng(21)
+    L, QN, n, bs = 45, 3, 8, 16
+    kv = synth.bf16_normal(rng, (L, 576))
+    q = synth.bf16_normal(rng, (1, QN, 576))
+    bt = rng.permutation(3).astype(np.int32)[None]
+    pool = np.zeros((3, bs, 1, 656), np.uint8)
+    pool, _ = cache.write_mla_rows(kv, np.array([L]), np.array([0]), bt, bs, pool)
+    Kd, Vd = cache.mla_unpack_rows(cache.mla_pack_rows(kv))
+    nblk = (L + n - 1) // n                                   # 6 blocks, the last holds 5 tokens
+    idx = np.full((1, 1, 8), -1, np.int32)
+    idx[0, 0, :nblk] = rng.permutation(nblk)
+    O, lse = mla.mla_sparse_decode(q, pool, idx, bt, np.array([L]), np.array([1]), 0.05,
+                                   sparse_block_size=n)
+    dense, ldense = attention.attend_rows(q[0].astype(np.float64), Kd, Vd, 0.05)
+    assert np.allclose(O[0], dense, rtol=1e-12, atol=1e-13)
+    assert np.allclose(lse[0], ldense, rtol=1e-13, atol=1e-13)
+    idx1 = np.full((1, 1, 2), -1, np.int32)
+    idx1[0, 0, 0] = 5                                         # tokens 40..44
+    O1, _ = mla.mla_sparse_decode(q, pool, idx1, bt, np.array([L]), np.array([1]), 0.05,
+                                  sparse_block_size=n)
+    ref, _ = attention.attend_rows(q[0].astype(np.float64), Kd[40:45], Vd[40:45], 0.05)
+    assert np.allclose(O1[0], ref, rtol=1e-12, atol=1e-13)
+    assert mla.valid_ids([1, -1], 45, 8).tolist() == list(range(8, 16))
+    with pytest.raises(ValueError):
+        mla.valid_ids([6], 45, 8)                             # 6 * 8 = 48 >= 45

@@ -141,3 +141,76 @@ def test_mla_row_layout_roundtrip():
     err = np.abs(V - kv[:, :512]).reshape(9, 4, 128)
     assert np.all(err <= scales[..., None].astype(np.float64) * 0.5 * (1 + 1e-5))
     assert np.array_equal(K[:, :512], V)
+
+
+def test_bf16_round_matches_library_cast():
+    """The oracle's nearest-even bf16 rounding against torch's CPU cast (a
+    library routine), ties included; NaN stays NaN."""
+    import torch
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(20000) * 3).astype(np.float32)
+    hi = rng.integers(0, 0x7F7F, 2000).astype(np.uint32)
+    ties = ((hi << 16) | 0x8000).view(np.float32) * np.where(rng.random(2000) < 0.5, 1, -1).astype(np.float32)
+    x = np.concatenate([x, ties, np.array([np.inf, -np.inf, 0.0, -0.0, 3.4e38, np.nan], np.float32)])
+    got = cache.bf16_round(x)
+    want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin].view(np.uint32), want[fin].view(np.uint32))
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+
+
+def _mla_case(rng, lengths, start):
+    lengths = np.asarray(lengths, np.int32)
+    bt, P = synth.page_tables(rng, lengths + np.asarray(start), 16)
+    kv = synth.bf16_normal(rng, (int(lengths.sum()), 576))
+    pool = np.zeros((P, 16, 1, 656), np.uint8)
+    return kv, synth.inclusive_prefix(lengths), np.asarray(start, np.int64), bt, pool
+
+
+def test_mla_rope_position_zero_is_identity():
+    rng = np.random.default_rng(12)
+    kv, cu, start, bt, pool = _mla_case(rng, [1, 1, 1], [0, 0, 0])
+    cos, sin = rope.cos_sin_table(8, 64, 1.0e4)
+    a, _ = cache.write_mla_rows(kv, cu, start, bt, 16, pool, cos, sin)
+    b, _ = cache.write_mla_rows(kv, cu, start, bt, 16, pool)
+    assert np.array_equal(a, b)
+
+
+def test_mla_rope_quarter_turn_pins_pairs_and_sign():
+    """A table with cos = 0, sin = 1 at every position maps the rope pair
+    (x_i, x_{i+32}) to (-x_{i+32}, x_i) exactly; the nope bytes and scales
+    do not change."""
+    rng = np.random.default_rng(13)
+    kv, cu, start, bt, pool = _mla_case(rng, [5, 3], [7, 0])
+    cos = np.zeros((32, 32), np.float32)
+    sin = np.ones((32, 32), np.float32)
+    rot, _ = cache.write_mla_rows(kv, cu, start, bt, 16, pool, cos, sin)
+    plain, slots = cache.write_mla_rows(kv, cu, start, bt, 16, pool)
+    r = rot.reshape(-1, 656)[slots]
+    p = plain.reshape(-1, 656)[slots]
+    assert np.array_equal(r[:, :512], p[:, :512]) and np.array_equal(r[:, 640:], p[:, 640:])
+    got = cache.bf16_value(r[:, 512:640].copy().view("<u2"))
+    x = kv[:, 512:].astype(np.float64)
+    assert np.array_equal(got[:, :32], -x[:, 32:]) and np.array_equal(got[:, 32:], x[:, :32])
+
+
+def test_mla_rope_dot_depends_on_relative_position():
+    """Rotated query and key rope parts (decoded from the rows, bf16) give
+    the same dot product when both positions shift by the same amount, to
+    the bf16 rounding of the stored values."""
+    rng = np.random.default_rng(14)
+    cos, sin = rope.cos_sin_table(512, 64, 1.0e4)
+    q = synth.bf16_normal(rng, (1, 576))
+    kv = synth.bf16_normal(rng, (1, 576))
+    cu = np.array([1], np.int32)
+
+    def dot(m, n):
+        qr = cache.mla_rope(q, cu, np.array([m]), cos, sin)[0, 512:].astype(np.float64)
+        pool = np.zeros((40, 16, 1, 656), np.uint8)
+        bt = np.arange(40, dtype=np.int32)[None]
+        rows, slots = cache.write_mla_rows(kv, cu, np.array([n]), bt, 16, pool, cos, sin)
+        k, _ = cache.mla_unpack_rows(rows.reshape(-1, 656)[slots])
+        return float(qr @ k[0, 512:])
+    for m, n, d in [(5, 2, 100), (300, 17, 150), (9, 9, 400)]:
+        assert abs(dot(m, n) - dot(m + d, n + d)) < 0.1
+    assert abs(dot(5, 2) - dot(5, 100)) > 0.1          # and does depend on the offset
