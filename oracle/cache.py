@@ -19,6 +19,10 @@ Three modes:
   int8_block128    RoPE on q and k, then Q and K -> INT8 with one fp32 scale
                    per (sequence, 128-token logical block, head); V stored
                    as bf16 unchanged.  Whole sequences only (start_pos 0).
+                   Optional K smoothing (the role of the Sage varlen
+                   "segment_mean" kernel): the per-(sequence, head) mean of
+                   the rotated keys is subtracted before quantising, which
+                   shifts every logit of a query row by the same amount.
   mla_row          one 656-byte row per token: 512 INT8 nope codes with one
                    fp32 scale per 128-wide tile, the 64-wide rope part as
                    bf16, then the 4 scales (README, 参数说明 row key:
@@ -145,19 +149,51 @@ def block128_quant(x_rot, cu_seqlens_q, num_blocks):
     return codes, scales
 
 
+# K smoothing mean: each rotated key value is clamped to [-2^15, 2^15] and
+# rounded (nearest-even) to a multiple of 2^-24; the sum over the sequence
+# is then exact (int64), so the mean does not depend on summation order:
+#   k_mean = float32( float64(sum) / (n * 2^24) )
+K_MEAN_FRAC_BITS = 24
+K_MEAN_CLAMP = 32768.0
+
+
+def k_smoothing_mean(k_rot, cu_seqlens_q):
+    """Per-(sequence, head) mean of rotated keys k_rot float32 [T, H, D]:
+    float32 [B, H, D] (zero for an empty sequence)."""
+    k_rot = np.asarray(k_rot, dtype=F32)
+    begin, end = seq_bounds(cu_seqlens_q)
+    T, H, D = k_rot.shape
+    km = np.zeros((len(begin), H, D), dtype=F32)
+    one = float(2 ** K_MEAN_FRAC_BITS)
+    for b in range(len(begin)):
+        n = int(end[b] - begin[b])
+        if n == 0:
+            continue
+        seg = np.clip(k_rot[begin[b]:end[b]].astype(np.float64), -K_MEAN_CLAMP, K_MEAN_CLAMP)
+        total = np.rint(seg * one).astype(np.int64).sum(axis=0)
+        km[b] = (total.astype(np.float64) / (n * one)).astype(F32)
+    return km
+
+
 def write_int8_block128_rope(q, k, v, cu_seqlens_q, block_table, page_size,
-                             cos, sin, num_blocks, k_pool, v_pool_bits):
+                             cos, sin, num_blocks, k_pool, v_pool_bits, smooth_k=False):
     """Sage-style write: RoPE(q, k), block-INT8 Q and K, bf16 V into pages.
 
     q, k, v: float32 [T, H, D] (bf16 values).  Whole sequences (positions
     start at 0).  Returns (k_pool int8, v_pool_bits uint16, k_scale
-    [B, nb, H], q8 int8 [T, H, D], q_scale [B, nb, H], slots).
+    [B, nb, H], q8 int8 [T, H, D], q_scale [B, nb, H], slots), and with
+    smooth_k the keys quantised are k_rot - k_mean (float32 subtraction)
+    and k_mean float32 [B, H, D] is appended.
     """
     B = len(cu_seqlens_q)
     start = np.zeros(B, dtype=np.int64)
-    _, p_of = token_positions(cu_seqlens_q, start)
+    b_of, p_of = token_positions(cu_seqlens_q, start)
     q_rot = rope.rotate(np.asarray(q, dtype=F32), p_of, cos, sin)
     k_rot = rope.rotate(np.asarray(k, dtype=F32), p_of, cos, sin)
+    km = None
+    if smooth_k:
+        km = k_smoothing_mean(k_rot, cu_seqlens_q)
+        k_rot = (k_rot - km[b_of]).astype(F32)
     q8, q_scale = block128_quant(q_rot, cu_seqlens_q, num_blocks)
     k8, k_scale = block128_quant(k_rot, cu_seqlens_q, num_blocks)
     slots = slot_mapping(cu_seqlens_q, start, block_table, page_size)
@@ -166,8 +202,9 @@ def write_int8_block128_rope(q, k, v, cu_seqlens_q, block_table, page_size,
     v_pool_bits = v_pool_bits.copy().reshape(P * ps, H, D)
     k_pool[slots] = k8
     v_pool_bits[slots] = bf16_bits(v)
-    return (k_pool.reshape(P, ps, H, D), v_pool_bits.reshape(P, ps, H, D),
-            k_scale, q8, q_scale, slots)
+    out = (k_pool.reshape(P, ps, H, D), v_pool_bits.reshape(P, ps, H, D),
+           k_scale, q8, q_scale, slots)
+    return out + (km,) if smooth_k else out
 
 
 MLA_NOPE = 512

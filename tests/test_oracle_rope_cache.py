@@ -214,3 +214,75 @@ def test_mla_rope_dot_depends_on_relative_position():
     for m, n, d in [(5, 2, 100), (300, 17, 150), (9, 9, 400)]:
         assert abs(dot(m, n) - dot(m + d, n + d)) < 0.1
     assert abs(dot(5, 2) - dot(5, 100)) > 0.1          # and does depend on the offset
+
+
+def test_k_smoothing_mean_is_exact_and_order_free():
+    """The smoothing mean is the exact mean of the 2^-24-rounded keys: within
+    2^-25 (plus float32 rounding) of the float64 mean, and bit-identical when
+    a sequence's tokens are permuted; values beyond 2^15 are clamped."""
+    rng = np.random.default_rng(31)
+    lengths = [130, 1, 257]
+    T = sum(lengths)
+    x = (rng.standard_normal((T, 3, 128)) * 4).astype(np.float32)
+    x[5, 0, :7] = np.float32(1e-9)                            # below the fixed-point step
+    cu = synth.inclusive_prefix(lengths)
+    km = cache.k_smoothing_mean(x, cu)
+    begin = [0, 130, 131]
+    for b, n in enumerate(lengths):
+        mean = x[begin[b]:begin[b] + n].astype(np.float64).mean(axis=0)
+        bound = 2.0 ** -25 + np.spacing(np.abs(mean).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(km[b].astype(np.float64) - mean) <= bound)
+    perm = np.concatenate([rng.permutation(130), 130 + np.arange(1), 131 + rng.permutation(257)])
+    assert np.array_equal(cache.k_smoothing_mean(x[perm], cu).view(np.uint32), km.view(np.uint32))
+    big = x.copy()
+    big[0, 0, 0] = np.float32(1e6)
+    kb = cache.k_smoothing_mean(big, cu)
+    want = (np.rint(np.clip(big[:130, 0, 0].astype(np.float64), -32768, 32768) * 2.0 ** 24).sum()
+            / (130 * 2.0 ** 24))
+    assert kb[0, 0, 0] == np.float32(want)
+
+
+def test_k_smoothing_shrinks_int8_error_with_a_key_offset():
+    """Keys with a common per-head offset on the slowest-rotating RoPE pairs
+    (channels the rotation barely moves over the sequence) lose most of their
+    resolution to block-INT8; subtracting the mean first keeps attention
+    much closer to exact float64 attention on the rotated keys, and the
+    cache otherwise equals the unsmoothed one (V, Q)."""
+    from oracle import attention as oatt
+    rng = np.random.default_rng(32)
+    lengths = np.array([300, 170], np.int32)
+    T, H, D, ps = int(lengths.sum()), 2, 128, 64
+    q = synth.bf16_normal(rng, (T, H, D))
+    off = np.zeros((H, D), np.float32)
+    off[:, 56:64] = 12.0
+    off[:, 120:128] = 12.0
+    k = cache.bf16_round((rng.standard_normal((T, H, D)) + off).astype(np.float32))
+    v = synth.bf16_normal(rng, (T, H, D))
+    bt, P = synth.page_tables(rng, lengths, ps)
+    cu = synth.inclusive_prefix(lengths)
+    cos, sin = rope.cos_sin_table(512, D, 1.0e4)
+    nb = 3
+    args = (q, k, v, cu, bt, ps, cos, sin, nb, np.zeros((P, ps, H, D), np.int8),
+            np.zeros((P, ps, H, D), np.uint16))
+    plain = cache.write_int8_block128_rope(*args)
+    smooth = cache.write_int8_block128_rope(*args, smooth_k=True)
+    km = smooth[6]
+    assert np.array_equal(plain[1], smooth[1]) and np.array_equal(plain[3], smooth[3])
+    b_of, p_of = cache.token_positions(cu, np.zeros(2, np.int64))
+    q_rot = rope.rotate(q, p_of, cos, sin).astype(np.float64)
+    k_rot = rope.rotate(k, p_of, cos, sin).astype(np.float64)
+    scale = 1.0 / np.sqrt(D)
+    errs = []
+    for out in (plain, smooth):
+        O, _ = oatt.paged_prefill_int8(out[3], out[4], out[0], out[2], out[1], bt, cu, lengths, scale)
+        err = 0.0
+        for b, (lo, n) in enumerate([(0, 300), (300, 170)]):
+            for h in range(H):
+                vis = oatt.causal_visible(n, n)
+                ref, _ = oatt.attend_rows(q_rot[lo:lo + n, h], k_rot[lo:lo + n, h],
+                                          cache.bf16_value(cache.bf16_bits(v[lo:lo + n, h])), scale, vis)
+                err = max(err, np.abs(O[lo:lo + n, h] - ref).max())
+        errs.append(err)
+    assert errs[1] < 0.5 * errs[0], errs
+    # the codes are those of the shifted keys
+    assert np.all(np.abs(km[:, :, 120:128] - 12.0) < 0.6)
