@@ -99,6 +99,14 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
  *     q_out (int8 [T, Hq, D], TND), scales to k_block_scale [B, num_blocks,
  *     Hkv] and q_block_scale [B, num_blocks, Hq].  Whole sequences only
  *     (start_pos must be NULL: every sequence starts at position 0).  D = 128.
+ *     With flags & QPKV_WRITE_SMOOTH_K (K smoothing, the role of the Sage
+ *     varlen page's segment_mean kernel) the keys quantised are k_rot - m,
+ *     m[b, h] = float32(float64(S) / (n_b * 2^24)) with S the exact int64 sum
+ *     over the sequence's n_b tokens of RNE(clamp(k_rot, -2^15, 2^15) * 2^24);
+ *     m goes to k_mean (float [B, Hkv, 128]) and workspace holds int64
+ *     partial sums [B, num_blocks, Hkv, 128] (qpkv_smooth_workspace_bytes).
+ *     Attention over the smoothed cache is unchanged (every logit of a query
+ *     row moves by scale * q . m); its lse moves by the same amount.
  *  QPKV_WRITE_MLA_ROW  k = kv bf16 [T, 576] (512 nope || 64 rope), Hkv = 1:
  *     each token becomes one 656-byte row of the pool [P, page_size, 1, 656]:
  *     bytes [0, 512) INT8 nope codes (tile i = dims 128i..128i+127 has scale
@@ -125,6 +133,9 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
 #define QPKV_WRITE_FP8_TOKEN_HEAD 0
 #define QPKV_WRITE_INT8_BLOCK128_ROPE 1
 #define QPKV_WRITE_MLA_ROW 2
+
+/* qpkv_write_params.flags */
+#define QPKV_WRITE_SMOOTH_K 1   /* INT8 mode: subtract the per-(sequence, head) key mean */
 
 typedef struct qpkv_write_params {
   int32_t mode;
@@ -156,7 +167,15 @@ typedef struct qpkv_write_params {
   float* q_block_scale;   /* INT8 mode [B, num_blocks, Hq] */
   int32_t* slot_mapping;  /* [T] or NULL */
   int32_t* error_word;    /* device int32 or NULL */
+  int32_t flags;          /* QPKV_WRITE_SMOOTH_K (INT8 mode) or 0 */
+  int32_t pad0;
+  float* k_mean;          /* INT8 + SMOOTH_K: out float [B, Hkv, 128] */
+  void* workspace;        /* INT8 + SMOOTH_K: scratch, 16-byte aligned */
+  size_t workspace_bytes;
 } qpkv_write_params;
+
+/* Scratch bytes of an INT8 write with QPKV_WRITE_SMOOTH_K (0 for negative sizes). */
+size_t qpkv_smooth_workspace_bytes(int32_t num_seqs, int32_t num_blocks, int32_t num_heads_kv);
 
 qpkv_status qpkv_write_cache(const qpkv_write_params* params, void* stream);
 

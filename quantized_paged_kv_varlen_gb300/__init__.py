@@ -26,6 +26,7 @@ PAGE_ROW_MLA = 656
 WRITE_FP8_TOKEN_HEAD = 0
 WRITE_INT8_BLOCK128_ROPE = 1
 WRITE_MLA_ROW = 2
+WRITE_SMOOTH_K = 1          # qpkv_write_params.flags
 PLAN_INFO_LEN = 16
 
 DEV_ERR_TIMEOUT = 1
@@ -59,7 +60,9 @@ class WriteParams(ctypes.Structure):
         (n, _p) for n in (
             "cu_seqlens_q", "start_pos", "block_table", "q", "k", "v", "rope_cos", "rope_sin",
             "k_pool", "v_pool", "k_scale_pool", "v_scale_pool", "k_block_scale", "q_out",
-            "q_block_scale", "slot_mapping", "error_word")]
+            "q_block_scale", "slot_mapping", "error_word")] + [
+        ("flags", _i32), ("pad0", _i32), ("k_mean", _p), ("workspace", _p),
+        ("workspace_bytes", ctypes.c_size_t)]
 
 
 
@@ -113,6 +116,7 @@ def _declare(lib):
         "qpkv_prefill_paged": (_i32, [ctypes.POINTER(PrefillParams), _p]),
         "qpkv_csr_to_block_table": (_i32, [_p, _p, _p, _i32, _i32, _i32, _p, _p]),
         "qpkv_mla_workspace_bytes": (S, [_i32, _i32]),
+        "qpkv_smooth_workspace_bytes": (S, [_i32, _i32, _i32]),
         "qpkv_mla_sparse_decode": (_i32, [ctypes.POINTER(MlaParams), _p]),
     }
     for name, (res, args) in sig.items():
@@ -223,13 +227,23 @@ def write_cache_fp8(k, v, cu_seqlens, block_table, k_pool, v_pool, k_scale_pool,
     _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(fp8)")
 
 
+def smooth_workspace(num_seqs, num_blocks, num_heads_kv, device="cuda"):
+    """Scratch for a K-smoothing INT8 write."""
+    torch = _torch()
+    n = int(load().qpkv_smooth_workspace_bytes(int(num_seqs), int(num_blocks), int(num_heads_kv)))
+    return torch.empty(((n + 15) // 16) * 16, dtype=torch.uint8, device=device)
+
+
 def write_cache_int8_block128_rope(q, k, v, cu_seqlens, block_table, max_seqlen, rope_cos,
                                    rope_sin, k_pool, v_pool, k_block_scale, q_out,
-                                   q_block_scale, slot_mapping=None, error_word=None):
+                                   q_block_scale, slot_mapping=None, error_word=None,
+                                   k_mean=None, workspace=None):
     """Sage-style prefill write: RoPE(q, k), INT8 per-(sequence, 128-token
     block, head) Q and K, bf16 V into pages.  q/k/v bf16 [T, H, 128];
     k_pool int8 [P, ps, Hkv, 128]; v_pool bf16 [P, ps, Hkv, 128];
-    k_block_scale [B, nb, Hkv]; q_out int8 [T, Hq, 128]; q_block_scale [B, nb, Hq]."""
+    k_block_scale [B, nb, Hkv]; q_out int8 [T, Hq, 128]; q_block_scale [B, nb, Hq].
+    With k_mean (fp32 [B, Hkv, 128], filled) the keys are smoothed: their
+    per-(sequence, head) mean is subtracted before quantising."""
     torch = _torch()
     lib = load()
     _need(q, "q", torch.bfloat16, 3)
@@ -256,6 +270,15 @@ def write_cache_int8_block128_rope(q, k, v, cu_seqlens, block_table, max_seqlen,
     p.k_block_scale, p.q_out, p.q_block_scale = _ptr(k_block_scale), _ptr(q_out), _ptr(q_block_scale)
     p.slot_mapping = _ptr(slot_mapping)
     p.error_word = _ptr(error_word)
+    if k_mean is not None:
+        _need(k_mean, "k_mean", torch.float32, 3)
+        if tuple(k_mean.shape) != (p.num_seqs, Hkv, D):
+            raise ValueError("k_mean must be [B, Hkv, 128]")
+        if workspace is None:
+            workspace = smooth_workspace(p.num_seqs, p.num_blocks, Hkv, k.device)
+        p.flags = WRITE_SMOOTH_K
+        p.k_mean = _ptr(k_mean)
+        p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(int8)")
 
 

@@ -221,7 +221,8 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
   switch (p->mode) {
     case QPKV_WRITE_FP8_TOKEN_HEAD:
       if (p->head_dim != 64 && p->head_dim != 128) return QPKV_ERR_UNSUPPORTED;
-      if (p->rope_cos != nullptr || p->rope_sin != nullptr) return QPKV_ERR_UNSUPPORTED;
+      if (p->rope_cos != nullptr || p->rope_sin != nullptr || p->flags != 0)
+        return QPKV_ERR_UNSUPPORTED;
       if (p->v == nullptr || p->v_pool == nullptr || p->k_scale_pool == nullptr ||
           p->v_scale_pool == nullptr)
         return QPKV_ERR_INVALID_ARG;
@@ -239,9 +240,17 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
         return QPKV_ERR_INVALID_ARG;
       if (p->num_blocks < (p->max_seqlen + 127) / 128 || p->rope_max_pos < p->max_seqlen)
         return QPKV_ERR_INVALID_ARG;
+      if (p->flags & ~QPKV_WRITE_SMOOTH_K) return QPKV_ERR_UNSUPPORTED;
+      if (p->flags & QPKV_WRITE_SMOOTH_K) {
+        if (p->k_mean == nullptr || p->workspace == nullptr || !aligned16(p->workspace))
+          return QPKV_ERR_INVALID_ARG;
+        if (p->workspace_bytes <
+            qpkv_smooth_workspace_bytes(p->num_seqs, p->num_blocks, p->num_heads_kv))
+          return QPKV_ERR_WORKSPACE_TOO_SMALL;
+      }
       break;
     case QPKV_WRITE_MLA_ROW:
-      if (p->head_dim != 576 || p->num_heads_kv != 1) return QPKV_ERR_UNSUPPORTED;
+      if (p->head_dim != 576 || p->num_heads_kv != 1 || p->flags != 0) return QPKV_ERR_UNSUPPORTED;
       if (p->rope_cos != nullptr && (p->rope_sin == nullptr || p->rope_max_pos < 1))
         return QPKV_ERR_INVALID_ARG;
       if (p->q != nullptr &&
@@ -410,6 +419,11 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
                                         static_cast<cudaStream_t>(stream), &status);
   if (status != QPKV_OK) return static_cast<qpkv_status>(status);
   return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
+}
+
+size_t qpkv_smooth_workspace_bytes(int32_t num_seqs, int32_t num_blocks, int32_t num_heads_kv) {
+  if (num_seqs < 0 || num_blocks < 0 || num_heads_kv < 0) return 0;
+  return static_cast<size_t>(num_seqs) * num_blocks * num_heads_kv * 128 * sizeof(long long);
 }
 
 size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads_q) {

@@ -112,11 +112,12 @@ __device__ __forceinline__ float block_max_256(float v, float* red) {
   return m;
 }
 
-// Rotate, quantise to INT8 with one block scale, and store the codes.
+// Rotate, subtract the smoothing mean km (shared, 128 floats; NULL: none),
+// quantise to INT8 with one block scale, and store the codes.
 // Returns nothing; writes codes to dst_row (128 int8) and the scale via *scale_out.
 __device__ __forceinline__ void rope_quant_block(const uint16_t* __restrict__ src_row, bool valid,
                                                  int pos, int half, const float* __restrict__ cos_t,
-                                                 const float* __restrict__ sin_t,
+                                                 const float* __restrict__ sin_t, const float* km,
                                                  int8_t* dst_row, float* scale_out, float* red) {
   float y1[32], y2[32];
   float amax = 0.f;
@@ -138,8 +139,12 @@ __device__ __forceinline__ void rope_quant_block(const uint16_t* __restrict__ sr
       for (int j = 0; j < 8; ++j) {
         const float cs = cv[j];
         const float sn = sv[j];
-        const float r1 = __fsub_rn(__fmul_rn(a[j], cs), __fmul_rn(bb[j], sn));
-        const float r2 = __fadd_rn(__fmul_rn(bb[j], cs), __fmul_rn(a[j], sn));
+        float r1 = __fsub_rn(__fmul_rn(a[j], cs), __fmul_rn(bb[j], sn));
+        float r2 = __fadd_rn(__fmul_rn(bb[j], cs), __fmul_rn(a[j], sn));
+        if (km != nullptr) {
+          r1 = __fsub_rn(r1, km[half * 32 + c * 8 + j]);
+          r2 = __fsub_rn(r2, km[64 + half * 32 + c * 8 + j]);
+        }
         y1[c * 8 + j] = r1;
         y2[c * 8 + j] = r2;
         amax = fmaxf(amax, fmaxf(fabsf(r1), fabsf(r2)));
@@ -175,6 +180,42 @@ __device__ __forceinline__ void rope_quant_block(const uint16_t* __restrict__ sr
   d2[1] = make_uint4(w2[4], w2[5], w2[6], w2[7]);
 }
 
+// K smoothing, pass 1: per (sequence, 128-token block, kv head) the int64 sum
+// over the block's tokens of RNE(clamp(k_rot, -2^15, 2^15) * 2^24) per dim
+// (exact, so the order of the sums does not matter); two row phases of 128
+// threads, thread d owns dim d.  The rotation is the one the write applies.
+constexpr float kMeanClamp = 32768.0f, kMeanOne = 16777216.0f;   // 2^15, 2^24
+
+__global__ void __launch_bounds__(256) k_block_sum_kernel(
+    int Hkv, int num_blocks, int max_pos, const int32_t* __restrict__ cu,
+    const uint16_t* __restrict__ k,
+    const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+    long long* __restrict__ partial) {
+  __shared__ long long part[128];
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int begin = seq_begin(cu, b);
+  const int L = __ldg(cu + b) - begin;
+  if (blk * kBlk >= L) return;
+  const int d = threadIdx.x & 127, phase = threadIdx.x >> 7, i = d & 63;
+  // tokens past the launched blocks or the RoPE tables are the write's to flag
+  const int n = min(kBlk, min(L, max_pos) - blk * kBlk);
+  long long acc = 0;
+  for (int r = phase; r < n; r += 2) {
+    const int pos = blk * kBlk + r;
+    const uint16_t* row = k + (static_cast<size_t>(begin + pos) * Hkv + h) * 128;
+    const float a = bf16_bits_to_float(__ldg(row + i)), bb = bf16_bits_to_float(__ldg(row + 64 + i));
+    const float cs = __ldg(cos_t + static_cast<size_t>(pos) * 64 + i);
+    const float sn = __ldg(sin_t + static_cast<size_t>(pos) * 64 + i);
+    const float y = d < 64 ? __fsub_rn(__fmul_rn(a, cs), __fmul_rn(bb, sn))
+                           : __fadd_rn(__fmul_rn(bb, cs), __fmul_rn(a, sn));
+    acc += __float2ll_rn(fminf(fmaxf(y, -kMeanClamp), kMeanClamp) * kMeanOne);
+  }
+  if (phase == 1) part[d] = acc;
+  __syncthreads();
+  if (phase == 0)
+    partial[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + d] = acc + part[d];
+}
+
 __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     int B, int Hq, int Hkv, int ps, int num_pages, int bt_stride, int num_blocks,
     const int32_t* __restrict__ cu, const int32_t* __restrict__ bt,
@@ -182,22 +223,44 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     const uint16_t* __restrict__ v, const float* __restrict__ cos_t,
     const float* __restrict__ sin_t, int8_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
     float* __restrict__ k_bscale, int8_t* __restrict__ q_out, float* __restrict__ q_bscale,
-    int32_t* __restrict__ slots, int* err) {
+    int32_t* __restrict__ slots, const long long* __restrict__ partial, float* __restrict__ k_mean,
+    int max_pos, int* err) {
   constexpr int D = 128;
   __shared__ float red[8];
+  __shared__ float km[D];
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int begin = seq_begin(cu, b);
   const int L = __ldg(cu + b) - begin;
   if (blk * kBlk >= L) return;  // block past this sequence's end
+  // a sequence longer than the launch (max_seqlen) or the RoPE tables
+  const int nblk = (L + kBlk - 1) / kBlk;
+  if ((nblk > static_cast<int>(gridDim.x) || L > max_pos) && blk == 0 && h == 0 &&
+      threadIdx.x == 0)
+    report_error(err, kDevErrBadLength);
+  const bool smooth = partial != nullptr && h < Hkv;
+  if (smooth) {
+    // K smoothing, pass 2: the sequence's mean from the exact block sums
+    if (threadIdx.x < D) {
+      long long sum = 0;
+      const int nsum = min(nblk, static_cast<int>(gridDim.x));
+      for (int j = 0; j < nsum; ++j)
+        sum += partial[((static_cast<size_t>(b) * num_blocks + j) * Hkv + h) * D + threadIdx.x];
+      const float m =
+          __double2float_rn(__ll2double_rn(sum) / (static_cast<double>(L) * static_cast<double>(kMeanOne)));
+      km[threadIdx.x] = m;
+      if (blk == 0) k_mean[(static_cast<size_t>(b) * Hkv + h) * D + threadIdx.x] = m;
+    }
+    __syncthreads();
+  }
   const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
   const int pos = blk * kBlk + r;
-  const bool valid = pos < L;
+  const bool valid = pos < L && pos < max_pos;
   const int t = begin + pos;
 
   if (h < Hq) {
     const uint16_t* src = q + (static_cast<size_t>(t) * Hq + h) * D;
     int8_t* dst = q_out + (static_cast<size_t>(t) * Hq + h) * D;
-    rope_quant_block(src, valid, pos, half, cos_t, sin_t, dst,
+    rope_quant_block(src, valid, pos, half, cos_t, sin_t, nullptr, dst,
                      q_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hq + h, red);
   }
   if (h < Hkv) {
@@ -210,7 +273,7 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     int8_t* dst = k_pool + (slot * Hkv + h) * D;
     // the block reduction needs every thread; an invalid page only drops the store
     __shared__ __align__(16) int8_t sink[2 * D];
-    rope_quant_block(src, valid, pos, half, cos_t, sin_t, ok ? dst : sink,
+    rope_quant_block(src, valid, pos, half, cos_t, sin_t, smooth ? km : nullptr, ok ? dst : sink,
                      k_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hkv + h, red);
     if (ok) {
       const uint4* vs = reinterpret_cast<const uint4*>(v + (static_cast<size_t>(t) * Hkv + h) * D +
@@ -389,6 +452,16 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
       const int nblk = (p.max_seqlen + kBlk - 1) / kBlk;
       if (nblk == 0) return cudaSuccess;
       const int hmax = p.num_heads_q > p.num_heads_kv ? p.num_heads_q : p.num_heads_kv;
+      long long* partial = nullptr;
+      if (p.flags & QPKV_WRITE_SMOOTH_K) {
+        partial = static_cast<long long*>(p.workspace);
+        k_block_sum_kernel<<<dim3(nblk, p.num_heads_kv, p.num_seqs), threads, 0, stream>>>(
+            p.num_heads_kv, p.num_blocks, p.rope_max_pos, p.cu_seqlens_q,
+            static_cast<const uint16_t*>(p.k),
+            p.rope_cos, p.rope_sin, partial);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
       dim3 grid(nblk, hmax, p.num_seqs);
       write_int8_block128_rope_kernel<<<grid, threads, 0, stream>>>(
           p.num_seqs, p.num_heads_q, p.num_heads_kv, p.page_size, p.num_pages, p.bt_stride,
@@ -396,7 +469,7 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
           static_cast<const uint16_t*>(p.k), static_cast<const uint16_t*>(p.v), p.rope_cos,
           p.rope_sin, static_cast<int8_t*>(p.k_pool), static_cast<uint16_t*>(p.v_pool),
           p.k_block_scale, static_cast<int8_t*>(p.q_out), p.q_block_scale, p.slot_mapping,
-          p.error_word);
+          partial, p.k_mean, p.rope_max_pos, p.error_word);
       return cudaGetLastError();
     }
     case QPKV_WRITE_MLA_ROW: {

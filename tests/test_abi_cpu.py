@@ -193,6 +193,16 @@ def test_write_cache_rejects_before_launch(qlib):
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
     p.start_pos = None
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1   # no RoPE tables
+    p.rope_cos, p.rope_sin, p.rope_max_pos, p.max_seqlen, p.num_blocks = fake, fake, 64, 10, 1
+    p.flags = 2                      # unknown flag
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
+    p.flags = 1                      # K smoothing: needs k_mean and scratch
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
+    p.k_mean, p.workspace, p.workspace_bytes = fake, fake, 8
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 3
+    assert lib.qpkv_smooth_workspace_bytes(2, 1, 1) == 2 * 128 * 8
+    p.flags = 0
+    p.rope_cos, p.rope_sin, p.rope_max_pos = None, None, 0
     p.mode = 2                       # MLA needs head_dim 576
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 2
     p.head_dim = 576                 # MLA: rotating q needs the RoPE tables

@@ -73,6 +73,62 @@ def test_write_cache_int8_bit_exact(lib):
         assert np.array_equal(_u32(d["qs"].cpu().numpy()[b, :n]), _u32(qscale[b, :n]))
 
 
+def test_write_cache_int8_smooth_k_bit_exact_and_attention(lib):
+    """K smoothing: codes, block scales and the per-(sequence, head) mean
+    bit-exact; the prefill over the smoothed cache matches the oracle on the
+    same cache, and (the softmax being shift-invariant) the oracle on the
+    unsmoothed cache to the INT8 tolerance."""
+    rng = np.random.default_rng(51)
+    lengths = np.array([1, 300, 129], dtype=np.int32)
+    T, Hq, Hkv, D, ps = int(lengths.sum()), 4, 2, 128, 64
+    q = synth.bf16_normal(rng, (T, Hq, D))
+    off = np.zeros((Hkv, D), np.float32)
+    off[:, 120:128] = 9.0
+    k = ocache.bf16_round((rng.standard_normal((T, Hkv, D)) + off).astype(np.float32))
+    v = synth.bf16_normal(rng, (T, Hkv, D))
+    bt, P = synth.page_tables(rng, lengths, ps)
+    cos, sin = orope.cos_sin_table(512, 128, 1.0e4)
+    B, nb = 3, 3
+    k_pool = torch.full((P, ps, Hkv, D), 99, dtype=torch.int8, device=DEV)
+    v_pool = torch.zeros((P, ps, Hkv, D), dtype=torch.bfloat16, device=DEV)
+    ks = torch.full((B, nb, Hkv), float("nan"), dtype=torch.float32, device=DEV)
+    qs = torch.full((B, nb, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    q8 = torch.zeros((T, Hq, D), dtype=torch.int8, device=DEV)
+    km = torch.full((B, Hkv, D), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cu = synth.inclusive_prefix(lengths)
+    lib.write_cache_int8_block128_rope(
+        _t(q).to(torch.bfloat16), _t(k).to(torch.bfloat16), _t(v).to(torch.bfloat16), _t(cu), _t(bt),
+        300, _t(cos), _t(sin), k_pool, v_pool, ks, q8, qs, error_word=err, k_mean=km)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kp0 = np.full((P, ps, Hkv, D), 99, np.int8)
+    vp0 = np.zeros((P, ps, Hkv, D), np.uint16)
+    kp, vp, kscale, q8w, qscale, slots, kmw = ocache.write_int8_block128_rope(
+        q, k, v, cu, bt, ps, cos, sin, nb, kp0, vp0, smooth_k=True)
+    assert np.array_equal(_u32(km.cpu().numpy()), _u32(kmw))
+    got_k = k_pool.cpu().numpy().reshape(P * ps, Hkv, D)
+    assert np.array_equal(got_k[slots], kp.reshape(P * ps, Hkv, D)[slots])
+    assert np.array_equal(q8.cpu().numpy(), q8w)
+    for b, L in enumerate(lengths):
+        n = (int(L) + 127) // 128
+        assert np.array_equal(_u32(ks.cpu().numpy()[b, :n]), _u32(kscale[b, :n]))
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=DEV)
+    lib.prefill_paged(q8, qs, k_pool, ks, v_pool, _t(bt), _t(cu), _t(lengths), causal=True,
+                      out=out, lse=lse, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    scale = 1.0 / np.sqrt(128.0)
+    want_o, want_lse = oatt.paged_prefill_int8(q8w, qscale, kp, kscale, vp, bt, cu, lengths, scale)
+    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
+    plain = ocache.write_int8_block128_rope(q, k, v, cu, bt, ps, cos, sin, nb, kp0, vp0)
+    o_plain, _ = oatt.paged_prefill_int8(plain[3], plain[4], plain[0], plain[2], plain[1], bt, cu,
+                                         lengths, scale)
+    assert np.abs(bf16_to_f64(out) - o_plain).max() < 0.1
+
+
 def test_rope_table_matches_oracle(lib):
     """The library's table (double precision on the device, rounded to
     float) against the oracle's numpy float64 table: equal or 1 ulp apart."""
