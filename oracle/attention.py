@@ -94,21 +94,30 @@ def lse_merge(O_parts, lse_parts):
 # ---------------------------------------------------------------- decode (FP8)
 
 def gather_fp8_token_head(k_pool, v_pool, k_scale_pool, v_scale_pool,
-                          block_table_row, L, h):
-    """Dequantised K, V f64[L, D] of kv head h of one request."""
-    P, ps, H, D = k_pool.shape
-    rows = page_rows(block_table_row, ps, np.arange(L))
-    kp = k_pool.reshape(P * ps, H, D)
-    vp = v_pool.reshape(P * ps, H, D)
-    ks = k_scale_pool.reshape(P * ps, H)
-    vs = v_scale_pool.reshape(P * ps, H)
-    K = quant.dequant_fp8(kp[rows, h], ks[rows, h][:, None])
-    V = quant.dequant_fp8(vp[rows, h], vs[rows, h][:, None])
+                          block_table_row, L, h, layout="NHD"):
+    """Dequantised K, V f64[L, D] of kv head h of one request.
+
+    layout "NHD": pools [P, page_size, H, D]; "HND" (flashinfer's
+    kv_layout_code): pools [P, H, page_size, D].  Scale pools are
+    [P, page_size, H] in both."""
+    if layout == "HND":
+        P, H, ps, D = k_pool.shape
+    else:
+        P, ps, H, D = k_pool.shape
+    pos = np.arange(L)
+    page = np.asarray(block_table_row, dtype=np.int64)[pos // ps]
+    off = pos % ps
+    if layout == "HND":
+        kc, vc = k_pool[page, h, off], v_pool[page, h, off]
+    else:
+        kc, vc = k_pool[page, off, h], v_pool[page, off, h]
+    K = quant.dequant_fp8(kc, k_scale_pool[page, off, h][:, None])
+    V = quant.dequant_fp8(vc, v_scale_pool[page, off, h][:, None])
     return K, V
 
 
 def paged_decode_fp8(q, k_pool, v_pool, k_scale_pool, v_scale_pool,
-                     block_table, seqlens_kv, scale, requests=None):
+                     block_table, seqlens_kv, scale, requests=None, layout="NHD"):
     """One query token per request (L_q = 1) over an FP8 paged cache.
 
     q: f32/f64 [B, Hq, D] (bf16 values).  Returns (O f64[B, Hq, D],
@@ -116,7 +125,7 @@ def paged_decode_fp8(q, k_pool, v_pool, k_scale_pool, v_scale_pool,
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
-    Hkv = k_pool.shape[2]
+    Hkv = k_pool.shape[1 if layout == "HND" else 2]
     G = Hq // Hkv
     O = np.zeros((B, Hq, D))
     lse = np.full((B, Hq), NEG_INF)
@@ -124,7 +133,7 @@ def paged_decode_fp8(q, k_pool, v_pool, k_scale_pool, v_scale_pool,
         L = int(seqlens_kv[b])
         for h in range(Hkv):
             K, V = gather_fp8_token_head(k_pool, v_pool, k_scale_pool, v_scale_pool,
-                                         block_table[b], L, h)
+                                         block_table[b], L, h, layout)
             o, l = attend_rows(q[b, h * G:(h + 1) * G], K, V, scale)
             O[b, h * G:(h + 1) * G] = o
             lse[b, h * G:(h + 1) * G] = l

@@ -92,12 +92,14 @@ def bf16_value(bits: np.ndarray) -> np.ndarray:
 
 def write_fp8_token_head(k, v, cu_seqlens_q, start_pos, block_table, page_size,
                          k_pool, v_pool, k_scale_pool, v_scale_pool,
-                         q=None, cos=None, sin=None):
+                         q=None, cos=None, sin=None, layout="NHD"):
     """FP8 per-(token, head) write.  k, v: float32 [T, H, D] (bf16 values).
 
     Pools are updated in place copies and returned:
     (k_pool, v_pool, k_scale_pool, v_scale_pool, slots, q_rot or None).
-    With cos/sin given, q and k are rotated first (v never is).
+    With cos/sin given, q and k are rotated first (v never is).  layout
+    "HND" takes K/V pools [P, H, page_size, D] (token at page offset o of
+    head h in [page, h, o]); the scale pools stay [P, page_size, H].
     """
     k = np.asarray(k, dtype=F32)
     v = np.asarray(v, dtype=F32)
@@ -110,6 +112,19 @@ def write_fp8_token_head(k, v, cu_seqlens_q, start_pos, block_table, page_size,
     slots = slot_mapping(cu_seqlens_q, start_pos, block_table, page_size)
     kc, ks = quant.quant_fp8_last_axis(k)
     vc, vs = quant.quant_fp8_last_axis(v)
+    if layout == "HND":
+        P, H, ps, D = k_pool.shape
+        b_of, p_of = token_positions(cu_seqlens_q, start_pos)
+        page = np.asarray(block_table, dtype=np.int64)[b_of, p_of // page_size]
+        off = p_of % page_size
+        k_pool, v_pool = k_pool.copy(), v_pool.copy()
+        k_scale_pool, v_scale_pool = k_scale_pool.copy(), v_scale_pool.copy()
+        for hh in range(H):
+            k_pool[page, hh, off] = kc[:, hh]
+            v_pool[page, hh, off] = vc[:, hh]
+            k_scale_pool[page, off, hh] = ks[:, hh]
+            v_scale_pool[page, off, hh] = vs[:, hh]
+        return k_pool, v_pool, k_scale_pool, v_scale_pool, slots, q_rot
     P, ps, H, D = k_pool.shape
     k_pool = k_pool.copy().reshape(P * ps, H, D)
     v_pool = v_pool.copy().reshape(P * ps, H, D)

@@ -323,3 +323,32 @@ def test_mla_block_sparse_covering_equals_dense():
     assert mla.valid_ids([1, -1], 45, 8).tolist() == list(range(8, 16))
     with pytest.raises(ValueError):
         mla.valid_ids([6], 45, 8)                             # 6 * 8 = 48 >= 45
+
+
+def test_hnd_layout_holds_the_same_tokens_and_decodes_the_same():
+    """HND pools [P, H, page_size, D] hold token (page, offset o) of head h
+    at [page, h, o]: the same codes as NHD's [page, o, h], with the scale
+    pools unchanged, and decode over either layout gives identical results."""
+    wl = synth.batched_decode(3, B=3, lo=20, hi=70, Hq=8, Hkv=2, D=64, page_size=16)
+    k, v = wl.kv_all()
+    P, ps, H, D = wl.num_pages, wl.page_size, wl.Hkv, wl.D
+    start = np.zeros(wl.B, np.int64)
+    zs = np.zeros((P, ps, H), np.float32)
+    nhd = cache.write_fp8_token_head(k, v, wl.cu_seqlens, start, wl.block_table, ps,
+                                     np.zeros((P, ps, H, D), np.uint8),
+                                     np.zeros((P, ps, H, D), np.uint8), zs, zs)
+    hnd = cache.write_fp8_token_head(k, v, wl.cu_seqlens, start, wl.block_table, ps,
+                                     np.zeros((P, H, ps, D), np.uint8),
+                                     np.zeros((P, H, ps, D), np.uint8), zs, zs, layout="HND")
+    b_of, p_of = cache.token_positions(wl.cu_seqlens, start)
+    for t in range(0, len(b_of), 7):
+        page = wl.block_table[b_of[t], p_of[t] // ps]
+        o = p_of[t] % ps
+        for h in range(H):
+            assert np.array_equal(hnd[0][page, h, o], nhd[0][page, o, h])
+            assert np.array_equal(hnd[1][page, h, o], nhd[1][page, o, h])
+    assert np.array_equal(hnd[2], nhd[2]) and np.array_equal(hnd[3], nhd[3])
+    O1, l1 = attention.paged_decode_fp8(wl.q, *nhd[:4], wl.block_table, wl.lengths, wl.scale)
+    O2, l2 = attention.paged_decode_fp8(wl.q, *hnd[:4], wl.block_table, wl.lengths, wl.scale,
+                                        layout="HND")
+    assert np.array_equal(O1, O2) and np.array_equal(l1, l2)
