@@ -136,6 +136,7 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
 
 /* qpkv_write_params.flags */
 #define QPKV_WRITE_SMOOTH_K 1   /* INT8 mode: subtract the per-(sequence, head) key mean */
+#define QPKV_WRITE_HND 2        /* FP8 mode: K/V pools [P, Hkv, page_size, D] (scales unchanged) */
 
 typedef struct qpkv_write_params {
   int32_t mode;
@@ -197,7 +198,19 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* params, void* stream);
  * UNSUPPORTED (head_dim not in {64, 128}, Hq/Hkv not in {1, 2, 4, 8},
  * page_size not a multiple of 16 dividing 256 or a multiple of 256),
  * WORKSPACE_TOO_SMALL, CUDA. */
-#define QPKV_PLAN_INFO_LEN 16
+#define QPKV_PLAN_INFO_LEN 24
+
+/* K/V pool layouts of the FP8 decode path (flashinfer's kv_layout_code in
+ * "[Refactor] Unify JIT/Customization/AOT mode", BatchDecodeWithPagedKVCacheRun):
+ * NHD = [P, page_size, Hkv, D] (the default), HND = [P, Hkv, page_size, D].
+ * The per-(token, head) scale pools stay [P, page_size, Hkv] in both. */
+#define QPKV_KV_LAYOUT_NHD 0
+#define QPKV_KV_LAYOUT_HND 1
+
+/* Switch a plan (from qpkv_decode_plan / qpkv_decode_plan_host) to the K/V
+ * pool layout of the pools later passed to qpkv_decode_run / _attend; a new
+ * plan starts as NHD.  Errors: INVALID_ARG (not a plan, unknown layout). */
+qpkv_status qpkv_decode_plan_set_kv_layout(int64_t* plan_info, int32_t kv_layout);
 
 qpkv_status qpkv_decode_workspace_sizes(const int32_t* seqlens_kv_host, int32_t batch_size,
                                         int32_t num_qo_heads, int32_t num_kv_heads,

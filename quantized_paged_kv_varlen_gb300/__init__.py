@@ -27,7 +27,9 @@ WRITE_FP8_TOKEN_HEAD = 0
 WRITE_INT8_BLOCK128_ROPE = 1
 WRITE_MLA_ROW = 2
 WRITE_SMOOTH_K = 1          # qpkv_write_params.flags
-PLAN_INFO_LEN = 16
+WRITE_HND = 2
+PLAN_INFO_LEN = 24
+KV_LAYOUTS = {"NHD": 0, "HND": 1}   # K/V pool layouts of the FP8 decode path
 
 DEV_ERR_TIMEOUT = 1
 DEV_ERR_BAD_PAGE = 2
@@ -108,6 +110,7 @@ def _declare(lib):
         "qpkv_decode_attend": (_i32, [P64, _p, S, _p, _p, _p, _p, _p, _p, _i32, _i32, _p,
                                       _i32, ctypes.c_float, _p, _p]),
         "qpkv_decode_merge": (_i32, [P64, _p, S, _p, _p, _p, _p]),
+        "qpkv_decode_plan_set_kv_layout": (_i32, [P64, _i32]),
         "qpkv_decode_static": (_i32, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
                                       _i32, _p, _i32, ctypes.c_float, _p, _p, _p, _p]),
         "qpkv_fp8_attn_fwd": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p,
@@ -203,9 +206,10 @@ def _base_params(mode, cu_seqlens, block_table, page_size, num_pages, num_tokens
 
 
 def write_cache_fp8(k, v, cu_seqlens, block_table, k_pool, v_pool, k_scale_pool, v_scale_pool,
-                    start_pos=None, slot_mapping=None, error_word=None):
+                    start_pos=None, slot_mapping=None, error_word=None, kv_layout="NHD"):
     """FP8 per-(token, head) cache write.  k, v: bf16 [T, Hkv, D]; pools u8
-    [P, page_size, Hkv, D]; scale pools float32 [P, page_size, Hkv]."""
+    [P, page_size, Hkv, D] (kv_layout "HND": [P, Hkv, page_size, D]); scale
+    pools float32 [P, page_size, Hkv] in both layouts."""
     torch = _torch()
     lib = load()
     _need(k, "k", torch.bfloat16, 3)
@@ -214,8 +218,12 @@ def write_cache_fp8(k, v, cu_seqlens, block_table, k_pool, v_pool, k_scale_pool,
     _need(v_pool, "v_pool", torch.uint8, 4)
     _need(k_scale_pool, "k_scale_pool", torch.float32, 3)
     _need(v_scale_pool, "v_scale_pool", torch.float32, 3)
-    P, ps, H, D = k_pool.shape
+    if kv_layout == "HND":
+        P, H, ps, D = k_pool.shape
+    else:
+        P, ps, H, D = k_pool.shape
     p = _base_params(WRITE_FP8_TOKEN_HEAD, cu_seqlens, block_table, ps, P, k.shape[0], 0)
+    p.flags = WRITE_HND if kv_layout == "HND" else 0
     p.num_heads_kv = H
     p.head_dim = D
     p.k, p.v = _ptr(k), _ptr(v)
@@ -338,7 +346,7 @@ class DecodePlan:
     """
 
     def __init__(self, seqlens_kv, num_qo_heads, num_kv_heads, page_size, head_dim,
-                 device="cuda", num_sms=None):
+                 device="cuda", num_sms=None, kv_layout="NHD"):
         torch = _torch()
         import numpy as np
         lib = load()
@@ -346,6 +354,9 @@ class DecodePlan:
         self.lens = lens
         self.B = int(lens.shape[0])
         self.Hq, self.Hkv, self.D, self.page_size = num_qo_heads, num_kv_heads, head_dim, page_size
+        if kv_layout not in KV_LAYOUTS:
+            raise ValueError("kv_layout must be 'NHD' or 'HND'")
+        self.kv_layout = kv_layout
         if num_sms is None:
             num_sms = torch.cuda.get_device_properties(device).multi_processor_count
         self.num_sms = int(num_sms)
@@ -378,6 +389,8 @@ class DecodePlan:
                                     ctypes.c_void_p(buf.data_ptr()), buf.numel(),
                                     _ptr(self.int_ws), self.int_ws.numel(), self.plan_info,
                                     _stream()), "qpkv_decode_plan")
+        _check(lib.qpkv_decode_plan_set_kv_layout(self.plan_info, KV_LAYOUTS[self.kv_layout]),
+               "qpkv_decode_plan_set_kv_layout")
         ev = torch.cuda.Event()
         ev.record()
         self._copied[self._which] = ev
@@ -410,7 +423,8 @@ class DecodePlan:
         _need(block_table, "block_table", torch.int32, 2)
         if tuple(q.shape) != (self.B, self.Hq, self.D):
             raise ValueError(f"q must be [{self.B}, {self.Hq}, {self.D}]")
-        if k_pool.shape[1] != self.page_size or k_pool.shape[2] != self.Hkv:
+        ps_dim, h_dim = (2, 1) if self.kv_layout == "HND" else (1, 2)
+        if k_pool.shape[ps_dim] != self.page_size or k_pool.shape[h_dim] != self.Hkv:
             raise ValueError("pool shape does not match the plan")
 
     def run(self, q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table, sm_scale,

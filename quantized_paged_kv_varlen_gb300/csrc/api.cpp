@@ -121,6 +121,7 @@ void fill_plan_layout(const int32_t* lens, int32_t B, int64_t Hq, int64_t Hkv, i
   p->num_kv_heads = Hkv;
   p->head_dim = D;
   for (int32_t b = 0; b < B; ++b) p->max_len = lens[b] > p->max_len ? lens[b] : p->max_len;
+  p->kv_layout = QPKV_KV_LAYOUT_NHD;
   p->magic = kPlanMagic;
 }
 
@@ -172,6 +173,16 @@ using namespace qpkv;
 
 extern "C" {
 
+qpkv_status qpkv_decode_plan_set_kv_layout(int64_t* plan_info, int32_t kv_layout) {
+  DecodePlan p;
+  if (!load_plan(plan_info, &p)) return QPKV_ERR_INVALID_ARG;
+  if (kv_layout != QPKV_KV_LAYOUT_NHD && kv_layout != QPKV_KV_LAYOUT_HND)
+    return QPKV_ERR_INVALID_ARG;
+  p.kv_layout = kv_layout;
+  std::memcpy(plan_info, &p, sizeof(p));
+  return QPKV_OK;
+}
+
 const char* qpkv_status_string(qpkv_status s) {
   switch (s) {
     case QPKV_OK: return "ok";
@@ -221,7 +232,7 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
   switch (p->mode) {
     case QPKV_WRITE_FP8_TOKEN_HEAD:
       if (p->head_dim != 64 && p->head_dim != 128) return QPKV_ERR_UNSUPPORTED;
-      if (p->rope_cos != nullptr || p->rope_sin != nullptr || p->flags != 0)
+      if (p->rope_cos != nullptr || p->rope_sin != nullptr || (p->flags & ~QPKV_WRITE_HND))
         return QPKV_ERR_UNSUPPORTED;
       if (p->v == nullptr || p->v_pool == nullptr || p->k_scale_pool == nullptr ||
           p->v_scale_pool == nullptr)

@@ -175,7 +175,9 @@ __device__ __forceinline__ void split3(float x, float s1, float inv1, uint8_t& c
   c3 = f32_to_e4m3(r2 * inv1 * 256.0f);
 }
 
-template <int D, int G>
+// HND: K/V pools [P, Hkv, ps, D] (compile-time, so the NHD kernel carries
+// no code for the other layout)
+template <int D, int G, bool HND>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attend_kernel(const __grid_constant__ CUtensorMap k_map,
                          const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
@@ -237,16 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k < n_my) it = a.items[blockIdx.x + static_cast<size_t>(k) * gridDim.x];
       return it;
     };
-    // pool row of box `lane` of an item (-1: none / skipped page)
+    // box `lane` of an item: x = token row page * ps + offset (indexes the
+    // scale pools), y = the K/V row of the tensor maps (x for NHD, page *
+    // Hkv * ps + offset for HND); -1: none / skipped page
     auto box_rows = [&](int k, const DecodeItem& it) {
-      int row = -1;
+      int2 row = make_int2(-1, -1);
       if (k < n_my && lane < item_tiles(it) * bpt) {
         const int tok = it.t0 + (lane / bpt) * kTile + (lane % bpt) * R;
         if (tok < it.t1) {
           const int page =
               __ldg(a.block_table + static_cast<size_t>(it.b) * a.bt_stride + tok / ps);
           if (page >= 0 && page < a.num_pages) {
-            row = page * ps + (tok % ps);
+            row.x = page * ps + (tok % ps);
+            row.y = HND ? page * a.Hkv * ps + (tok % ps) : row.x;
           } else {
             report_error(a.err, kDevErrBadPage);
           }
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int pos = 0;   // ring position (K and V tiles)
     int kq = 0;    // K tiles emitted (scale-ring position)
-    auto emit = [&](int k, const DecodeItem& it, int rows, int j, bool is_v) -> bool {
+    auto emit = [&](int k, const DecodeItem& it, int2 rows, int j, bool is_v) -> bool {
       const int s = pos % NS;
       bool ok = true;
       if (lane == 0) ok = wait_or_abort(&sh.empty[s], ((pos / NS) & 1) ^ 1, sh, a.err);
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nvalid = min(kTile, it.t1 - tok0);
       const int nfull = nvalid / R;               // boxes entirely inside the item
       const int tail = nvalid - nfull * R;        // rows of the partly valid box
-      const int my_row = __shfl_sync(0xffffffffu, rows, j * bpt + (lane < bpt ? lane : 0));
+      const int my_row = __shfl_sync(0xffffffffu, rows.y, j * bpt + (lane < bpt ? lane : 0));
       const unsigned issue = __ballot_sync(0xffffffffu, lane < nfull && my_row >= 0);
       if (!is_v && j == 0) {
         // first tile of the item: publish its descriptor and query rows
@@ -290,13 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < nfull && my_row >= 0)
         tma_load_3d(stage + lane * R * D, is_v ? &v_map : &k_map, &sh.full[s], 0, it.hk, my_row);
       if (tail > 0) {
-        const int row0 = __shfl_sync(0xffffffffu, rows, j * bpt + nfull);
+        const int row0 = __shfl_sync(0xffffffffu, rows.y, j * bpt + nfull);
         if (row0 >= 0) {
           const uint8_t* pool = is_v ? a.v_pool : a.k_pool;
           for (int i = lane; i < tail * (D / 16); i += 32) {
             const int r = i / (D / 16), c = i % (D / 16);
+            const size_t kv_row = HND ? static_cast<size_t>(row0 + r) + static_cast<size_t>(it.hk) * ps
+                                      : static_cast<size_t>(row0 + r) * a.Hkv + it.hk;
             cp_async_16(stage + swizzled_offset(nfull * R + r, 16 * c, D),
-                        pool + (static_cast<size_t>(row0 + r) * a.Hkv + it.hk) * D + 16 * c);
+                        pool + kv_row * D + 16 * c);
           }
         }
       }
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int m = 0; m < kTile / 32; ++m) {
           const int t = lane + 32 * m;
-          const int row0 = __shfl_sync(0xffffffffu, rows, j * bpt + t / R);
+          const int row0 = __shfl_sync(0xffffffffu, rows.x, j * bpt + t / R);
           if (t < nvalid && row0 >= 0) {
             const size_t e = static_cast<size_t>(row0 + t % R) * a.Hkv + it.hk;
             cp_async_4(slot + t, a.k_scale + e);
@@ -319,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // descriptors run two items ahead, page rows one item ahead
     DecodeItem d0 = load_desc(0), d1 = load_desc(1), d2 = load_desc(2);
-    int r0 = box_rows(0, d0), r1 = box_rows(1, d1);
+    int2 r0 = box_rows(0, d0), r1 = box_rows(1, d1);
     bool ok = n_my > 0;
     for (int j = 0; ok && j < item_tiles(d0); ++j) ok = emit(0, d0, r0, j, false);
     for (int k = 0; ok && k < n_my; ++k) {
       const DecodeItem d3 = load_desc(k + 3);
-      const int r2 = box_rows(k + 2, d2);
+      const int2 r2 = box_rows(k + 2, d2);
       if (k + 1 < n_my)
         for (int j = 0; ok && j < item_tiles(d1); ++j) ok = emit(k + 1, d1, r1, j, false);
       for (int j = 0; ok && j < item_tiles(d0); ++j) ok = emit(k, d0, r0, j, true);
@@ -693,9 +700,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(int B, int Hq,
 
 template <int D, int G>
 cudaError_t launch_attend_t(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
-                            cudaStream_t stream) {
+                            bool hnd, cudaStream_t stream) {
   using C = Cfg<D, G>;
-  auto* kern = decode_attend_kernel<D, G>;
+  auto* kern = hnd ? decode_attend_kernel<D, G, true> : decode_attend_kernel<D, G, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -727,10 +734,15 @@ cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, void* 
   const int Hkv = static_cast<int>(plan.num_kv_heads);
   const int G = static_cast<int>(plan.num_qo_heads / plan.num_kv_heads);
   const int R = page_size < kTile ? page_size : kTile;
+  // pool as (d, kv head, K/V row); NHD rows are tokens (stride Hkv * D, head
+  // stride D), HND rows run through each (page, head) run of ps tokens
+  // (stride D, head stride ps * D)
+  const bool hnd = plan.kv_layout == QPKV_KV_LAYOUT_HND;
   CUtensorMap km, vm;
   const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
-                            static_cast<uint64_t>(num_pages) * page_size};
-  const uint64_t strides[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv) * D};
+                            static_cast<uint64_t>(num_pages) * page_size * (hnd ? Hkv : 1)};
+  const uint64_t strides[2] = {hnd ? static_cast<uint64_t>(page_size) * D : static_cast<uint64_t>(D),
+                               hnd ? static_cast<uint64_t>(D) : static_cast<uint64_t>(Hkv) * D};
   const uint32_t box[3] = {static_cast<uint32_t>(D), 1u, static_cast<uint32_t>(R)};
   const CUtensorMapSwizzle swz =
       D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -761,7 +773,7 @@ cudaError_t launch_decode_attend(const DecodePlan& plan, float* float_ws, void* 
   a.part_lse = float_ws + plan.total_splits * plan.num_qo_heads * plan.head_dim;
   a.err = error_word;
 #define QPKV_DECODE_CASE(DD, GG) \
-  if (D == DD && G == GG) return launch_attend_t<DD, GG>(km, vm, a, stream);
+  if (D == DD && G == GG) return launch_attend_t<DD, GG>(km, vm, a, hnd, stream);
   QPKV_DECODE_CASE(128, 1)
   QPKV_DECODE_CASE(128, 2)
   QPKV_DECODE_CASE(128, 4)

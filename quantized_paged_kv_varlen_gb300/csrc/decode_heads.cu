@@ -128,7 +128,7 @@ struct HShared {
   uint64_t ep_ready[2];      // item's O scales written, O may be read once complete
   uint64_t q_done[2];        // item's query terms and their scales written
   DecodeItem desc[2];
-  int tab[2][kMaxTilesItem];   // pool row of each tile's box, -1 if its page is bad
+  int tab[2][kMaxTilesItem];   // K/V row of each tile's box in the tensor maps, -1 if its page is bad
   float sig_q[2][32];          // query term scale per query head
   float sig_p[2][32];          // probability term scale per query head
   float ep_scale[2][kTile];   // per O row: sig_p / softmax denominator
@@ -197,7 +197,9 @@ __device__ __forceinline__ void hsplit3x2(float x0, float x1, float inv1, float 
 
 
 
-template <int D, int G>
+// HND: K/V pools [P, Hkv, ps, D] (a compile-time switch, so the NHD kernel
+// carries no code for the other layout)
+template <int D, int G, bool HND>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_heads_kernel(const __grid_constant__ CUtensorMap k_map,
                         const __grid_constant__ CUtensorMap v_map, const HeadsArgs a) {
@@ -273,19 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < a.num_items) it = a.items[idx];
       const int ntl = it.b < 0 ? 0 : htiles(it, nt);
       // lane j resolves tile j's page
-      int row = -1;
+      int row = -1, krow = -1;
       if (lane < ntl) {
         const int tok = it.t0 + lane * nt;
         const int page = __ldg(a.block_table + static_cast<size_t>(it.b) * a.bt_stride + tok / ps);
         if (page >= 0 && page < a.num_pages) {
           row = page * ps + tok % ps;
+          krow = HND ? page * Hkv * ps + tok % ps : row;
         } else {
           report_error(a.err, kDevErrBadPage);
         }
       }
       // the resources of item o-2 must be released by every role
       if (!warp_wait(&sh.desc_free[d], ((o >> 1) & 1) ^ 1, sh, a.err, lane)) break;
-      if (lane < kMaxTilesItem) sh.tab[d][lane] = row;
+      if (lane < kMaxTilesItem) sh.tab[d][lane] = krow;
       if (lane == 0) sh.desc[d] = it;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.tab_full[d]);
@@ -362,8 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = lane; i < Hkv * per_head; i += 32) {
             const int h = i / per_head, rem = i % per_head;
             const int t = rem / kChunks, c = rem % kChunks;
-            cp_async_16(stage + swizzled_offset(h * nt + t, 16 * c, D),
-                        pool + (static_cast<size_t>(row + t) * Hkv + h) * D + 16 * c);
+            const size_t kv_row = HND ? static_cast<size_t>(row + t) + static_cast<size_t>(h) * a.page_size
+                                      : static_cast<size_t>(row + t) * Hkv + h;
+            cp_async_16(stage + swizzled_offset(h * nt + t, 16 * c, D), pool + kv_row * D + 16 * c);
           }
           cp_async_wait_all();
           fence_proxy_async_smem();   // generic-proxy rows, read by the tensor cores
@@ -834,9 +838,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int G>
 cudaError_t launch_heads_t(const CUtensorMap& km, const CUtensorMap& vm, const HeadsArgs& a,
-                           cudaStream_t stream) {
+                           bool hnd, cudaStream_t stream) {
   using C = HCfg<D>;
-  auto* kern = decode_heads_kernel<D, G>;
+  auto* kern = hnd ? decode_heads_kernel<D, G, true> : decode_heads_kernel<D, G, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -887,10 +891,15 @@ cudaError_t launch_decode_heads(const DecodePlan& plan, float* float_ws, void* i
     return cudaErrorInvalidValue;
   }
   // pool viewed as (d, token row, kv head): boxes come out head-major in smem
+  // (HND: rows run through each (page, head) run of ps tokens, row stride D,
+  // head stride ps * D)
+  const bool hnd = plan.kv_layout == QPKV_KV_LAYOUT_HND;
   CUtensorMap km, vm;
-  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(num_pages) * page_size,
+  const uint64_t dims[3] = {static_cast<uint64_t>(D),
+                            static_cast<uint64_t>(num_pages) * page_size * (hnd ? Hkv : 1),
                             static_cast<uint64_t>(Hkv)};
-  const uint64_t strides[2] = {static_cast<uint64_t>(Hkv) * D, static_cast<uint64_t>(D)};
+  const uint64_t strides[2] = {hnd ? static_cast<uint64_t>(D) : static_cast<uint64_t>(Hkv) * D,
+                               hnd ? static_cast<uint64_t>(page_size) * D : static_cast<uint64_t>(D)};
   const uint32_t box[3] = {static_cast<uint32_t>(D), static_cast<uint32_t>(nt),
                            static_cast<uint32_t>(Hkv)};
   const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -925,7 +934,7 @@ cudaError_t launch_decode_heads(const DecodePlan& plan, float* float_ws, void* i
   a.err = error_word;
   const int G = Hq / Hkv;
 #define QPKV_HEADS_CASE(DD, GG) \
-  if (D == DD && G == GG) return launch_heads_t<DD, GG>(km, vm, a, stream);
+  if (D == DD && G == GG) return launch_heads_t<DD, GG>(km, vm, a, hnd, stream);
   QPKV_HEADS_CASE(128, 1)
   QPKV_HEADS_CASE(128, 2)
   QPKV_HEADS_CASE(128, 4)

@@ -33,6 +33,7 @@ struct DecodePlan {
   int64_t max_len;   // longest request; block_table rows must cover it
   int64_t kind;      // 0: one kv head per work item, 1: all kv heads per work item
   int64_t counter_offset;  // kind 1: bytes into the int workspace of 2 int32 work counters
+  int64_t kv_layout;       // QPKV_KV_LAYOUT_NHD (planned) or QPKV_KV_LAYOUT_HND (set later)
   int64_t magic;
 };
 constexpr int64_t kPlanMagic = 0x71706b76706c616eLL;  // "qpkvplan"

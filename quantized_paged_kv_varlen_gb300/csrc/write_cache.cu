@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ bt,
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, uint8_t* __restrict__ k_pool,
     uint8_t* __restrict__ v_pool, float* __restrict__ k_scale, float* __restrict__ v_scale,
-    int32_t* __restrict__ slots, int* err) {
+    int32_t* __restrict__ slots, int hnd, int* err) {
   constexpr int EPL = D / 32;  // 2 or 4 elements per lane
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
   if (page < 0) return;
   const size_t slot = static_cast<size_t>(page) * ps + (p % ps);
   if (slots != nullptr && h == 0 && lane == 0) slots[t] = static_cast<int32_t>(slot);
+  // K/V row of (token, head): NHD [P, ps, H, D], HND [P, H, ps, D]
+  const size_t kv_row = hnd ? (static_cast<size_t>(page) * H + h) * ps + (p % ps) : slot * H + h;
 
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
       for (int i = 0; i < EPL; ++i)
         packed |= static_cast<uint32_t>(f32_to_e4m3(__fdiv_rn(x[i], scale))) << (8 * i);
     }
-    uint8_t* dst = (which ? v_pool : k_pool) + (slot * H + h) * D + lane * EPL;
+    uint8_t* dst = (which ? v_pool : k_pool) + kv_row * D + lane * EPL;
     if constexpr (EPL == 4) {
       *reinterpret_cast<uint32_t*>(dst) = packed;
     } else {
@@ -445,7 +447,7 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
           p.cu_seqlens_q, p.start_pos, p.block_table, static_cast<const uint16_t*>(p.k),
           static_cast<const uint16_t*>(p.v), static_cast<uint8_t*>(p.k_pool),
           static_cast<uint8_t*>(p.v_pool), p.k_scale_pool, p.v_scale_pool, p.slot_mapping,
-          p.error_word);
+          (p.flags & QPKV_WRITE_HND) ? 1 : 0, p.error_word);
       return cudaGetLastError();
     }
     case QPKV_WRITE_INT8_BLOCK128_ROPE: {

@@ -46,6 +46,18 @@ def test_struct_mirror_and_strings(qlib):
     assert lib.qpkv_version() >= 100
 
 
+PLAN_LEN = 24   # QPKV_PLAN_INFO_LEN
+
+
+def test_plan_info_length_matches_header():
+    import re
+    from pathlib import Path
+    import quantized_paged_kv_varlen_gb300 as q
+    hdr = (Path(__file__).resolve().parent.parent / "include" / "qpkv.h").read_text()
+    n = int(re.search(r"#define QPKV_PLAN_INFO_LEN (\d+)", hdr).group(1))
+    assert n == PLAN_LEN == q.PLAN_INFO_LEN
+
+
 def _plan(lib, lens, Hq=32, Hkv=8, ps=16, D=128, sms=148):
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     ib, fb = ctypes.c_size_t(), ctypes.c_size_t()
@@ -53,7 +65,7 @@ def _plan(lib, lens, Hq=32, Hkv=8, ps=16, D=128, sms=148):
                                          ctypes.byref(ib), ctypes.byref(fb))
     assert st == 0
     host = np.zeros(ib.value, dtype=np.uint8)
-    info = (ctypes.c_int64 * 16)()
+    info = (ctypes.c_int64 * PLAN_LEN)()
     st = lib.qpkv_decode_plan_host(lens.ctypes.data, len(lens), Hq, Hkv, ps, D, sms,
                                    host.ctypes.data, host.nbytes, info)
     assert st == 0
@@ -133,7 +145,7 @@ def test_plan_rejects_page_size_and_small_buffers(qlib):
     _, lib = qlib
     lens = np.ascontiguousarray([100, 200], dtype=np.int32)
     host = np.zeros(1 << 16, dtype=np.uint8)
-    info = (ctypes.c_int64 * 16)()
+    info = (ctypes.c_int64 * PLAN_LEN)()
     assert lib.qpkv_decode_plan_host(lens.ctypes.data, 2, 32, 8, 24, 128, 148,
                                      host.ctypes.data, host.nbytes, info) == 2
     assert lib.qpkv_decode_plan_host(lens.ctypes.data, 2, 32, 8, 16, 128, 148,
@@ -142,19 +154,22 @@ def test_plan_rejects_page_size_and_small_buffers(qlib):
 
 def test_run_rejects_foreign_plan_and_null_pointers(qlib):
     _, lib = qlib
-    bogus = (ctypes.c_int64 * 16)(*([7] * 16))
+    bogus = (ctypes.c_int64 * PLAN_LEN)(*([7] * PLAN_LEN))
     fake = ctypes.c_void_p(0x100000)
     st = lib.qpkv_decode_run(bogus, fake, 1 << 20, fake, fake, fake, fake, fake, fake, 10, 16,
                              fake, 4, ctypes.c_float(0.1), fake, None, None, None)
     assert st == 1
     p = _plan(lib, [100, 200])
-    info = (ctypes.c_int64 * 16)(*p["info"])
+    info = (ctypes.c_int64 * PLAN_LEN)(*p["info"])
     st = lib.qpkv_decode_run(info, None, 1 << 20, fake, fake, fake, fake, fake, fake, 10, 16,
                              fake, 4, ctypes.c_float(0.1), fake, None, None, None)
     assert st == 1
     st = lib.qpkv_decode_run(info, fake, 16, fake, fake, fake, fake, fake, fake, 10, 16,
                              fake, 16, ctypes.c_float(0.1), fake, None, None, None)
     assert st == 3
+    assert lib.qpkv_decode_plan_set_kv_layout(info, 2) == 1          # unknown layout
+    assert lib.qpkv_decode_plan_set_kv_layout(bogus, 1) == 1         # not a plan
+    assert lib.qpkv_decode_plan_set_kv_layout(info, 1) == 0 and info[15] == 1
     misaligned = ctypes.c_void_p(0x100004)
     st = lib.qpkv_decode_run(info, fake, 1 << 30, fake, misaligned, fake, fake, fake, fake, 10,
                              16, fake, 16, ctypes.c_float(0.1), fake, None, None, None)

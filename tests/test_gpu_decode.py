@@ -16,10 +16,14 @@ FILL = 0x7F                # an E4M3 NaN code in every unwritten pool byte
 SCALE_FILL = np.float32("nan")
 
 
-def _dev_inputs(lib, wl, k, v):
+def _pool_shape(P, ps, H, D, layout):
+    return (P, H, ps, D) if layout == "HND" else (P, ps, H, D)
+
+
+def _dev_inputs(lib, wl, k, v, layout="NHD"):
     dev = "cuda"
     P, ps, H, D = wl.num_pages, wl.page_size, wl.Hkv, wl.D
-    k_pool = torch.full((P, ps, H, D), FILL, dtype=torch.uint8, device=dev)
+    k_pool = torch.full(_pool_shape(P, ps, H, D, layout), FILL, dtype=torch.uint8, device=dev)
     v_pool = torch.full_like(k_pool, FILL)
     ks = torch.full((P, ps, H), float("nan"), dtype=torch.float32, device=dev)
     vs = torch.full_like(ks, float("nan"))
@@ -30,11 +34,11 @@ def _dev_inputs(lib, wl, k, v):
     kt = torch.from_numpy(k).to(dev).to(torch.bfloat16)
     vt = torch.from_numpy(v).to(dev).to(torch.bfloat16)
     lib.write_cache_fp8(kt, vt, cu, bt, k_pool, v_pool, ks, vs, slot_mapping=slots,
-                        error_word=err)
+                        error_word=err, kv_layout=layout)
     return dict(k_pool=k_pool, v_pool=v_pool, ks=ks, vs=vs, bt=bt, slots=slots, err=err)
 
 
-def _oracle_cache(wl, k, v, reqs=None):
+def _oracle_cache(wl, k, v, reqs=None, layout="NHD"):
     """Oracle pools; with reqs given, a compact pool holding only their pages
     (and a block table remapped to it)."""
     lens = wl.lengths
@@ -56,11 +60,11 @@ def _oracle_cache(wl, k, v, reqs=None):
             parts_v.append(v[offs[b]:offs[b + 1]])
         kk, vv = np.concatenate(parts_k), np.concatenate(parts_v)
         cu = np.cumsum(lens[reqs])
-    shape = (max(P, 1), wl.page_size, wl.Hkv, wl.D)
-    fill = np.full(shape, FILL, np.uint8)
-    sfill = np.full(shape[:3], SCALE_FILL, np.float32)
+    fill = np.full(_pool_shape(max(P, 1), wl.page_size, wl.Hkv, wl.D, layout), FILL, np.uint8)
+    sfill = np.full((max(P, 1), wl.page_size, wl.Hkv), SCALE_FILL, np.float32)
     kp, vp, ksp, vsp, slots, _ = ocache.write_fp8_token_head(
-        kk, vv, cu, np.zeros(len(reqs), np.int64), bt, wl.page_size, fill, fill, sfill, sfill)
+        kk, vv, cu, np.zeros(len(reqs), np.int64), bt, wl.page_size, fill, fill, sfill, sfill,
+        layout=layout)
     return kp, vp, ksp, vsp, bt, reqs
 
 
@@ -68,10 +72,10 @@ def _u32(a):
     return np.ascontiguousarray(a).view(np.uint32)
 
 
-def _check_decode(lib, wl, reqs=None, check_pool_bytes=True, kv=None):
+def _check_decode(lib, wl, reqs=None, check_pool_bytes=True, kv=None, layout="NHD"):
     k, v = wl.kv_all() if kv is None else kv
-    d = _dev_inputs(lib, wl, k, v)
-    plan = lib.DecodePlan(wl.lengths, wl.Hq, wl.Hkv, wl.page_size, wl.D)
+    d = _dev_inputs(lib, wl, k, v, layout)
+    plan = lib.DecodePlan(wl.lengths, wl.Hq, wl.Hkv, wl.page_size, wl.D, kv_layout=layout)
     q = torch.from_numpy(wl.q).cuda().to(torch.bfloat16)
     out = torch.empty_like(q)
     lse = torch.empty(wl.B, wl.Hq, dtype=torch.float32, device="cuda")
@@ -80,9 +84,9 @@ def _check_decode(lib, wl, reqs=None, check_pool_bytes=True, kv=None):
     torch.cuda.synchronize()
     assert int(d["err"].item()) == 0
 
-    kp, vp, ksp, vsp, obt, reqs = _oracle_cache(wl, k, v, reqs)
+    kp, vp, ksp, vsp, obt, reqs = _oracle_cache(wl, k, v, reqs, layout)
     want_o, want_lse = oatt.paged_decode_fp8(wl.q[reqs], kp, vp, ksp, vsp, obt,
-                                             wl.lengths[reqs], wl.scale)
+                                             wl.lengths[reqs], wl.scale, layout=layout)
     got_o = bf16_to_f64(out)[reqs]
     got_lse = lse.cpu().numpy().astype(np.float64)[reqs]
     assert_attention_close(got_o, want_o)
@@ -135,14 +139,32 @@ def test_decode_tiny_gqa4_d64(lib):
     ([600, 31], 16, 16, 4, 128, 0),            # 32-token tiles would cross 16-token pages
 ])
 def test_decode_edge_shapes(lib, lengths, ps, Hq, Hkv, D, kind):
+    _, plan = _check_decode(lib, _edge_workload(lengths, ps, Hq, Hkv, D))
+    assert plan.kind == kind
+
+
+def _edge_workload(lengths, ps, Hq, Hkv, D):
     rng = np.random.default_rng(11)
     lengths = np.asarray(lengths, dtype=np.int32)
     bt, P = synth.page_tables(rng, lengths, ps, extra_pages=3)
-    wl = synth.DecodeWorkload(seed=11, B=len(lengths), Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
-                              lengths=lengths, block_table=bt, num_pages=P,
-                              q=synth.bf16_normal(rng, (len(lengths), Hq, D)),
-                              scale=1.0 / np.sqrt(D), workload_id=9)
-    _, plan = _check_decode(lib, wl)
+    return synth.DecodeWorkload(seed=11, B=len(lengths), Hq=Hq, Hkv=Hkv, D=D, page_size=ps,
+                                lengths=lengths, block_table=bt, num_pages=P,
+                                q=synth.bf16_normal(rng, (len(lengths), Hq, D)),
+                                scale=1.0 / np.sqrt(D), workload_id=9)
+
+
+@pytest.mark.parametrize("lengths,ps,Hq,Hkv,D,kind", [
+    ([0, 1, 127, 128, 129], 16, 4, 1, 64, 0),
+    ([300, 64, 17], 64, 8, 2, 128, 0),
+    ([700, 33, 256], 256, 16, 2, 128, 0),
+    ([1200, 5], 16, 32, 8, 128, 1),
+    ([777, 64], 32, 16, 8, 128, 1),            # a tile is half a page of 32
+    ([300, 64, 17, 1], 32, 16, 4, 128, 1),     # 4 kv heads: 32-token tiles, partial tails
+])
+def test_decode_hnd_layout(lib, lengths, ps, Hq, Hkv, D, kind):
+    """K/V pools [P, Hkv, page_size, D] (flashinfer's HND): the write places
+    each (token, head) row bit for bit and both decode kernels read it."""
+    _, plan = _check_decode(lib, _edge_workload(lengths, ps, Hq, Hkv, D), layout="HND")
     assert plan.kind == kind
 
 
