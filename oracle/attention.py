@@ -144,7 +144,7 @@ def paged_decode_fp8(q, k_pool, v_pool, k_scale_pool, v_scale_pool,
 
 def paged_prefill_int8(q8, q_scale, k_pool, k_scale, v_pool_bits, block_table,
                        cu_seqlens_q, seqlens_kv, scale, causal=True,
-                       rows=None):
+                       rows=None, v_scale=None):
     """Sage-style varlen prefill: INT8 Q and K with per-(sequence, 128-token
     block, head) scales, bf16 V, all K/V gathered through block_table.
 
@@ -152,6 +152,8 @@ def paged_prefill_int8(q8, q_scale, k_pool, k_scale, v_pool_bits, block_table,
     [P, ps, Hkv, D]; v_pool_bits uint16 (bf16) [P, ps, Hkv, D].
     Query block of query i is i // 128, key block of key j is j // 128.
     ``rows``: optional list of (token, head) pairs to compute (else all).
+    With ``v_scale`` (f32 [B, Hkv, D]) the V pool holds E4M3 codes and
+    V = code * v_scale[b, head, channel].
     Returns (O f64[T, H, D], lse f64[T, H]).
     """
     T, H, D = q8.shape
@@ -186,7 +188,10 @@ def paged_prefill_int8(q8, q_scale, k_pool, k_scale, v_pool_bits, block_table,
                     continue
             hk = h // G
             K = quant.dequant_int8(kp[prow, hk], k_scale[b, kblk, hk][:, None])
-            V = cache.bf16_value(vp[prow, hk])
+            if v_scale is None:
+                V = cache.bf16_value(vp[prow, hk])
+            else:
+                V = quant.dequant_fp8(vp[prow, hk], v_scale[b, hk][None, :])
             Q = quant.dequant_int8(q8[begin[b] + sel, h],
                                    q_scale[b, qblk[sel], h][:, None])
             o, l = attend_rows(Q, K, V, scale, None if vis is None else vis[sel])

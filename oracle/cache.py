@@ -23,6 +23,9 @@ Three modes:
                    "segment_mean" kernel): the per-(sequence, head) mean of
                    the rotated keys is subtracted before quantising, which
                    shifts every logit of a query row by the same amount.
+                   Optional FP8 V (Sage-style, for an FP8 P.V product): V
+                   -> E4M3 with one fp32 scale per (sequence, head,
+                   channel), the channel's absmax over the sequence / 448.
   mla_row          one 656-byte row per token: 512 INT8 nope codes with one
                    fp32 scale per 128-wide tile, the 64-wide rope part as
                    bf16, then the 4 scales (README, 参数说明 row key:
@@ -190,15 +193,38 @@ def k_smoothing_mean(k_rot, cu_seqlens_q):
     return km
 
 
+def v_channel_fp8(v, cu_seqlens_q):
+    """Per-(sequence, head, channel) E4M3 quantisation of V float32 [T, H, D]:
+    scale = absmax over the sequence's tokens / 448 (float32 division), codes
+    RNE-satfinite of v / scale.  Returns (codes u8 [T, H, D], scale f32
+    [B, H, D]); a channel that is all zero has scale 0 and zero codes."""
+    v = np.asarray(v, dtype=F32)
+    begin, end = seq_bounds(cu_seqlens_q)
+    T, H, D = v.shape
+    codes = np.zeros((T, H, D), dtype=np.uint8)
+    scales = np.zeros((len(begin), H, D), dtype=F32)
+    for b in range(len(begin)):
+        if end[b] == begin[b]:
+            continue
+        seg = v[begin[b]:end[b]]
+        s = quant.absmax_scale(np.max(np.abs(seg), axis=0), quant.FP8_QMAX)
+        scales[b] = s
+        codes[begin[b]:end[b]] = quant.quant_fp8(seg, s[None])
+    return codes, scales
+
+
 def write_int8_block128_rope(q, k, v, cu_seqlens_q, block_table, page_size,
-                             cos, sin, num_blocks, k_pool, v_pool_bits, smooth_k=False):
+                             cos, sin, num_blocks, k_pool, v_pool_bits, smooth_k=False,
+                             v_fp8=False):
     """Sage-style write: RoPE(q, k), block-INT8 Q and K, bf16 V into pages.
 
     q, k, v: float32 [T, H, D] (bf16 values).  Whole sequences (positions
     start at 0).  Returns (k_pool int8, v_pool_bits uint16, k_scale
     [B, nb, H], q8 int8 [T, H, D], q_scale [B, nb, H], slots), and with
     smooth_k the keys quantised are k_rot - k_mean (float32 subtraction)
-    and k_mean float32 [B, H, D] is appended.
+    and k_mean float32 [B, H, D] is appended; with v_fp8 the V pool holds
+    E4M3 codes (u8) and the per-channel scales float32 [B, H, D] are appended
+    last.
     """
     B = len(cu_seqlens_q)
     start = np.zeros(B, dtype=np.int64)
@@ -216,10 +242,16 @@ def write_int8_block128_rope(q, k, v, cu_seqlens_q, block_table, page_size,
     k_pool = k_pool.copy().reshape(P * ps, H, D)
     v_pool_bits = v_pool_bits.copy().reshape(P * ps, H, D)
     k_pool[slots] = k8
-    v_pool_bits[slots] = bf16_bits(v)
+    extra = (km,) if smooth_k else ()
+    if v_fp8:
+        v_codes, v_scale = v_channel_fp8(v, cu_seqlens_q)
+        v_pool_bits[slots] = v_codes
+        extra = extra + (v_scale,)
+    else:
+        v_pool_bits[slots] = bf16_bits(v)
     out = (k_pool.reshape(P, ps, H, D), v_pool_bits.reshape(P, ps, H, D),
            k_scale, q8, q_scale, slots)
-    return out + (km,) if smooth_k else out
+    return out + extra
 
 
 MLA_NOPE = 512

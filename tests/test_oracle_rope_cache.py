@@ -286,3 +286,63 @@ def test_k_smoothing_shrinks_int8_error_with_a_key_offset():
     assert errs[1] < 0.5 * errs[0], errs
     # the codes are those of the shifted keys
     assert np.all(np.abs(km[:, :, 120:128] - 12.0) < 0.6)
+
+
+def test_v_channel_fp8_scales_per_sequence_head_channel():
+    """FP8 V: one scale per (sequence, head, channel) from that channel's
+    absmax over the sequence (checked by explicit loops), the absmax element
+    coding to +-448, a channel scaled by a power of two keeping its codes,
+    and an all-zero channel giving scale 0 and zero codes."""
+    rng = np.random.default_rng(33)
+    lengths = [5, 9]
+    v = synth.bf16_normal(rng, (14, 2, 8))
+    v[5:, 1, 3] = 0.0
+    v[:5, 0, 2] *= np.float32(8.0)
+    cu = synth.inclusive_prefix(lengths)
+    codes, scales = cache.v_channel_fp8(v, cu)
+    for b, (lo, hi) in enumerate([(0, 5), (5, 14)]):
+        for h in range(2):
+            for c in range(8):
+                amax = max(abs(float(x)) for x in v[lo:hi, h, c])
+                assert scales[b, h, c] == np.float32(np.float32(amax) / np.float32(448.0))
+                if amax > 0:
+                    j = lo + int(np.argmax(np.abs(v[lo:hi, h, c])))
+                    assert e4m3.decode(codes[j, h, c]) == (448.0 if v[j, h, c] > 0 else -448.0)
+    assert scales[1, 1, 3] == 0 and np.all(codes[5:, 1, 3] == 0)
+    v2 = v.copy()
+    v2[:5, 0, 2] /= np.float32(8.0)
+    codes2, scales2 = cache.v_channel_fp8(v2, cu)
+    assert np.array_equal(codes2[:5, 0, 2], codes[:5, 0, 2])
+    assert scales2[0, 0, 2] * 8 == scales[0, 0, 2]
+
+
+def test_prefill_with_fp8_v_factors_the_channel_scale():
+    """O over FP8 V is (attention over the raw E4M3 values) times each
+    channel's scale: the per-channel scale factors out of P.V."""
+    from oracle import attention as oatt
+    rng = np.random.default_rng(34)
+    lengths = np.array([70, 150], np.int32)
+    T, H, D, ps = int(lengths.sum()), 2, 128, 64
+    q, k, v = (synth.bf16_normal(rng, (T, H, D)) for _ in range(3))
+    bt, P = synth.page_tables(rng, lengths, ps)
+    cu = synth.inclusive_prefix(lengths)
+    cos, sin = rope.cos_sin_table(256, D, 1.0e4)
+    out = cache.write_int8_block128_rope(q, k, v, cu, bt, ps, cos, sin, 2,
+                                         np.zeros((P, ps, H, D), np.int8),
+                                         np.zeros((P, ps, H, D), np.uint8), v_fp8=True)
+    kp, vp, ks, q8, qs, slots, vscale = out
+    scale = 1.0 / np.sqrt(D)
+    O, lse = oatt.paged_prefill_int8(q8, qs, kp, ks, vp, bt, cu, lengths, scale, v_scale=vscale)
+    ones = np.ones_like(vscale)
+    O1, lse1 = oatt.paged_prefill_int8(q8, qs, kp, ks, vp, bt, cu, lengths, scale, v_scale=ones)
+    b_of, _ = cache.token_positions(cu, np.zeros(2, np.int64))
+    assert np.allclose(O, O1 * vscale[b_of].astype(np.float64), rtol=1e-12, atol=1e-14)
+    assert np.array_equal(lse, lse1)
+    # and against the bf16 V it quantises: each value moves by at most 2^-4 of
+    # itself, so O by at most 2^-4 of the channel's absmax (448 * scale)
+    plain = cache.write_int8_block128_rope(q, k, v, cu, bt, ps, cos, sin, 2,
+                                           np.zeros((P, ps, H, D), np.int8),
+                                           np.zeros((P, ps, H, D), np.uint16))
+    Ob, _ = oatt.paged_prefill_int8(q8, qs, kp, ks, plain[1], bt, cu, lengths, scale)
+    bound = 2.0 ** -4 * 448.0 * vscale[b_of].astype(np.float64) * (1 + 1e-6)
+    assert np.all(np.abs(O - Ob) <= bound)
