@@ -582,7 +582,25 @@ def run_extras(device, iters=10):
     ms_r = _median_ms(fr, iters)
     out["int8_prefill_varlen"]["ragged_kv_ms"] = ms_r
     out["int8_prefill_varlen"]["ragged_kv_tflops"] = flops / (ms_r / 1e3) / 1e12
-    del k_pool, v_pool, q8p, qb, kb, vb, op, k_rag, v_rag
+    del k_rag, v_rag
+    # the same paged prefill with Sage-style FP8 V (per-channel scales) and an
+    # FP8 P.V product; the write quantises V with the same call
+    v8_pool = torch.zeros((wl.num_pages, wl.page_size, H, D), dtype=torch.uint8, device=device)
+    vsc = torch.zeros((len(L), H, D), dtype=torch.float32, device=device)
+    wsw = q.smooth_workspace(len(L), nb, H, device)
+    wr8 = lambda: q.write_cache_int8_block128_rope(qb, kb, vb, cu, bt, int(L.max()), cos, sin,
+                                                   k_pool, v8_pool, ks, q8p, qs, error_word=err,
+                                                   v_channel_scale=vsc, workspace=wsw)
+    wr8()
+    f8 = lambda: q.prefill_paged(q8p, qs, k_pool, ks, v8_pool, bt, cu, lk, causal=True, out=op,
+                                 workspace=wsp, error_word=err, v_scale=vsc)
+    for _ in range(3):
+        f8()
+    ms_8 = _median_ms(f8, iters)
+    out["int8_prefill_varlen"]["fp8_v_ms"] = ms_8
+    out["int8_prefill_varlen"]["fp8_v_tflops"] = flops / (ms_8 / 1e3) / 1e12
+    out["int8_prefill_varlen"]["fp8_v_write_cache_ms"] = _median_ms(wr8, iters)
+    del k_pool, v_pool, v8_pool, q8p, qb, kb, vb, op
 
     # MLA-absorb sparse decode
     d = synth.mla_sparse_device(0, device)

@@ -107,6 +107,11 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
  *     partial sums [B, num_blocks, Hkv, 128] (qpkv_smooth_workspace_bytes).
  *     Attention over the smoothed cache is unchanged (every logit of a query
  *     row moves by scale * q . m); its lse moves by the same amount.
+ *     With flags & QPKV_WRITE_V_FP8 (Sage-style FP8 V, for an FP8 P.V
+ *     product) v_pool holds E4M3 codes (u8 [P, page_size, Hkv, 128]) of
+ *     v / s, s[b, h, c] = absmax over sequence b of channel c of head h / 448
+ *     (float32 division; s = 0 gives zero codes), and s goes to
+ *     v_channel_scale (float [B, Hkv, 128]).  Both options use workspace.
  *  QPKV_WRITE_MLA_ROW  k = kv bf16 [T, 576] (512 nope || 64 rope), Hkv = 1:
  *     each token becomes one 656-byte row of the pool [P, page_size, 1, 656]:
  *     bytes [0, 512) INT8 nope codes (tile i = dims 128i..128i+127 has scale
@@ -137,6 +142,7 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
 /* qpkv_write_params.flags */
 #define QPKV_WRITE_SMOOTH_K 1   /* INT8 mode: subtract the per-(sequence, head) key mean */
 #define QPKV_WRITE_HND 2        /* FP8 mode: K/V pools [P, Hkv, page_size, D] (scales unchanged) */
+#define QPKV_WRITE_V_FP8 4      /* INT8 mode: V as E4M3 with one scale per (sequence, head, channel) */
 
 typedef struct qpkv_write_params {
   int32_t mode;
@@ -171,11 +177,13 @@ typedef struct qpkv_write_params {
   int32_t flags;          /* QPKV_WRITE_SMOOTH_K (INT8 mode) or 0 */
   int32_t pad0;
   float* k_mean;          /* INT8 + SMOOTH_K: out float [B, Hkv, 128] */
-  void* workspace;        /* INT8 + SMOOTH_K: scratch, 16-byte aligned */
+  void* workspace;        /* INT8 + SMOOTH_K or V_FP8: scratch, 16-byte aligned */
   size_t workspace_bytes;
+  float* v_channel_scale; /* INT8 + V_FP8: out float [B, Hkv, 128] */
 } qpkv_write_params;
 
-/* Scratch bytes of an INT8 write with QPKV_WRITE_SMOOTH_K (0 for negative sizes). */
+/* Scratch bytes of an INT8 write with QPKV_WRITE_SMOOTH_K and / or
+ * QPKV_WRITE_V_FP8 (0 for negative sizes). */
 size_t qpkv_smooth_workspace_bytes(int32_t num_seqs, int32_t num_blocks, int32_t num_heads_kv);
 
 qpkv_status qpkv_write_cache(const qpkv_write_params* params, void* stream);
@@ -408,6 +416,10 @@ typedef struct qpkv_prefill_params {
   void* workspace;
   size_t workspace_bytes;
   int32_t* error_word;
+  const float* v_scale;   /* NULL: v_pool is bf16.  Else v_pool holds E4M3 codes (u8, shaped
+                             like k_pool) and v_scale [B, Hkv, 128] the per-(sequence, head,
+                             channel) scales of QPKV_WRITE_V_FP8; P.V is then an FP8 product
+                             with P as two E4M3 terms (hi + lo, about 8 significant bits) */
 } qpkv_prefill_params;
 
 /* Device workspace bytes qpkv_prefill_paged needs for num_seqs sequences of

@@ -28,6 +28,7 @@ WRITE_INT8_BLOCK128_ROPE = 1
 WRITE_MLA_ROW = 2
 WRITE_SMOOTH_K = 1          # qpkv_write_params.flags
 WRITE_HND = 2
+WRITE_V_FP8 = 4
 PLAN_INFO_LEN = 24
 KV_LAYOUTS = {"NHD": 0, "HND": 1}   # K/V pool layouts of the FP8 decode path
 
@@ -64,7 +65,7 @@ class WriteParams(ctypes.Structure):
             "k_pool", "v_pool", "k_scale_pool", "v_scale_pool", "k_block_scale", "q_out",
             "q_block_scale", "slot_mapping", "error_word")] + [
         ("flags", _i32), ("pad0", _i32), ("k_mean", _p), ("workspace", _p),
-        ("workspace_bytes", ctypes.c_size_t)]
+        ("workspace_bytes", ctypes.c_size_t), ("v_channel_scale", _p)]
 
 
 
@@ -77,7 +78,7 @@ class PrefillParams(ctypes.Structure):
         (n, _p) for n in (
             "cu_seqlens_q", "seqlens_kv", "cu_seqlens_kv", "block_table", "q", "q_block_scale", "k_pool",
             "k_block_scale", "v_pool", "o", "lse", "workspace")] + [
-        ("workspace_bytes", ctypes.c_size_t), ("error_word", _p)]
+        ("workspace_bytes", ctypes.c_size_t), ("error_word", _p), ("v_scale", _p)]
 
 
 class MlaParams(ctypes.Structure):
@@ -245,20 +246,22 @@ def smooth_workspace(num_seqs, num_blocks, num_heads_kv, device="cuda"):
 def write_cache_int8_block128_rope(q, k, v, cu_seqlens, block_table, max_seqlen, rope_cos,
                                    rope_sin, k_pool, v_pool, k_block_scale, q_out,
                                    q_block_scale, slot_mapping=None, error_word=None,
-                                   k_mean=None, workspace=None):
+                                   k_mean=None, workspace=None, v_channel_scale=None):
     """Sage-style prefill write: RoPE(q, k), INT8 per-(sequence, 128-token
     block, head) Q and K, bf16 V into pages.  q/k/v bf16 [T, H, 128];
     k_pool int8 [P, ps, Hkv, 128]; v_pool bf16 [P, ps, Hkv, 128];
     k_block_scale [B, nb, Hkv]; q_out int8 [T, Hq, 128]; q_block_scale [B, nb, Hq].
     With k_mean (fp32 [B, Hkv, 128], filled) the keys are smoothed: their
-    per-(sequence, head) mean is subtracted before quantising."""
+    per-(sequence, head) mean is subtracted before quantising.  With
+    v_channel_scale (fp32 [B, Hkv, 128], filled) V is stored as E4M3 codes
+    (v_pool uint8) with one scale per (sequence, head, channel)."""
     torch = _torch()
     lib = load()
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
     _need(k_pool, "k_pool", torch.int8, 4)
-    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.uint8 if v_channel_scale is not None else torch.bfloat16, 4)
     _need(q_out, "q_out", torch.int8, 3)
     _need(k_block_scale, "k_block_scale", torch.float32, 3)
     _need(q_block_scale, "q_block_scale", torch.float32, 3)
@@ -278,14 +281,17 @@ def write_cache_int8_block128_rope(q, k, v, cu_seqlens, block_table, max_seqlen,
     p.k_block_scale, p.q_out, p.q_block_scale = _ptr(k_block_scale), _ptr(q_out), _ptr(q_block_scale)
     p.slot_mapping = _ptr(slot_mapping)
     p.error_word = _ptr(error_word)
-    if k_mean is not None:
-        _need(k_mean, "k_mean", torch.float32, 3)
-        if tuple(k_mean.shape) != (p.num_seqs, Hkv, D):
-            raise ValueError("k_mean must be [B, Hkv, 128]")
+    for name, t in (("k_mean", k_mean), ("v_channel_scale", v_channel_scale)):
+        if t is not None:
+            _need(t, name, torch.float32, 3)
+            if tuple(t.shape) != (p.num_seqs, Hkv, D):
+                raise ValueError(f"{name} must be [B, Hkv, 128]")
+    if k_mean is not None or v_channel_scale is not None:
         if workspace is None:
             workspace = smooth_workspace(p.num_seqs, p.num_blocks, Hkv, k.device)
-        p.flags = WRITE_SMOOTH_K
-        p.k_mean = _ptr(k_mean)
+        p.flags = (WRITE_SMOOTH_K if k_mean is not None else 0) | (
+            WRITE_V_FP8 if v_channel_scale is not None else 0)
+        p.k_mean, p.v_channel_scale = _ptr(k_mean), _ptr(v_channel_scale)
         p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(int8)")
 
@@ -501,19 +507,21 @@ def prefill_workspace(num_seqs, num_tokens, num_heads_q, device="cuda"):
 
 def prefill_paged(q8, q_block_scale, k_pool, k_block_scale, v_pool, block_table, cu_seqlens_q,
                   seqlens_kv, sm_scale=None, causal=True, out=None, lse=None, workspace=None,
-                  error_word=None, cu_seqlens_kv=None):
+                  error_word=None, cu_seqlens_kv=None, v_scale=None):
     """Varlen prefill with INT8 Q/K (block-128 scales) and bf16 V: q8 int8
     [T, Hq, 128]; a paged cache k_pool int8 / v_pool bf16 [P, ps, Hkv, 128]
     with block_table and seqlens_kv, or (cu_seqlens_kv given) ragged K/V
     [T_kv, Hkv, 128] with inclusive prefix sums of the kv lengths; scales
     fp32 [B, NB, H]; returns bf16 O [T, Hq, 128] (``lse`` fp32 [T, Hq]
-    filled when given)."""
+    filled when given).  With v_scale (fp32 [B, Hkv, 128]) v_pool holds
+    E4M3 codes (uint8) and P.V runs in FP8."""
     torch = _torch()
     lib = load()
     ragged = cu_seqlens_kv is not None
     _need(q8, "q8", torch.int8, 3)
     _need(k_pool, "k_pool", torch.int8, 3 if ragged else 4)
-    _need(v_pool, "v_pool", torch.bfloat16, 3 if ragged else 4)
+    _need(v_pool, "v_pool", torch.uint8 if v_scale is not None else torch.bfloat16,
+          3 if ragged else 4)
     _need(q_block_scale, "q_block_scale", torch.float32, 3)
     _need(k_block_scale, "k_block_scale", torch.float32, 3)
     _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
@@ -558,6 +566,11 @@ def prefill_paged(q8, q_block_scale, k_pool, k_block_scale, v_pool, block_table,
     prm.o, prm.lse = _ptr(out), _ptr(lse)
     prm.workspace, prm.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     prm.error_word = _ptr(error_word)
+    if v_scale is not None:
+        _need(v_scale, "v_scale", torch.float32, 3)
+        if tuple(v_scale.shape) != (B, Hkv, D):
+            raise ValueError("v_scale must be [B, Hkv, 128]")
+        prm.v_scale = _ptr(v_scale)
     _check(lib.qpkv_prefill_paged(ctypes.byref(prm), _stream()), "qpkv_prefill_paged")
     return out
 

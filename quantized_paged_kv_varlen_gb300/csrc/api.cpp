@@ -251,10 +251,11 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
         return QPKV_ERR_INVALID_ARG;
       if (p->num_blocks < (p->max_seqlen + 127) / 128 || p->rope_max_pos < p->max_seqlen)
         return QPKV_ERR_INVALID_ARG;
-      if (p->flags & ~QPKV_WRITE_SMOOTH_K) return QPKV_ERR_UNSUPPORTED;
-      if (p->flags & QPKV_WRITE_SMOOTH_K) {
-        if (p->k_mean == nullptr || p->workspace == nullptr || !aligned16(p->workspace))
-          return QPKV_ERR_INVALID_ARG;
+      if (p->flags & ~(QPKV_WRITE_SMOOTH_K | QPKV_WRITE_V_FP8)) return QPKV_ERR_UNSUPPORTED;
+      if ((p->flags & QPKV_WRITE_V_FP8) && p->v_channel_scale == nullptr) return QPKV_ERR_INVALID_ARG;
+      if (p->flags & (QPKV_WRITE_SMOOTH_K | QPKV_WRITE_V_FP8)) {
+        if ((p->flags & QPKV_WRITE_SMOOTH_K) && p->k_mean == nullptr) return QPKV_ERR_INVALID_ARG;
+        if (p->workspace == nullptr || !aligned16(p->workspace)) return QPKV_ERR_INVALID_ARG;
         if (p->workspace_bytes <
             qpkv_smooth_workspace_bytes(p->num_seqs, p->num_blocks, p->num_heads_kv))
           return QPKV_ERR_WORKSPACE_TOO_SMALL;
@@ -434,7 +435,9 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
 
 size_t qpkv_smooth_workspace_bytes(int32_t num_seqs, int32_t num_blocks, int32_t num_heads_kv) {
   if (num_seqs < 0 || num_blocks < 0 || num_heads_kv < 0) return 0;
-  return static_cast<size_t>(num_seqs) * num_blocks * num_heads_kv * 128 * sizeof(long long);
+  // int64 K sums, then float V channel maxima
+  return static_cast<size_t>(num_seqs) * num_blocks * num_heads_kv * 128 *
+         (sizeof(long long) + sizeof(float));
 }
 
 size_t qpkv_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads_q) {

@@ -88,6 +88,7 @@ struct PArgs {
   const int32_t* lk;    // [B]
   const int32_t* bt;    // [B, bt_stride]
   const int8_t* q8;     // [T, Hq, D]
+  const float* sv;      // FP8 V: channel scales [B, Hkv, D]
   const float* sq;      // [B, NB, Hq]
   const float* sk;      // [B, NB, Hkv]
   uint16_t* o;          // bf16 [T, Hq, D]
@@ -348,6 +349,9 @@ struct TileWalk {
   }
 };
 
+// V8: V is E4M3 with per-(sequence, head, channel) scales and P.V runs as
+// an FP8 product (P as two E4M3 terms hi + lo); else V is bf16 and P bf16.
+template <bool V8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_int8_kernel(const __grid_constant__ CUtensorMap q_map,
                         const __grid_constant__ CUtensorMap k_map,
@@ -527,10 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waits; rows of a V tile past L_kv (the unwritten rest of a sequence's
     // last page, whose bits may be NaN) are zeroed first, since P = 0 there
     // does not cancel a NaN.  Lane 0 issues the MMAs.
-    const uint32_t idesc_pv = make_idesc(kFmtBF16, kFmtBF16, 0, 1, kT, kD);
-    // MN-major V: two 64-column atoms 16 KB apart (leading byte offset),
-    // 16 key rows (2 KB) per K = 16 step
-    const uint64_t vdesc0 = make_smem_desc(smem_u32(smem + kOffV), kHalf, 1024, kSwizzle128B);
+    const uint32_t idesc_pv = V8 ? make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, kT, kD)
+                                 : make_idesc(kFmtBF16, kFmtBF16, 0, 1, kT, kD);
+    // MN-major V.  bf16: two 64-column atoms 16 KB apart (leading byte
+    // offset), 16 key rows (2 KB) per K = 16 step.  E4M3: one 128-byte atom
+    // per key row, 32 key rows (4 KB) per K = 32 step
+    const uint64_t vdesc0 = V8 ? make_smem_desc(smem_u32(smem + kOffV), 0, 1024, kSwizzle128B)
+                               : make_smem_desc(smem_u32(smem + kOffV), kHalf, 1024, kSwizzle128B);
     Items it;
     it.start(a);
     TileWalk vw;
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (!mbar_test_wait(&sh.v_empty[s], par)) {
           return true;
         }
-        mbar_arrive_expect_tx(&sh.v_full[s], kH16Tile);
+        mbar_arrive_expect_tx(&sh.v_full[s], V8 ? kI8Tile : kH16Tile);
         const Tile& t = vw.t;
         cp_async_wait_but_one();
 #pragma unroll 1
@@ -560,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = page_row(vw.t, sh.vring, i, vw.j);
           uint8_t* dst = smem + kOffV + s * kH16Tile + i * a.rows_box * 128;
           tma_load_3d(dst, &v_map, &sh.v_full[s], 0, t.hk, row);
-          tma_load_3d(dst + kHalf, &v_map, &sh.v_full[s], 64, t.hk, row);
+          if (!V8) tma_load_3d(dst + kHalf, &v_map, &sh.v_full[s], 64, t.hk, row);
         }
         ++vis;
         vw.next(a);
@@ -604,8 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* vt = smem + kOffV + s * kH16Tile;
         const int r0 = t.Lk - j * kT;
         if (r0 < kT) {
-          for (int i = lane; i < (kT - r0) * 16; i += 32) {
-            const int row = r0 + (i >> 4), c = i & 15;
+          constexpr int kRowChunks = V8 ? 8 : 16;   // 16-byte pieces per key row
+          for (int i = lane; i < (kT - r0) * kRowChunks; i += 32) {
+            const int row = r0 + i / kRowChunks, c = i % kRowChunks;
             *reinterpret_cast<uint4*>(vt + (c >> 3) * kHalf + row * 128 + (c & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
@@ -615,11 +623,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           tc_fence_after_sync();
           const uint64_t db = vdesc0 + static_cast<uint64_t>((s * kH16Tile) >> 4);
+          if (V8) {
+            // key chunk q (32 keys): the hi terms of half q / 2 sit in its S
+            // columns [64 (q / 2) + 8 (q % 2), +8), the lo terms 16 further
 #pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            tc_mma_f16_tmem_a(tmem + kColO, tmem + kColS + sb * kT + (kk >> 2) * 64 + 8 * (kk & 3),
-                              db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const int q = kk & 3, term = kk >> 2;
+              tc_mma_f8_tmem_a(tmem + kColO,
+                               tmem + kColS + sb * kT + (q >> 1) * 64 + (q & 1) * 8 + term * 16,
+                               db + static_cast<uint64_t>((q * 32 * 128) >> 4), idesc_pv,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              tc_mma_f16_tmem_a(tmem + kColO, tmem + kColS + sb * kT + (kk >> 2) * 64 + 8 * (kk & 3),
+                                db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+          }
           tc_commit(&sh.v_empty[s]);
           tc_commit(&sh.pv_done[sb]);
           if (j == t.nkv - 1) tc_commit(&sh.o_full);
@@ -767,18 +788,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(srow + 64 * half + 32 * c2, v);
           tmem_ld_wait();
           const int lim2 = climit - 32 * c2;
-          uint32_t pk[16];
+          if (V8) {
+            // P as two E4M3 terms (built in f16x2), four keys per column:
+            // hi to columns [64 half + 8 c2, +8), lo 16 columns further
+            uint32_t ph[8], pl[8];
 #pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const float x0 = 2 * w <= lim2 ? __uint_as_float(v[2 * w]) : -INFINITY;
-            const float x1 = 2 * w + 1 <= lim2 ? __uint_as_float(v[2 * w + 1]) : -INFINITY;
-            const float p0 = fast_exp2(fmaf(x0, sc24, nm));
-            const float p1 = fast_exp2(fmaf(x1, sc24, nm));
-            l += p0 + p1;
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int w = 0; w < 8; ++w) {
+              float p[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x = 4 * w + e <= lim2 ? __uint_as_float(v[4 * w + e]) : -INFINITY;
+                p[e] = fast_exp2(fmaf(x, sc24, nm));
+              }
+              l += (p[0] + p[1]) + (p[2] + p[3]);
+              const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
+              const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
+              const uint16_t h01 = f16x2_to_e4m3x2(f01);
+              const uint16_t h23 = f16x2_to_e4m3x2(f23);
+              const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(f01, e4m3x2_to_f16x2(h01)));
+              const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(f23, e4m3x2_to_f16x2(h23)));
+              ph[w] = h01 | (static_cast<uint32_t>(h23) << 16);
+              pl[w] = l01 | (static_cast<uint32_t>(l23) << 16);
+            }
+            tmem_st8(srow + 64 * half + 8 * c2, ph);
+            tmem_st8(srow + 64 * half + 16 + 8 * c2, pl);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const float x0 = 2 * w <= lim2 ? __uint_as_float(v[2 * w]) : -INFINITY;
+              const float x1 = 2 * w + 1 <= lim2 ? __uint_as_float(v[2 * w + 1]) : -INFINITY;
+              const float p0 = fast_exp2(fmaf(x0, sc24, nm));
+              const float p1 = fast_exp2(fmaf(x1, sc24, nm));
+              l += p0 + p1;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            tmem_st16(srow + 64 * half + 16 * c2, pk);
           }
-          tmem_st16(srow + 64 * half + 16 * c2, pk);
         }
         tmem_st_wait();
         tc_fence_before_sync();
@@ -810,6 +857,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld32(orow + 32 * c2, v);
         tmem_ld_wait();
+        if (V8) {
+          // the channel scales of this half's 32 columns (same for all rows)
+          const float* svp = a.sv + (static_cast<size_t>(t.b) * a.Hkv + t.hk) * kD + 64 * half + 32 * c2;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(__uint_as_float(v[i]) * __ldg(svp + i));
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1023,12 +1077,16 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   const uint32_t qbox[3] = {kD, 1u, kT};
   const uint32_t kbox[3] = {kD, 1u, static_cast<uint32_t>(rows_box)};
   const uint32_t vbox[3] = {64u, 1u, static_cast<uint32_t>(rows_box)};
+  // FP8 V (v_scale given): E4M3 codes shaped like K, one 128-byte box row
+  const bool v8 = p.v_scale != nullptr;
   if (encode_tensor_map(&qm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(p.q), qdims, qstr,
                         qbox, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tensor_map(&km, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(p.k_pool), kdims,
                         kstr, kbox, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-      encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.v_pool), kdims,
-                        vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS) {
+      (v8 ? encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(p.v_pool),
+                              kdims, kstr, kbox, CU_TENSOR_MAP_SWIZZLE_128B)
+          : encode_tensor_map(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.v_pool),
+                              kdims, vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B)) != CUDA_SUCCESS) {
     *status = QPKV_ERR_CUDA;
     return cudaErrorInvalidValue;
   }
@@ -1036,6 +1094,7 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   a.B = p.num_seqs;
   a.T = p.num_tokens;
   a.q8 = static_cast<const int8_t*>(p.q);
+  a.sv = p.v_scale;
   a.Hq = p.num_heads_q;
   a.Hkv = p.num_heads_kv;
   a.G = p.num_heads_q / p.num_heads_kv;
@@ -1060,12 +1119,13 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
   a.lse = p.lse;
   a.ws = static_cast<const int32_t*>(p.workspace);
   a.err = p.error_word;
-  e = cudaFuncSetAttribute(prefill_int8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto* kern = v8 ? prefill_int8_kernel<true> : prefill_int8_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  prefill_int8_kernel<<<sms, kThreads, kSmem, stream>>>(qm, km, vm, a);
+  kern<<<sms, kThreads, kSmem, stream>>>(qm, km, vm, a);
   return cudaGetLastError();
 }
 }  // namespace qpkv

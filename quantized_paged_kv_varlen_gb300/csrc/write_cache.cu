@@ -218,6 +218,23 @@ __global__ void __launch_bounds__(256) k_block_sum_kernel(
     partial[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + d] = acc + part[d];
 }
 
+// FP8 V, pass 1: per (sequence, 128-token block, kv head) the largest |v|
+// of each channel over the block's tokens (a maximum: order-free).
+__global__ void __launch_bounds__(128) v_block_max_kernel(
+    int Hkv, int num_blocks, const int32_t* __restrict__ cu, const uint16_t* __restrict__ v,
+    float* __restrict__ vmax) {
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  const int begin = seq_begin(cu, b);
+  const int L = __ldg(cu + b) - begin;
+  if (blk * kBlk >= L) return;
+  const int n = min(kBlk, L - blk * kBlk);
+  float m = 0.f;
+  for (int r = 0; r < n; ++r)
+    m = fmaxf(m, fabsf(bf16_bits_to_float(
+                     __ldg(v + (static_cast<size_t>(begin + blk * kBlk + r) * Hkv + h) * 128 + d))));
+  vmax[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + d] = m;
+}
+
 __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     int B, int Hq, int Hkv, int ps, int num_pages, int bt_stride, int num_blocks,
     const int32_t* __restrict__ cu, const int32_t* __restrict__ bt,
@@ -226,10 +243,11 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     const float* __restrict__ sin_t, int8_t* __restrict__ k_pool, uint16_t* __restrict__ v_pool,
     float* __restrict__ k_bscale, int8_t* __restrict__ q_out, float* __restrict__ q_bscale,
     int32_t* __restrict__ slots, const long long* __restrict__ partial, float* __restrict__ k_mean,
-    int max_pos, int* err) {
+    const float* __restrict__ vmax, float* __restrict__ v_cscale, int max_pos, int* err) {
   constexpr int D = 128;
   __shared__ float red[8];
   __shared__ float km[D];
+  __shared__ float vsc[D];
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int begin = seq_begin(cu, b);
   const int L = __ldg(cu + b) - begin;
@@ -251,6 +269,20 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
           __double2float_rn(__ll2double_rn(sum) / (static_cast<double>(L) * static_cast<double>(kMeanOne)));
       km[threadIdx.x] = m;
       if (blk == 0) k_mean[(static_cast<size_t>(b) * Hkv + h) * D + threadIdx.x] = m;
+    }
+    __syncthreads();
+  }
+  const bool v8 = vmax != nullptr && h < Hkv;
+  if (v8) {
+    // FP8 V, pass 2: the channel's absmax over the sequence -> scale / 448
+    if (threadIdx.x < D) {
+      float amax = 0.f;
+      const int nsum = min(nblk, static_cast<int>(gridDim.x));
+      for (int j = 0; j < nsum; ++j)
+        amax = fmaxf(amax, vmax[((static_cast<size_t>(b) * num_blocks + j) * Hkv + h) * D + threadIdx.x]);
+      const float sc = __fdiv_rn(amax, 448.0f);
+      vsc[threadIdx.x] = sc;
+      if (blk == 0) v_cscale[(static_cast<size_t>(b) * Hkv + h) * D + threadIdx.x] = sc;
     }
     __syncthreads();
   }
@@ -277,12 +309,38 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     __shared__ __align__(16) int8_t sink[2 * D];
     rope_quant_block(src, valid, pos, half, cos_t, sin_t, smooth ? km : nullptr, ok ? dst : sink,
                      k_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hkv + h, red);
-    if (ok) {
+    if (ok && !v8) {
       const uint4* vs = reinterpret_cast<const uint4*>(v + (static_cast<size_t>(t) * Hkv + h) * D +
                                                        half * 64);
       uint4* vd = reinterpret_cast<uint4*>(v_pool + (slot * Hkv + h) * D + half * 64);
 #pragma unroll
       for (int c = 0; c < 8; ++c) vd[c] = vs[c];
+    } else if (ok) {
+      // E4M3 codes of v / channel scale (float32 division), this thread's 64
+      // channels; the pool holds one byte per element
+      const uint16_t* vs = v + (static_cast<size_t>(t) * Hkv + h) * D + half * 64;
+      uint8_t* vd = reinterpret_cast<uint8_t*>(v_pool) + (slot * Hkv + h) * D + half * 64;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float xa[8], xb[8];
+        load_bf16x8(vs + 16 * g, xa);
+        load_bf16x8(vs + 16 * g + 8, xb);
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int c = 16 * g + 4 * e + k;
+            const float sc = vsc[half * 64 + c];
+            const float xv = 4 * e + k < 8 ? xa[4 * e + k] : xb[4 * e + k - 8];
+            const uint32_t code = sc != 0.f ? f32_to_e4m3(__fdiv_rn(xv, sc)) : 0u;
+            word |= code << (8 * k);
+          }
+          w[e] = word;
+        }
+        *reinterpret_cast<uint4*>(vd + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
 }
@@ -455,6 +513,17 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
       if (nblk == 0) return cudaSuccess;
       const int hmax = p.num_heads_q > p.num_heads_kv ? p.num_heads_q : p.num_heads_kv;
       long long* partial = nullptr;
+      float* vmax = nullptr;
+      if (p.flags & QPKV_WRITE_V_FP8) {
+        // after the K sums in the scratch: float [B, num_blocks, Hkv, 128]
+        vmax = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) +
+                                        static_cast<size_t>(p.num_seqs) * p.num_blocks *
+                                            p.num_heads_kv * 128 * sizeof(long long));
+        v_block_max_kernel<<<dim3(nblk, p.num_heads_kv, p.num_seqs), 128, 0, stream>>>(
+            p.num_heads_kv, p.num_blocks, p.cu_seqlens_q, static_cast<const uint16_t*>(p.v), vmax);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
       if (p.flags & QPKV_WRITE_SMOOTH_K) {
         partial = static_cast<long long*>(p.workspace);
         k_block_sum_kernel<<<dim3(nblk, p.num_heads_kv, p.num_seqs), threads, 0, stream>>>(
@@ -471,7 +540,7 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
           static_cast<const uint16_t*>(p.k), static_cast<const uint16_t*>(p.v), p.rope_cos,
           p.rope_sin, static_cast<int8_t*>(p.k_pool), static_cast<uint16_t*>(p.v_pool),
           p.k_block_scale, static_cast<int8_t*>(p.q_out), p.q_block_scale, p.slot_mapping,
-          partial, p.k_mean, p.rope_max_pos, p.error_word);
+          partial, p.k_mean, vmax, p.v_channel_scale, p.rope_max_pos, p.error_word);
       return cudaGetLastError();
     }
     case QPKV_WRITE_MLA_ROW: {

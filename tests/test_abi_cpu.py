@@ -215,7 +215,12 @@ def test_write_cache_rejects_before_launch(qlib):
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
     p.k_mean, p.workspace, p.workspace_bytes = fake, fake, 8
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 3
-    assert lib.qpkv_smooth_workspace_bytes(2, 1, 1) == 2 * 128 * 8
+    assert lib.qpkv_smooth_workspace_bytes(2, 1, 1) == 2 * 128 * (8 + 4)
+    p.flags, p.k_mean = 4, None      # FP8 V: needs the channel-scale output
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
+    p.v_channel_scale = fake         # ... and the scratch
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 3
+    p.v_channel_scale = None
     p.flags = 0
     p.rope_cos, p.rope_sin, p.rope_max_pos = None, None, 0
     p.mode = 2                       # MLA needs head_dim 576

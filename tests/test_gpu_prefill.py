@@ -8,7 +8,8 @@ from oracle import attention as oatt
 from oracle import cache as ocache
 from oracle import rope as orope
 from quantized_paged_kv_varlen_gb300 import synth
-from tests.gpu_util import ATOL_P_BF16, assert_attention_close, assert_lse_close, bf16_to_f64
+from tests.gpu_util import (ATOL_P_BF16, ATOL_P_FP8, REL_L2_FP8_P, assert_attention_close,
+                            assert_lse_close, bf16_to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -310,3 +311,95 @@ def test_prefill_full_size_sampled(lib):
         got_l = lse[torch.from_numpy(begin[b] + ti).long(), torch.from_numpy(hi).long()]
         assert_attention_close(got_o, want_o[ti, hi], atol=ATOL_P_BF16)
         assert_lse_close(got_l.cpu().numpy().astype(np.float64), want_lse[ti, hi])
+
+
+# ------------------------------------------------------------------ FP8 V
+
+def _fp8v_case(seed, Lq, Lk, Hq, Hkv, ps):
+    """INT8 Q/K as in _random_case, V as E4M3 codes with per-(sequence, head,
+    channel) scales from the oracle's FP8-V quantiser of bf16 draws."""
+    c = _random_case(seed, Lq, Lk, Hq, Hkv, ps)
+    rng = np.random.default_rng((seed, 78))
+    Lk = np.asarray(Lk, np.int32)
+    v = synth.bf16_normal(rng, (int(Lk.sum()), Hkv, 128))
+    codes, vscale = ocache.v_channel_fp8(v, synth.inclusive_prefix(Lk))
+    P, ps_, _, _ = c["k_pool"].shape
+    vpool = np.full((P, ps_, Hkv, 128), 0x7F, np.uint8)     # NaN codes off the written rows
+    begin = np.concatenate([[0], np.cumsum(Lk)[:-1]])
+    for b, L in enumerate(Lk):
+        rows = ocache.slot_mapping(np.array([int(L)]), np.zeros(1, np.int64), c["bt"][b:b + 1], ps_)
+        vpool.reshape(P * ps_, Hkv, 128)[rows] = codes[begin[b]:begin[b] + int(L)]
+    c["v_codes"], c["vscale"] = vpool, vscale
+    return c
+
+
+@pytest.mark.parametrize("Lq,Lk,Hq,Hkv,ps,causal", [
+    ([1, 130, 300], [1, 130, 300], 2, 2, 64, True),
+    ([77, 128, 1], [300, 128, 513], 4, 1, 32, True),       # cached prefix, GQA 4:1
+    ([130, 257], [390, 100], 2, 1, 128, False),
+    ([640, 520], [640, 520], 1, 1, 16, True),
+])
+def test_prefill_fp8_v(lib, Lq, Lk, Hq, Hkv, ps, causal):
+    """FP8 V with channel scales: P.V as an FP8 product (P in two E4M3
+    terms) against the oracle on the same codes."""
+    c = _fp8v_case(sum(Lq) + ps, Lq, Lk, Hq, Hkv, ps)
+    T = c["q8"].shape[0]
+    lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = lib.prefill_paged(_t(c["q8"]), _t(c["qs"]), _t(c["k_pool"]), _t(c["ks"]), _t(c["v_codes"]),
+                            _t(c["bt"]), _t(c["cu"]), _t(c["Lk"]), causal=causal, lse=lse,
+                            error_word=err, v_scale=_t(c["vscale"]))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want_o, want_lse = oatt.paged_prefill_int8(c["q8"], c["qs"], c["k_pool"], c["ks"], c["v_codes"],
+                                               c["bt"], c["cu"], c["Lk"], 1.0 / np.sqrt(128.0), causal,
+                                               v_scale=c["vscale"])
+    assert_attention_close(bf16_to_f64(out), want_o, rel=REL_L2_FP8_P, atol=ATOL_P_FP8)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
+
+
+def test_write_cache_int8_v_fp8_bit_exact_and_ragged_prefill(lib):
+    """The write's FP8 V (codes and channel scales) bit-exact against the
+    oracle, then a ragged (packed K/V) prefill over those codes."""
+    rng = np.random.default_rng(61)
+    lengths = np.array([200, 1, 333], dtype=np.int32)
+    T, Hq, Hkv, D, ps = int(lengths.sum()), 4, 2, 128, 64
+    q = synth.bf16_normal(rng, (T, Hq, D))
+    k = synth.bf16_normal(rng, (T, Hkv, D))
+    v = synth.bf16_normal(rng, (T, Hkv, D))
+    v[:, 1, 5] = 0.0                                           # an all-zero channel
+    bt, P = synth.page_tables(rng, lengths, ps)
+    cos, sin = orope.cos_sin_table(512, 128, 1.0e4)
+    B, nb = 3, 3
+    k_pool = torch.zeros((P, ps, Hkv, D), dtype=torch.int8, device=DEV)
+    v_pool = torch.full((P, ps, Hkv, D), 0x7F, dtype=torch.uint8, device=DEV)
+    ks = torch.zeros((B, nb, Hkv), dtype=torch.float32, device=DEV)
+    qs = torch.zeros((B, nb, Hq), dtype=torch.float32, device=DEV)
+    q8 = torch.zeros((T, Hq, D), dtype=torch.int8, device=DEV)
+    vsc = torch.full((B, Hkv, D), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cu = synth.inclusive_prefix(lengths)
+    lib.write_cache_int8_block128_rope(
+        _t(q).to(torch.bfloat16), _t(k).to(torch.bfloat16), _t(v).to(torch.bfloat16), _t(cu), _t(bt),
+        333, _t(cos), _t(sin), k_pool, v_pool, ks, q8, qs, error_word=err, v_channel_scale=vsc)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kp, vp, kscale, q8w, qscale, slots, vscw = ocache.write_int8_block128_rope(
+        q, k, v, cu, bt, ps, cos, sin, nb, np.zeros((P, ps, Hkv, D), np.int8),
+        np.full((P, ps, Hkv, D), 0x7F, np.uint8), v_fp8=True)
+    assert np.array_equal(_u32(vsc.cpu().numpy()), _u32(vscw))
+    got_v = v_pool.cpu().numpy().reshape(P * ps, Hkv, D)
+    assert np.array_equal(got_v[slots], vp.reshape(P * ps, Hkv, D)[slots])
+    assert np.array_equal(q8.cpu().numpy(), q8w)
+    # ragged prefill over the packed rows
+    k_rag = k_pool.reshape(P * ps, Hkv, D)[torch.from_numpy(slots).long().to(DEV)].contiguous()
+    v_rag = v_pool.reshape(P * ps, Hkv, D)[torch.from_numpy(slots).long().to(DEV)].contiguous()
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=DEV)
+    out = lib.prefill_paged(q8, qs, k_rag, ks, v_rag, None, _t(cu), _t(lengths), causal=True,
+                            lse=lse, error_word=err, cu_seqlens_kv=_t(cu), v_scale=vsc)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want_o, want_lse = oatt.paged_prefill_int8(q8w, qscale, kp, kscale, vp, bt, cu, lengths,
+                                               1.0 / np.sqrt(128.0), True, v_scale=vscw)
+    assert_attention_close(bf16_to_f64(out), want_o, rel=REL_L2_FP8_P, atol=ATOL_P_FP8)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
