@@ -641,6 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- merge
 // One warp per (request, q head); lane l owns D/32 consecutive outputs.
+// The lanes load the splits' lse values together (32 per round) and reduce
+// them with shuffles; the partial outputs are then read eight splits at a
+// time, all loads of a group in flight before their weighted sum.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(int B, int Hq,
                                                            const int32_t* __restrict__ split_off,
@@ -648,36 +651,55 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(int B, int Hq,
                                                            const float* __restrict__ part_lse,
                                                            uint16_t* __restrict__ o,
                                                            float* __restrict__ lse) {
-  constexpr int EPL = D / 32;
+  constexpr int EPL = D / 32, kGroup = 8;
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= B * Hq) return;
   const int b = w / Hq, h = w % Hq;
-  const int s0 = split_off[b], s1 = split_off[b + 1];
+  const int s0 = split_off[b], n = split_off[b + 1] - s0;
   float M = -INFINITY;
-  for (int s = s0; s < s1; ++s) M = fmaxf(M, part_lse[static_cast<size_t>(s) * Hq + h]);
+  for (int i = lane; i < n; i += 32) M = fmaxf(M, __ldg(part_lse + static_cast<size_t>(s0 + i) * Hq + h));
+  M = warp_max(M);
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   float den = 0.f;
   if (M > -INFINITY) {
-    for (int s = s0; s < s1; ++s) {
-      const float ls = part_lse[static_cast<size_t>(s) * Hq + h];
-      const float wgt = ls > -INFINITY ? __expf(ls - M) : 0.f;
+    for (int base = 0; base < n; base += 32) {
+      float wgt = 0.f;
+      if (base + lane < n) {
+        const float ls = __ldg(part_lse + static_cast<size_t>(s0 + base + lane) * Hq + h);
+        wgt = ls > -INFINITY ? __expf(ls - M) : 0.f;
+      }
       den += wgt;
-      const float* src = part_o + (static_cast<size_t>(s) * Hq + h) * D + lane * EPL;
-      if constexpr (EPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += wgt * v.x;
-        acc[1] += wgt * v.y;
-        acc[2] += wgt * v.z;
-        acc[3] += wgt * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += wgt * v.x;
-        acc[1] += wgt * v.y;
+      const int cnt = min(32, n - base);
+      for (int j = 0; j < cnt; j += kGroup) {
+        float v[kGroup][EPL];
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          const float* src =
+              part_o + (static_cast<size_t>(s0 + base + j + u) * Hq + h) * D + lane * EPL;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) v[u][e] = 0.f;
+          if (j + u < cnt) {
+            if constexpr (EPL == 4) {
+              const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+              const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+              v[u][0] = x.x; v[u][1] = x.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          const float wu = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
+        }
       }
     }
+    den = warp_sum(den);
   }
   const float inv = den > 0.f ? 1.0f / den : 0.f;
   uint16_t out[EPL];
