@@ -14,7 +14,7 @@ to the right-down causal region (参数说明 row sparse_mode: 3 =
 rightDownCausal, the lower triangle whose boundary runs from the bottom-right
 corner; 0 = everything).
 
-Readings (the design doc lists them): query i of a request with L_q queries and
+Readings where the pages are silent: query i of a request with L_q queries and
 L_kv keys sees key j iff j <= i + (L_kv - L_q) under sparse_mode 3; q head h
 reads kv head h // (Hq / Hkv); lse = logsumexp of the scaled logits (natural
 log); a row with no visible key gives O = 0 and lse = -inf.

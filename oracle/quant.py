@@ -13,7 +13,7 @@ The pages fix the granularities, not the rounding:
   参数说明 rows key_quant_mode / value_quant_mode = 2 (per_tile) and
   tile_size = 128.
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
   scale = float32(absmax) / float32(QMAX), QMAX = 448 (E4M3) or 127 (INT8);
   code  = round(float32(x) / scale) with IEEE float32 division;
   E4M3 rounding is nearest-even with saturation to +-448;
