@@ -23,18 +23,27 @@
 //              Q tile, then each key tile) into the f16 K-major SW128
 //              operand layout, one 64-column half each; lane 0 of warp 0
 //              issues the int8 Q and K copies (K rows of the pages a key
-//              tile spans, block_table lookups; pages past L_kv read as
-//              zeros) up to three steps ahead
+//              tile spans; pages past L_kv read as zeros) up to three steps
+//              ahead, with the page ids fetched two tiles earlier into a
+//              shared ring (IdRing)
 //   warp 1     QK MMAs  S[128 q x 128 k] = Q16 . K16^T        (kind::f16)
-//   warp 10    PV MMAs  O[128 q x 128 d] += P . V              (kind::f16)
-//              and the bf16 V copies, one key tile ahead
-//              P (bf16) is read from tensor memory, where the softmax wrote
-//              it over columns [0, 32) and [64, 96) of its S buffer (each
-//              column half of the scores holds its own keys' P)
+//   warp 10    PV MMAs  O[128 q x 128 d] += P . V, and the V copies (one
+//              box per page and 64-column half for bf16 V, one per page
+//              for E4M3 V), one key tile ahead.  bf16 V: kind::f16 with P
+//              (bf16) read from tensor memory, where the softmax wrote it
+//              over columns [0, 32) and [64, 96) of its S buffer.  E4M3 V
+//              (the V8 instantiation): kind::f8f6f4 with P as two E4M3
+//              terms hi + lo in columns [64 h, 64 h + 16) and
+//              [64 h + 16, 64 h + 32) of column half h, the per-channel V
+//              scales applied in the epilogue
 //   warps 2-9  online softmax, two threads per query row (columns [0, 64)
 //              on warps 2-5, [64, 128) on warps 6-9), lazy maximum (moves
 //              only by more than 2^8, then O is rescaled), and the epilogue
 //              O / l -> bf16 plus the lse.
+// The copy-issuing lanes do no integer division by the runtime page size
+// and no error reporting: both slowed the whole pipeline (a division runs
+// through the MUFU pipe the softmax keeps busy); bad page ids are flagged
+// by the prep pass and read as zeros.
 // TMEM: three S buffers and O (512 columns).
 //
 // Work: a unit is the pair of q tiles (t, n-1-t) of one (sequence, head).
@@ -57,7 +66,7 @@ constexpr int kWarpLoad = 0, kWarpQk = 1, kWarpPv = 10, kWarpConv = 11;
 constexpr int kSoftmax = 256;           // two threads per query row
 constexpr int kK8Stages = 4;            // staged int8 Q / K tiles
 constexpr int kK16Bufs = 2;             // converted K tiles
-constexpr int kVStages = 2;             // bf16 V tiles
+constexpr int kVStages = 2;             // V tiles (bf16, or E4M3 in the first half)
 constexpr int kI8Tile = kT * kD;        // 16 KB
 constexpr int kH16Tile = 2 * kT * kD;   // 32 KB: two 64-column halves
 constexpr int kHalf = kT * 128;         // 16 KB, one half (128 rows of 128 bytes)
