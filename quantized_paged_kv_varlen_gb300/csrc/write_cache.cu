@@ -11,6 +11,12 @@
 // Rounding is explicit so the bytes are reproducible: IEEE float32 division
 // (__fdiv_rn), nearest-even conversions, RoPE products and sums rounded
 // separately (__fmul_rn / __fadd_rn / __fsub_rn, no contraction).
+//
+// Options: the HND K/V pool layout (FP8 mode); K smoothing and E4M3 V with
+// per-channel scales (INT8 mode: a first pass writes exact per-block
+// partials, int64 key sums / float channel maxima, to the caller's scratch,
+// and the block write combines a sequence's partials); RoPE on the 64-wide
+// rope part of MLA rows and queries.
 #include "common.cuh"
 #include "internal.h"
 
