@@ -368,7 +368,11 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
  *                 num_blocks, Hq] (query block of row i is i / 128)
  *   k_pool        int8 [P, page_size, Hkv, 128], k_block_scale fp32
  *                 [B, num_blocks, Hkv] (key block of key j is j / 128)
- *   v_pool        bf16 [P, page_size, Hkv, 128]
+ *   v_pool        bf16 [P, page_size, Hkv, 128]; or, with v_scale set
+ *                 (Sage-style FP8 V, written with QPKV_WRITE_V_FP8), E4M3
+ *                 codes u8 of the same shape and v_scale fp32 [B, Hkv, 128]:
+ *                 v_j = code * v_scale[b, hk, channel], P enters P.V as two
+ *                 E4M3 terms (relative L2 error of o within 2e-2)
  *   o             bf16 [T, Hq, 128]; lse fp32 [T, Hq] or NULL
  *   workspace     qpkv_prefill_workspace_bytes(B, T, Hq) bytes of device
  *                 memory, overwritten by every call (the call's work order)
