@@ -222,3 +222,34 @@ def test_mla_block_sparse(lib, lengths, qps, QN, bs, S, n_ids, sbs, mode):
                                               sparse_block_size=sbs)
     assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
+
+
+def test_mla_tnd_keys_through_block_size_one(lib):
+    """A packed TND key tensor [KV_T, 1, 656] read as a pool of block size 1
+    whose block-table row b lists sequence b's rows."""
+    rng = np.random.default_rng(71)
+    lengths = np.array([150, 61, 300], np.int32)
+    KV_T, QN, S = int(lengths.sum()), 16, 128
+    kv = synth.bf16_normal(rng, (KV_T, 576))
+    rows = ocache.mla_pack_rows(kv)                              # packed TND rows
+    begin = np.concatenate([[0], np.cumsum(lengths)[:-1]])
+    bt = np.full((3, int(lengths.max())), -1, np.int32)
+    for b in range(3):
+        bt[b, :lengths[b]] = begin[b] + np.arange(lengths[b])
+    q = synth.bf16_normal(rng, (3, QN, 576))
+    idx = np.full((3, 1, S), -1, np.int32)
+    for t in range(3):
+        n = min(100, int(lengths[t]))
+        idx[t, 0, :n] = rng.permutation(int(lengths[t]))[:n]
+    cu_q = np.arange(1, 4, dtype=np.int32)
+    pool = _t(rows.reshape(KV_T, 1, 1, 656))
+    lse = torch.empty((3, QN), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = lib.mla_sparse_decode(_t(q).to(torch.bfloat16), pool, _t(idx), _t(bt), _t(lengths), _t(cu_q),
+                                scale=1.0 / 24.0, lse=lse, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want_o, want_lse = omla.mla_sparse_decode(q, rows.reshape(KV_T, 1, 1, 656), idx, bt, lengths,
+                                              cu_q, 1.0 / 24.0)
+    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
