@@ -379,28 +379,48 @@ class DecodePlan:
                         for _ in range(2)]
         self._copied = [None, None]
         self._which = 0
+        self._ready = None                   # copy to wait for before the next run
+        self._released = torch.cuda.Event()  # the last run / attend / merge done with int_ws
+        self._released_set = False
         self.plan_info = (ctypes.c_int64 * PLAN_INFO_LEN)()
         self.replan()
 
-    def replan(self):
-        """Run the host planner again and copy the work list to the device on
-        the current stream (the per-step cost of the plan/run split)."""
+    def replan(self, stream=None):
+        """Run the host planner again and copy the work list to the device
+        (the per-step cost of the plan/run split).  The copy runs on the
+        current stream, or on ``stream`` (a torch.cuda.Stream): there it
+        waits until the previous run / attend / merge is done with the int
+        workspace, and the next run / attend waits for it, so the copy can
+        overlap other work on the current stream."""
         torch = _torch()
         lib = load()
         buf = self._pinned[self._which]
         if self._copied[self._which] is not None:
             self._copied[self._which].synchronize()
+        s = stream if stream is not None else torch.cuda.current_stream()
+        if stream is not None and self._released_set:
+            stream.wait_event(self._released)
         _check(lib.qpkv_decode_plan(self.lens.ctypes.data, self.B, self.Hq, self.Hkv,
                                     self.page_size, self.D, self.num_sms,
                                     ctypes.c_void_p(buf.data_ptr()), buf.numel(),
                                     _ptr(self.int_ws), self.int_ws.numel(), self.plan_info,
-                                    _stream()), "qpkv_decode_plan")
+                                    ctypes.c_void_p(s.cuda_stream)), "qpkv_decode_plan")
         _check(lib.qpkv_decode_plan_set_kv_layout(self.plan_info, KV_LAYOUTS[self.kv_layout]),
                "qpkv_decode_plan_set_kv_layout")
         ev = torch.cuda.Event()
-        ev.record()
+        ev.record(s)
         self._copied[self._which] = ev
+        self._ready = ev if stream is not None else None
         self._which ^= 1
+
+    def _before_run(self):
+        if self._ready is not None:
+            _torch().cuda.current_stream().wait_event(self._ready)
+            self._ready = None
+
+    def _after_run(self):
+        self._released.record()
+        self._released_set = True
 
     @property
     def num_items(self):
@@ -440,30 +460,35 @@ class DecodePlan:
         self._check_run(q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table)
         if out is None:
             out = torch.empty_like(q)
+        self._before_run()
         _check(lib.qpkv_decode_run(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
                                    _ptr(self.int_ws), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                    _ptr(k_scale_pool), _ptr(v_scale_pool), k_pool.shape[0],
                                    self.page_size, _ptr(block_table), block_table.shape[1],
                                    float(sm_scale), _ptr(out), _ptr(lse), _ptr(error_word),
                                    _stream()), "qpkv_decode_run")
+        self._after_run()
         return out
 
     def attend(self, q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table, sm_scale,
                error_word=None):
         lib = load()
         self._check_run(q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table)
+        self._before_run()
         _check(lib.qpkv_decode_attend(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
                                       _ptr(self.int_ws), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                       _ptr(k_scale_pool), _ptr(v_scale_pool), k_pool.shape[0],
                                       self.page_size, _ptr(block_table), block_table.shape[1],
                                       float(sm_scale), _ptr(error_word), _stream()),
                "qpkv_decode_attend")
+        self._after_run()
 
     def merge(self, out, lse=None):
         lib = load()
         _check(lib.qpkv_decode_merge(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
                                      _ptr(self.int_ws), _ptr(out), _ptr(lse), _stream()),
                "qpkv_decode_merge")
+        self._after_run()
         return out
 
 
