@@ -10,7 +10,9 @@
  * qpkv_status.  Argument checks that need no device memory run on the host
  * before anything is launched; contents of device arrays (page ids, sparse
  * indices) are checked by the kernels, which skip a bad entry and set a bit
- * in the caller's device `error_word` (int32, may be NULL).
+ * in a device error word: the caller's `error_word` (int32), or, when the
+ * caller passes NULL, a word the library keeps per GPU, which
+ * qpkv_error_check reads and clears (see "device error word" below).
  *
  * Strides are in elements.  All layouts are row-major and contiguous unless
  * a stride argument says otherwise.  Names follow the source pages:
@@ -45,8 +47,8 @@ typedef int32_t qpkv_status;
 #define QPKV_ERR_UNSUPPORTED 2         /* head_dim, page_size, head ratio, dtype, mode */
 #define QPKV_ERR_WORKSPACE_TOO_SMALL 3 /* a caller workspace is smaller than required */
 #define QPKV_ERR_CUDA 4                /* a CUDA runtime/driver call or launch failed */
-#define QPKV_ERR_DEVICE 5              /* reserved: device error word reported by a caller */
-#define QPKV_ERR_TIMEOUT 6             /* reserved: device wait timeout reported by a caller */
+#define QPKV_ERR_DEVICE 5              /* a kernel set a bit of the device error word */
+#define QPKV_ERR_TIMEOUT 6             /* a kernel's pipeline wait ran out (QPKV_DEV_ERR_TIMEOUT) */
 #define QPKV_ERR_STATIC_LIMIT 7        /* problem too large for qpkv_decode_static's fixed scratch */
 
 /* bits a kernel ORs into the device error word */
@@ -57,6 +59,37 @@ typedef int32_t qpkv_status;
 
 /* Text of a status code (static storage, never NULL). */
 const char* qpkv_status_string(qpkv_status status);
+
+/* ------------------------------------------------------ device error word
+ * Kernels report what they cannot return (a skipped bad page id or sparse
+ * index, a pipeline wait that ran out) by OR-ing QPKV_DEV_ERR_* bits into a
+ * device int32.  Every entry point that takes an `error_word` uses the
+ * caller's word when one is given and otherwise a word owned by the library
+ * (one per GPU, a file-scope __device__ variable; the first call on a
+ * device looks up its address with that device current).  The outputs of a
+ * call that set QPKV_DEV_ERR_TIMEOUT are undefined.
+ *
+ * qpkv_error_status maps a word's bits to a status: QPKV_ERR_TIMEOUT when
+ * the timeout bit is set, else QPKV_ERR_DEVICE for any other bit, else
+ * QPKV_OK.
+ *
+ * qpkv_error_check takes the library's word of the current device (an
+ * atomic exchange with 0, in a one-thread kernel on `stream`), copies it to
+ * the host and synchronises `stream` (the only call of this library that
+ * waits); *bits_out (may be NULL) receives the bits and the return value is
+ * qpkv_error_status(bits), or QPKV_ERR_CUDA when a CUDA call fails.  Bits
+ * set by work on other streams that has not finished are reported by a
+ * later check. */
+qpkv_status qpkv_error_status(int32_t bits);
+qpkv_status qpkv_error_check(void* stream, int32_t* bits_out);
+
+/* Self-test of the bounded wait that every pipeline wait of the library's
+ * kernels uses: a one-CTA kernel waits on an mbarrier whose arrival never
+ * comes, gives up after limit_cycles SM cycles (1000 .. 4e9; the kernels use
+ * 4e9, about 2 s) and sets QPKV_DEV_ERR_TIMEOUT in error_word (the
+ * library's word when NULL).  The kernel then returns normally and the
+ * context stays usable.  INVALID_ARG for a limit outside the range. */
+qpkv_status qpkv_selftest_wait_timeout(int64_t limit_cycles, int32_t* error_word, void* stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t qpkv_version(void);
@@ -173,7 +206,7 @@ typedef struct qpkv_write_params {
   void* q_out;            /* INT8 mode: int8 [T, Hq, D]; MLA: bf16 [T, Hq, 576] */
   float* q_block_scale;   /* INT8 mode [B, num_blocks, Hq] */
   int32_t* slot_mapping;  /* [T] or NULL */
-  int32_t* error_word;    /* device int32 or NULL */
+  int32_t* error_word;    /* device int32, or NULL for the library's word */
   int32_t flags;          /* QPKV_WRITE_SMOOTH_K (INT8 mode) or 0 */
   int32_t pad0;
   float* k_mean;          /* INT8 + SMOOTH_K: out float [B, Hkv, 128] */
@@ -295,8 +328,10 @@ qpkv_status qpkv_decode_merge(const int64_t* plan_info, const void* float_ws,
  * cudaMalloc, cudaFree or other allocating routine.
  *
  * The first call on each device looks up the arrays' device addresses
- * (cudaGetSymbolAddress) with that device current; make that first call
- * outside any stream capture.  Every call reuses the same arrays: calls
+ * (cudaGetSymbolAddress) with that device current.  The work list goes
+ * through one shared host buffer by a pageable copy, so a call made while
+ * its stream is capturing returns QPKV_ERR_UNSUPPORTED and enqueues
+ * nothing.  Every call reuses the same arrays: calls
  * whose work overlaps on the GPU (different streams, or different host
  * threads without ordering) race and corrupt each other's results; nothing
  * in the arrays needs to start at zero (each call rewrites what it reads).
@@ -329,7 +364,7 @@ qpkv_status qpkv_decode_static(const int32_t* seqlens_kv_host, int32_t batch_siz
  *   o          device bf16 [B, Sq, Hq, D]; rows that see no key are 0
  *   lse        device fp32 [B, Sq, Hq] or NULL: natural log of the sum of
  *              exp(scaled logits); -inf for rows that see no key
- *   error_word device int32 or NULL: QPKV_DEV_ERR_* bits set by the kernel
+ *   error_word device int32 (NULL: the library's word): QPKV_DEV_ERR_* bits set by the kernel
  * kv head of q head h: h / (Hq / Hkv).  Supported: D = 128, Hq % Hkv == 0;
  * every pointer 16-byte aligned.  P enters the PV product as two E4M3
  * terms (hi + lo, about 8 significant bits).  The caller owns all
@@ -376,7 +411,7 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
  *   o             bf16 [T, Hq, 128]; lse fp32 [T, Hq] or NULL
  *   workspace     qpkv_prefill_workspace_bytes(B, T, Hq) bytes of device
  *                 memory, overwritten by every call (the call's work order)
- *   error_word    int32 or NULL: QPKV_DEV_ERR_BAD_PAGE (a block_table entry
+ *   error_word    int32 (NULL: the library's word): QPKV_DEV_ERR_BAD_PAGE (a block_table entry
  *                 outside [0, P) read as zeros), QPKV_DEV_ERR_BAD_LENGTH (a
  *                 sequence whose lengths exceed num_blocks * 128, the
  *                 block_table row or num_tokens: its rows are zeroed),

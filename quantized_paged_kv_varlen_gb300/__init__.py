@@ -15,7 +15,7 @@ import ctypes
 import os
 
 __all__ = [
-    "QpkvError", "load", "rope_table", "write_cache_fp8", "write_cache_int8_block128_rope",
+    "QpkvError", "load", "check_errors", "selftest_wait_timeout", "rope_table", "write_cache_fp8", "write_cache_int8_block128_rope",
     "write_cache_mla", "DecodePlan", "PAGE_ROW_MLA",
 ]
 
@@ -35,6 +35,12 @@ KV_LAYOUTS = {"NHD": 0, "HND": 1}   # K/V pool layouts of the FP8 decode path
 DEV_ERR_TIMEOUT = 1
 DEV_ERR_BAD_PAGE = 2
 DEV_ERR_BAD_INDEX = 4
+DEV_ERR_BAD_LENGTH = 8
+
+ERR_UNSUPPORTED = 2
+ERR_CUDA = 4
+ERR_DEVICE = 5
+ERR_TIMEOUT = 6
 
 _lib = None
 
@@ -122,6 +128,9 @@ def _declare(lib):
         "qpkv_mla_workspace_bytes": (S, [_i32, _i32]),
         "qpkv_smooth_workspace_bytes": (S, [_i32, _i32, _i32]),
         "qpkv_mla_sparse_decode": (_i32, [ctypes.POINTER(MlaParams), _p]),
+        "qpkv_error_status": (_i32, [_i32]),
+        "qpkv_error_check": (_i32, [_p, ctypes.POINTER(_i32)]),
+        "qpkv_selftest_wait_timeout": (_i32, [ctypes.c_int64, _p, _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -187,6 +196,28 @@ def rope_table(theta, max_pos, rot_dim, rope_scale=1.0, device="cuda"):
     _check(lib.qpkv_rope_table(float(theta), float(rope_scale), int(max_pos), int(rot_dim),
                                _ptr(cos), _ptr(sin), _stream()), "qpkv_rope_table")
     return cos, sin
+
+
+def check_errors(raise_on_error=True):
+    """Read and clear the library's device error word of the current GPU
+    (the word kernels use when a call passed no ``error_word``); waits for
+    the current stream.  Returns the QPKV_DEV_ERR_* bits, or raises
+    QpkvError (status QPKV_ERR_DEVICE / QPKV_ERR_TIMEOUT) when a bit is set
+    and ``raise_on_error``."""
+    lib = load()
+    bits = _i32(0)
+    st = lib.qpkv_error_check(_stream(), ctypes.byref(bits))
+    if st != 0 and (raise_on_error or st == ERR_CUDA):
+        raise QpkvError(st, f"qpkv_error_check (bits {bits.value:#x})")
+    return bits.value
+
+
+def selftest_wait_timeout(limit_cycles, error_word=None):
+    """Launch the one-CTA self-test whose mbarrier wait never completes: it
+    gives up after ``limit_cycles`` SM cycles and sets DEV_ERR_TIMEOUT in
+    ``error_word`` (or the library's word)."""
+    _check(load().qpkv_selftest_wait_timeout(int(limit_cycles), _ptr(error_word), _stream()),
+           "qpkv_selftest_wait_timeout")
 
 
 def _base_params(mode, cu_seqlens, block_table, page_size, num_pages, num_tokens, max_seqlen):

@@ -273,8 +273,11 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
     default:
       return QPKV_ERR_UNSUPPORTED;
   }
-  return launch_write_cache(*p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPKV_OK
-                                                                                  : QPKV_ERR_CUDA;
+  qpkv_write_params w = *p;
+  if (w.error_word == nullptr && (w.error_word = default_error_word()) == nullptr)
+    return QPKV_ERR_CUDA;
+  return launch_write_cache(w, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QPKV_OK
+                                                                                 : QPKV_ERR_CUDA;
 }
 
 qpkv_status qpkv_decode_workspace_sizes(const int32_t* lens, int32_t B, int32_t Hq, int32_t Hkv,
@@ -373,6 +376,7 @@ qpkv_status qpkv_decode_attend(const int64_t* plan_info, void* float_ws, size_t 
                                   k_scale_pool, v_scale_pool, num_pages, page_size, block_table,
                                   bt_stride);
   if (st != QPKV_OK) return st;
+  if (error_word == nullptr && (error_word = default_error_word()) == nullptr) return QPKV_ERR_CUDA;
   int status = QPKV_OK;
   const cudaError_t e = launch_decode_attend(
       p, static_cast<float*>(float_ws), int_ws, q, k_pool, v_pool, k_scale_pool, v_scale_pool,
@@ -424,6 +428,7 @@ qpkv_status qpkv_fp8_attn_fwd(const void* q, const void* k, const void* v, int32
     return QPKV_ERR_INVALID_ARG;
   if (seqlen_k > 0 && (q == nullptr || k == nullptr || v == nullptr)) return QPKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return QPKV_ERR_INVALID_ARG;
+  if (error_word == nullptr && (error_word = default_error_word()) == nullptr) return QPKV_ERR_CUDA;
   int status = QPKV_OK;
   const cudaError_t e = launch_fp8_attn(q, k, v, batch, seqlen_q, seqlen_k, num_qo_heads,
                                         num_kv_heads, head_dim, q_descale, k_descale, v_descale,
@@ -472,8 +477,11 @@ qpkv_status qpkv_prefill_paged(const qpkv_prefill_params* p, void* stream) {
     return QPKV_ERR_INVALID_ARG;
   if (p->workspace_bytes < prefill_workspace_bytes(p->num_seqs, p->num_tokens, p->num_heads_q))
     return QPKV_ERR_WORKSPACE_TOO_SMALL;
+  qpkv_prefill_params w = *p;
+  if (w.error_word == nullptr && (w.error_word = default_error_word()) == nullptr)
+    return QPKV_ERR_CUDA;
   int status = QPKV_OK;
-  const cudaError_t e = launch_prefill_int8(*p, static_cast<cudaStream_t>(stream), &status);
+  const cudaError_t e = launch_prefill_int8(w, static_cast<cudaStream_t>(stream), &status);
   if (status != QPKV_OK) return static_cast<qpkv_status>(status);
   return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
 }
@@ -530,8 +538,11 @@ qpkv_status qpkv_mla_sparse_decode(const qpkv_mla_params* p, void* stream) {
     return QPKV_ERR_INVALID_ARG;
   if (p->workspace_bytes < mla_workspace_bytes(p->num_tokens, static_cast<int>(keys)))
     return QPKV_ERR_WORKSPACE_TOO_SMALL;
+  qpkv_mla_params w = *p;
+  if (w.error_word == nullptr && (w.error_word = default_error_word()) == nullptr)
+    return QPKV_ERR_CUDA;
   int status = QPKV_OK;
-  const cudaError_t e = launch_mla_sparse(*p, static_cast<cudaStream_t>(stream), &status);
+  const cudaError_t e = launch_mla_sparse(w, static_cast<cudaStream_t>(stream), &status);
   if (status != QPKV_OK) return static_cast<qpkv_status>(status);
   return e == cudaSuccess ? QPKV_OK : QPKV_ERR_CUDA;
 }

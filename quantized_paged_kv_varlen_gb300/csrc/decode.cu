@@ -694,8 +694,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(int B, int Hq,
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
           const float wu = __shfl_sync(0xffffffffu, wgt, (j + u) & 31);
+          // a split with weight 0 adds nothing, even if its partial row holds NaN
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
+          for (int e = 0; e < EPL; ++e) acc[e] = wu > 0.f ? fmaf(wu, v[u][e], acc[e]) : acc[e];
         }
       }
     }

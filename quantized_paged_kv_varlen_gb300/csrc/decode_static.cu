@@ -11,8 +11,10 @@
 // Every GPU that loads the library holds both until the process exits.  In
 // host code the array names are host-side stand-ins, not device addresses,
 // so the first call on each device looks the device addresses up with
-// cudaGetSymbolAddress (that device current) and keeps them; that first call
-// should come before any stream capture.  All calls share the arrays and
+// cudaGetSymbolAddress (that device current) and keeps them.  The work
+// list is staged through one shared host buffer by a pageable copy, so a
+// call refuses to run (QPKV_ERR_UNSUPPORTED, nothing enqueued) while its
+// stream is capturing.  All calls share the arrays and
 // each call rewrites everything it later reads (nothing must start at zero);
 // calls whose GPU work overlaps race on them.  Batches that need more space
 // are rejected on the host with QPKV_ERR_STATIC_LIMIT.  Nothing here
@@ -84,6 +86,12 @@ extern "C" qpkv_status qpkv_decode_static(const int32_t* seqlens_kv_host, int32_
   if (int_bytes > QPKV_STATIC_INT_BYTES || float_bytes > QPKV_STATIC_FLOAT_BYTES)
     return QPKV_ERR_STATIC_LIMIT;
   if (o == nullptr) return QPKV_ERR_INVALID_ARG;
+  // The copy below reads g_host_staging when it runs; a recorded copy would
+  // read whatever a later call planned there.
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capturing) != cudaSuccess)
+    return QPKV_ERR_CUDA;
+  if (capturing != cudaStreamCaptureStatusNone) return QPKV_ERR_UNSUPPORTED;
 
   int64_t plan_info[QPKV_PLAN_INFO_LEN];
   DeviceScratch scratch;

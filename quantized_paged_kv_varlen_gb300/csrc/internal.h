@@ -77,6 +77,10 @@ cudaError_t launch_prefill_int8(const qpkv_prefill_params& p, cudaStream_t strea
 size_t mla_workspace_bytes(int num_tokens, int sparse_size);
 cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int* status);
 
+// The library-owned device error word of the current device (errors.cu),
+// used by the entry points when the caller passes no word; NULL on failure.
+int32_t* default_error_word();
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
                            void* base, const uint64_t* dims, const uint64_t* strides_bytes,

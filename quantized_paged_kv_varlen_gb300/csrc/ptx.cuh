@@ -79,17 +79,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-// The timeout uses the SM cycle counter, sampled every 64 polls, so a
-// completed phase is noticed within one poll.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once
+// limit_cycles SM cycles have passed.  The cycle counter is sampled every
+// 64 polls, so a completed phase is noticed within one poll.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit_cycles = kWaitTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitTimeoutCycles) return false;
+    if (clock64() - t0 > limit_cycles) return false;
   }
 }
 

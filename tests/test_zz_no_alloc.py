@@ -1,8 +1,10 @@
 """The allocation-free decode entry point (qpkv_decode_static), for callers
 that cannot allocate device memory: its output must match the planned
-decode (qpkv_decode_plan + qpkv_decode_run) on the same inputs, on two
-calls in a row (the fixed scratch keeps the previous call's contents), and
-oversized batches must be rejected on the host.
+decode (qpkv_decode_plan + qpkv_decode_run) and the CPU oracle on the same
+inputs, on two calls in a row (the fixed scratch keeps the previous call's
+contents), the second call must leave the device's free memory and torch's
+allocation count unchanged, a call on a capturing stream must be refused
+with nothing recorded, and oversized batches must be rejected on the host.
 
 This file sorts last so that a run stopping at the first failure has
 already run every other test."""
@@ -12,9 +14,12 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import attention as oatt
+from oracle import cache as ocache
 from quantized_paged_kv_varlen_gb300 import synth
-from tests.gpu_util import assert_attention_close, assert_lse_close, bf16_to_f64
+from tests.gpu_util import DECODE_TIGHT, assert_attention_close, assert_lse_close, bf16_to_f64
 
+UNSUPPORTED = 2
 STATIC_LIMIT = 7
 
 
@@ -67,15 +72,53 @@ def test_static_decode_matches_planned_decode_twice(lib, which):
     ref = plan.run(q, d["k_pool"], d["v_pool"], d["ks"], d["vs"], d["bt"], wl.scale, lse=ref_lse)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     raw = lib.load()
-    for _ in range(2):
+    # the oracle on the same cache bytes (written by the oracle's own quantiser)
+    k, v = wl.kv_all()
+    P, ps, H, D = wl.num_pages, wl.page_size, wl.Hkv, wl.D
+    z8 = np.zeros((P, ps, H, D), np.uint8)
+    zs = np.zeros((P, ps, H), np.float32)
+    kp, vp, ks, vs, _, _ = ocache.write_fp8_token_head(
+        k, v, np.cumsum(wl.lengths), np.zeros(wl.B, np.int64), wl.block_table, ps, z8, z8, zs, zs)
+    want_o, want_lse = oatt.paged_decode_fp8(wl.q, kp, vp, ks, vs, wl.block_table, wl.lengths,
+                                             wl.scale)
+    for call in range(2):
         out = torch.full_like(q, float("nan"))
         lse = torch.full((wl.B, wl.Hq), float("nan"), dtype=torch.float32, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         assert _call_static(raw, wl, wl.lengths, q, d, out, lse, err, sms) == 0
         torch.cuda.synchronize()
+        if call == 1:
+            # nothing allocated by the call itself (the first call may load modules)
+            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() == alloc0
         assert int(err.item()) == 0
         assert_attention_close(bf16_to_f64(out), bf16_to_f64(ref))
         assert_lse_close(lse.cpu().numpy(), ref_lse.cpu().numpy())
+        assert_attention_close(bf16_to_f64(out), want_o, tight=DECODE_TIGHT)
+        assert_lse_close(lse.cpu().numpy(), want_lse)
+
+
+@pytest.mark.gpu
+def test_static_decode_refuses_a_capturing_stream(lib):
+    """Begin a capture, make the call, end the capture: the call returns
+    QPKV_ERR_UNSUPPORTED and records nothing."""
+    wl = synth.tiny_decode(0)
+    d = _cache(lib, wl)
+    q = torch.from_numpy(wl.q).cuda().bfloat16()
+    out = torch.zeros_like(q)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    raw = lib.load()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        st = _call_static(raw, wl, wl.lengths, q, d, out, None, None, sms)
+        g.capture_end()
+    torch.cuda.synchronize()
+    assert st == UNSUPPORTED
 
 
 def test_static_decode_rejects_batches_beyond_its_scratch():
