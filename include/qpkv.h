@@ -124,6 +124,14 @@ qpkv_status qpkv_rope_table(float theta, float rope_scale, int32_t max_pos, int3
  *     [P, page_size, Hkv, D] + float scale pools [P, page_size, Hkv];
  *     scale = absmax_D / 448, code = RNE_satfinite(x / scale) (IEEE fp32
  *     division), absmax 0 -> scale 0 and zero codes.  D in {64, 128}.
+ *     With rope_cos / rope_sin (float [rope_max_pos, D/2], qpkv_rope_table
+ *     with rot_dim D) k is rotated first (rotate-half, pairs (i, i + D/2),
+ *     each product and sum rounded to float32) at the token's position and
+ *     the float32 result quantised; v never is.  With q as well (bf16
+ *     [T, Hq, D], Hq = num_heads_q) the rotated queries are rounded to bf16
+ *     (nearest-even) into q_out (bf16, same shape; may alias q).  A position
+ *     outside the tables leaves the token unwritten and sets
+ *     QPKV_DEV_ERR_BAD_LENGTH.
  *  QPKV_WRITE_INT8_BLOCK128_ROPE  q, k, v bf16 [T, H, D]: RoPE (rotate-half,
  *     pairs (i, i + D/2), tables from qpkv_rope_table) on q and k, then one
  *     scale per (sequence, 128-token block, head): scale = absmax / 127,

@@ -238,10 +238,15 @@ def _base_params(mode, cu_seqlens, block_table, page_size, num_pages, num_tokens
 
 
 def write_cache_fp8(k, v, cu_seqlens, block_table, k_pool, v_pool, k_scale_pool, v_scale_pool,
-                    start_pos=None, slot_mapping=None, error_word=None, kv_layout="NHD"):
+                    start_pos=None, slot_mapping=None, error_word=None, kv_layout="NHD",
+                    rope_cos=None, rope_sin=None, q=None, q_out=None):
     """FP8 per-(token, head) cache write.  k, v: bf16 [T, Hkv, D]; pools u8
     [P, page_size, Hkv, D] (kv_layout "HND": [P, Hkv, page_size, D]); scale
-    pools float32 [P, page_size, Hkv] in both layouts."""
+    pools float32 [P, page_size, Hkv] in both layouts.  With rope_cos /
+    rope_sin (fp32 [max_pos, D/2], ``rope_table(theta, max_pos, D)``) k is
+    rotated at each token's position before it is quantised; with q (bf16
+    [T, Hq, D]) the rotated queries go to q_out (bf16, allocated when None,
+    may be q itself), which is returned."""
     torch = _torch()
     lib = load()
     _need(k, "k", torch.bfloat16, 3)
@@ -261,10 +266,29 @@ def write_cache_fp8(k, v, cu_seqlens, block_table, k_pool, v_pool, k_scale_pool,
     p.k, p.v = _ptr(k), _ptr(v)
     p.k_pool, p.v_pool = _ptr(k_pool), _ptr(v_pool)
     p.k_scale_pool, p.v_scale_pool = _ptr(k_scale_pool), _ptr(v_scale_pool)
+    if rope_cos is not None:
+        _need(rope_cos, "rope_cos", torch.float32, 2)
+        _need(rope_sin, "rope_sin", torch.float32, 2)
+        if rope_cos.shape[1] != D // 2 or tuple(rope_sin.shape) != tuple(rope_cos.shape):
+            raise ValueError("RoPE tables must be [max_pos, D/2]")
+        p.rope_max_pos = rope_cos.shape[0]
+        p.rope_cos, p.rope_sin = _ptr(rope_cos), _ptr(rope_sin)
+    if q is not None:
+        if rope_cos is None:
+            raise ValueError("rotating q needs the RoPE tables")
+        _need(q, "q", torch.bfloat16, 3)
+        if q.shape[0] != k.shape[0] or q.shape[2] != D:
+            raise ValueError("q must be [T, Hq, D]")
+        if q_out is None:
+            q_out = torch.empty_like(q)
+        _need(q_out, "q_out", torch.bfloat16, 3)
+        p.num_heads_q = q.shape[1]
+        p.q, p.q_out = _ptr(q), _ptr(q_out)
     p.start_pos = _ptr(start_pos)
     p.slot_mapping = _ptr(slot_mapping)
     p.error_word = _ptr(error_word)
     _check(lib.qpkv_write_cache(ctypes.byref(p), _stream()), "qpkv_write_cache(fp8)")
+    return q_out
 
 
 def smooth_workspace(num_seqs, num_blocks, num_heads_kv, device="cuda"):

@@ -232,8 +232,13 @@ qpkv_status qpkv_write_cache(const qpkv_write_params* p, void* stream) {
   switch (p->mode) {
     case QPKV_WRITE_FP8_TOKEN_HEAD:
       if (p->head_dim != 64 && p->head_dim != 128) return QPKV_ERR_UNSUPPORTED;
-      if (p->rope_cos != nullptr || p->rope_sin != nullptr || (p->flags & ~QPKV_WRITE_HND))
-        return QPKV_ERR_UNSUPPORTED;
+      if (p->flags & ~QPKV_WRITE_HND) return QPKV_ERR_UNSUPPORTED;
+      if ((p->rope_cos == nullptr) != (p->rope_sin == nullptr)) return QPKV_ERR_INVALID_ARG;
+      if (p->rope_cos != nullptr && p->rope_max_pos < 1) return QPKV_ERR_INVALID_ARG;
+      if (p->q != nullptr &&
+          (p->rope_cos == nullptr || p->q_out == nullptr || p->num_heads_q < 1 ||
+           !aligned16(p->q) || !aligned16(p->q_out)))
+        return QPKV_ERR_INVALID_ARG;
       if (p->v == nullptr || p->v_pool == nullptr || p->k_scale_pool == nullptr ||
           p->v_scale_pool == nullptr)
         return QPKV_ERR_INVALID_ARG;

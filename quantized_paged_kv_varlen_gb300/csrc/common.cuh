@@ -65,6 +65,22 @@ __device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Packed f16x2 a + b (round to nearest even).
+__device__ __forceinline__ uint32_t f16x2_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// acc + both f16 halves of a packed pair, each added in f32 (mixed-precision
+// adds: the f16 values enter exactly).
+__device__ __forceinline__ float add_f16x2_to_f32(float acc, uint32_t h2) {
+  const uint16_t lo = static_cast<uint16_t>(h2 & 0xFFFFu), hi = static_cast<uint16_t>(h2 >> 16);
+  asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(lo));
+  asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(hi));
+  return acc;
+}
+
 __device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
   return e4m3x2_to_f32x2(static_cast<uint16_t>(code)).x;
 }

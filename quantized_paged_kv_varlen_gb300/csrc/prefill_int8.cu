@@ -728,7 +728,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(bar_id, 64);
       const float corr = 128.f * (static_cast<float>(qhalf) + sh.pair[half ^ 1][r]);
       named_barrier(bar_id, 64);
-      float m = -INFINITY, l = 0.f;
+      // l: the sum of the unrounded p (for the lse, and the E4M3-P
+      // instantiation's normaliser: E4M3 flushes p below 2^-10 to zero, and
+      // that lost mass would bias a sum of the rounded terms); lr: the sum of
+      // the bf16 P the P.V product sees, which normalises O in the bf16
+      // instantiation so that P's rounding cancels where one key dominates
+      float m = -INFINITY, l = 0.f, lr = 0.f;
       float sk_next = __ldg(skp);
       for (int j = 0; j < t.nkv; ++j) {
         // logit multiplier of this key tile (log2 units), kept above 0 so
@@ -767,6 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (m > -INFINITY) {
             f = exp2f(m - mx);
             l *= f;
+            lr *= f;
             need = true;
           }
           m = mx;
@@ -832,6 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               l += p0 + p1;
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
               pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+              lr += __uint_as_float(pk[w] << 16) + __uint_as_float(pk[w] & 0xFFFF0000u);
             }
             tmem_st16(srow + 64 * half + 16 * c2, pk);
           }
@@ -845,7 +852,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(bar_id, 64);
       const float lt = l + sh.pair[half ^ 1][r];
       named_barrier(bar_id, 64);
-      const float so = lt > 0.f ? 1.f / lt : 0.f;
+      float ln = lt;                 // the normaliser of O
+      if (!V8) {
+        sh.pair[half][r] = lr;
+        named_barrier(bar_id, 64);
+        ln = lr + sh.pair[half ^ 1][r];
+        named_barrier(bar_id, 64);
+      }
+      const float so = ln > 0.f ? 1.f / ln : 0.f;
       // the next item's q row half loads while this item's O is written
       uint4 qn[4];
       Tile tn;

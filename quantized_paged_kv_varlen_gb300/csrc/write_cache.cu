@@ -34,14 +34,52 @@ __device__ __forceinline__ int pool_page(const int32_t* __restrict__ bt, int bt_
 }
 
 // ---------------------------------------------- FP8 per-(token, head) mode
-// One warp per (token, kv head); lane l owns D/32 consecutive elements.
+// One warp per (token, kv head); lane l owns D/32 consecutive elements, so
+// the rotate-half partner of lane l's elements (i + D/2) sits on lane l ^ 16.
+
+// Rotate-half RoPE of the EPL elements x a lane owns (first element index
+// i0 = lane * EPL of a D-wide head) at table row `pos`: each product and sum
+// rounded to float32 separately.
+template <int D, int EPL>
+__device__ __forceinline__ void rope_lane(float (&x)[EPL], int lane, int pos,
+                                          const float* __restrict__ cos_t,
+                                          const float* __restrict__ sin_t) {
+  const bool first = lane < 16;                       // elements i < D/2
+  const int i0 = (lane & 15) * EPL;                   // pair index of x[0]
+  const float* c = cos_t + static_cast<size_t>(pos) * (D / 2) + i0;
+  const float* s = sin_t + static_cast<size_t>(pos) * (D / 2) + i0;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+    const float ce = __ldg(c + e), se = __ldg(s + e);
+    x[e] = first ? __fsub_rn(__fmul_rn(x[e], ce), __fmul_rn(other, se))
+                 : __fadd_rn(__fmul_rn(x[e], ce), __fmul_rn(other, se));
+  }
+}
+
+template <int EPL>
+__device__ __forceinline__ void load_bf16_lane(const uint16_t* src, float (&x)[EPL]) {
+  if constexpr (EPL == 4) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    x[0] = bf16_bits_to_float(raw.x & 0xFFFF);
+    x[1] = bf16_bits_to_float(raw.x >> 16);
+    x[2] = bf16_bits_to_float(raw.y & 0xFFFF);
+    x[3] = bf16_bits_to_float(raw.y >> 16);
+  } else {
+    const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+    x[0] = bf16_bits_to_float(raw & 0xFFFF);
+    x[1] = bf16_bits_to_float(raw >> 16);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
     int T, int B, int H, int ps, int num_pages, int bt_stride, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ bt,
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, uint8_t* __restrict__ k_pool,
     uint8_t* __restrict__ v_pool, float* __restrict__ k_scale, float* __restrict__ v_scale,
-    int32_t* __restrict__ slots, int hnd, int* err) {
+    int32_t* __restrict__ slots, int hnd, const float* __restrict__ rope_cos,
+    const float* __restrict__ rope_sin, int rope_max_pos, int* err) {
   constexpr int EPL = D / 32;  // 2 or 4 elements per lane
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -49,6 +87,10 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
   const int t = w / H, h = w - (w / H) * H;
   const int b = seq_of_token(cu, B, t);
   const int p = (start_pos ? __ldg(start_pos + b) : 0) + (t - seq_begin(cu, b));
+  if (rope_cos != nullptr && (p < 0 || p >= rope_max_pos)) {
+    if (lane == 0) report_error(err, kDevErrBadLength);
+    return;
+  }
   const int page = pool_page(bt, bt_stride, b, p, ps, num_pages, lane == 0 ? err : nullptr);
   if (page < 0) return;
   const size_t slot = static_cast<size_t>(page) * ps + (p % ps);
@@ -60,17 +102,8 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
   for (int which = 0; which < 2; ++which) {
     const uint16_t* src = (which ? v : k) + (static_cast<size_t>(t) * H + h) * D + lane * EPL;
     float x[EPL];
-    if constexpr (EPL == 4) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(src);
-      x[0] = bf16_bits_to_float(raw.x & 0xFFFF);
-      x[1] = bf16_bits_to_float(raw.x >> 16);
-      x[2] = bf16_bits_to_float(raw.y & 0xFFFF);
-      x[3] = bf16_bits_to_float(raw.y >> 16);
-    } else {
-      const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
-      x[0] = bf16_bits_to_float(raw & 0xFFFF);
-      x[1] = bf16_bits_to_float(raw >> 16);
-    }
+    load_bf16_lane<EPL>(src, x);
+    if (which == 0 && rope_cos != nullptr) rope_lane<D, EPL>(x, lane, p, rope_cos, rope_sin);   // K only
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -89,6 +122,43 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
       *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
     }
     if (lane == 0) (which ? v_scale : k_scale)[slot * H + h] = scale;
+  }
+}
+
+// The query side of the FP8-mode RoPE: one warp per (token, q head), the
+// rotated values rounded to bf16 (nearest-even) into q_out (may alias q:
+// each lane writes only what it read, after the whole warp has read).
+template <int D>
+__global__ void __launch_bounds__(256) rope_q_kernel(
+    int T, int B, int Hq, const int32_t* __restrict__ cu, const int32_t* __restrict__ start_pos,
+    const uint16_t* q, const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
+    int rope_max_pos, uint16_t* q_out, int* err) {
+  constexpr int EPL = D / 32;
+  const long w = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<long>(T) * Hq) return;
+  const int t = static_cast<int>(w / Hq);
+  const int b = seq_of_token(cu, B, t);
+  const int p = (start_pos ? __ldg(start_pos + b) : 0) + (t - seq_begin(cu, b));
+  if (p < 0 || p >= rope_max_pos) {
+    if (lane == 0) report_error(err, kDevErrBadLength);
+    return;
+  }
+  float x[EPL];
+  load_bf16_lane<EPL>(q + w * D + lane * EPL, x);
+  rope_lane<D, EPL>(x, lane, p, rope_cos, rope_sin);
+  uint16_t o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const __nv_bfloat16 bv = __float2bfloat16_rn(x[e]);
+    o[e] = *reinterpret_cast<const uint16_t*>(&bv);
+  }
+  uint16_t* dst = q_out + w * D + lane * EPL;
+  if constexpr (EPL == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(o[0] | (static_cast<uint32_t>(o[1]) << 16),
+                                                o[2] | (static_cast<uint32_t>(o[3]) << 16));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = o[0] | (static_cast<uint32_t>(o[1]) << 16);
   }
 }
 
@@ -511,7 +581,17 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
           p.cu_seqlens_q, p.start_pos, p.block_table, static_cast<const uint16_t*>(p.k),
           static_cast<const uint16_t*>(p.v), static_cast<uint8_t*>(p.k_pool),
           static_cast<uint8_t*>(p.v_pool), p.k_scale_pool, p.v_scale_pool, p.slot_mapping,
-          (p.flags & QPKV_WRITE_HND) ? 1 : 0, p.error_word);
+          (p.flags & QPKV_WRITE_HND) ? 1 : 0, p.rope_cos, p.rope_sin, p.rope_max_pos,
+          p.error_word);
+      if (p.q != nullptr) {
+        const long qwarps = static_cast<long>(p.num_tokens) * p.num_heads_q;
+        const int qgrid = static_cast<int>((qwarps * 32 + threads - 1) / threads);
+        auto* qk = p.head_dim == 128 ? rope_q_kernel<128> : rope_q_kernel<64>;
+        qk<<<qgrid, threads, 0, stream>>>(p.num_tokens, p.num_seqs, p.num_heads_q, p.cu_seqlens_q,
+                                          p.start_pos, static_cast<const uint16_t*>(p.q),
+                                          p.rope_cos, p.rope_sin, p.rope_max_pos,
+                                          static_cast<uint16_t*>(p.q_out), p.error_word);
+      }
       return cudaGetLastError();
     }
     case QPKV_WRITE_INT8_BLOCK128_ROPE: {

@@ -1,21 +1,29 @@
-"""Shared helpers of the GPU parity tests: tolerances and comparisons."""
+"""Shared helpers of the GPU parity tests: tolerances and comparisons.
+
+The stated bound for every attention output is, elementwise,
+|got - want| <= 1e-2 (MAX_ABS), with relative L2 <= 5e-3 when P is bf16 or
+fp32 and <= 2e-2 when P enters P.V as FP8.  The outputs are bf16: at
+|want| >= 4 the rounding of the exact result to bf16 alone can move it by
+up to 2^-8 |want| > 1e-2 (half an ulp), so only there the bound adds that
+half ulp.  Below 4 (every output of an N(0,1) workload but a few rows that
+see one or two keys) it is the plain 1e-2.
+
+With QPKV_PARITY_LOG set to a file name, every comparison appends one line
+(test name, max-abs error, rel-L2) to it: the record of achieved errors.
+"""
+import json
+import os
+
 import numpy as np
 
-# Attention output against the float64 oracle: elementwise |got - want| <=
-# ATOL_MAX + BF16_REL * |want| (a bf16 output carries 8 significant bits, so
-# rounding alone moves it by up to 2^-8 of its magnitude) and relative L2
-# with P in bf16 / fp32 (the FP8-P bound is looser); LSE absolute.
-ATOL_MAX = 2e-3
+MAX_ABS = 1e-2
 BF16_REL = 2.0 ** -8
-# The stated bound with P in bf16 (max-abs 1e-2), used where a row may see
-# only a few keys: bf16 rounding of P then moves O by up to ~2^-9 |v|.
-ATOL_P_BF16 = 1e-2
+BF16_EXEMPT_FROM = 4.0
 REL_L2 = 5e-3
 REL_L2_FP8_P = 2e-2
-# Elementwise guard where P enters P.V as two E4M3 terms: below 2^-6 the
-# terms are subnormal, the low term's step is 2^-10, so each key can move O
-# by ~2^-10 |v| (|v| up to ~4 here) beyond the 2^-8 relative rounding.
-ATOL_P_FP8 = 2e-2
+# The FP8 decode additionally meets a tighter bound: its probabilities keep
+# ~12 bits, so the error is the output's bf16 rounding plus at most 2e-3.
+DECODE_TIGHT = 2e-3
 LSE_ATOL = 1e-3
 
 
@@ -32,16 +40,34 @@ def rel_l2(got, want):
     return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
 
 
-def assert_attention_close(got, want, rel=REL_L2, atol=ATOL_MAX, what="O"):
+def _record(what, max_abs, r):
+    path = os.environ.get("QPKV_PARITY_LOG")
+    if not path:
+        return
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    with open(path, "a") as f:
+        f.write(json.dumps({"test": test, "what": what, "max_abs": max_abs, "rel_l2": r}) + "\n")
+
+
+def assert_attention_close(got, want, rel=REL_L2, max_abs=MAX_ABS, tight=None, what="O"):
+    """Elementwise |got - want| <= max_abs (+ bf16 half ulp at |want| >= 4),
+    rel-L2 <= rel, and with ``tight`` also |got - want| - 2^-8 |want| <= tight."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
-    excess = np.abs(got - want) - BF16_REL * np.abs(want)
-    err = float(np.max(excess)) if got.size else 0.0
+    err = np.abs(got - want)
     r = rel_l2(got, want)
-    assert err <= atol and r <= rel, (
-        f"{what}: max(|err| - 2^-8 |want|) {err:.3e} (<= {atol}), rel-L2 {r:.3e} (<= {rel})")
+    m = float(err.max()) if got.size else 0.0
+    _record(what, m, r)
+    allow = np.where(np.abs(want) >= BF16_EXEMPT_FROM, BF16_REL * np.abs(want), 0.0)
+    over = float((err - allow).max()) if got.size else 0.0
+    assert over <= max_abs and r <= rel, (
+        f"{what}: max-abs {m:.3e} (bound {max_abs}, bf16 half ulp added only at |want| >= 4: "
+        f"{over:.3e}), rel-L2 {r:.3e} (<= {rel})")
+    if tight is not None and got.size:
+        t = float((err - BF16_REL * np.abs(want)).max())
+        assert t <= tight, f"{what}: |err| - 2^-8 |want| = {t:.3e} > {tight}"
 
 
 def assert_lse_close(got, want, atol=LSE_ATOL):

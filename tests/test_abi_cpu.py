@@ -202,6 +202,10 @@ def test_write_cache_rejects_before_launch(qlib):
     p.k = fake + 4
     assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1
     p.k = fake
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1   # FP8 mode: q without RoPE tables
+    p.rope_cos = fake
+    assert lib.qpkv_write_cache(ctypes.byref(p), None) == 1   # ... or with one table only
+    p.rope_cos = None
     p.mode = 1                       # INT8 mode: start_pos must be NULL, tables present
     p.num_heads_q = 1
     p.start_pos = fake

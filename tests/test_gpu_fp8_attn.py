@@ -1,6 +1,7 @@
 """GPU parity: dense FP8 attention forward (FA-v3 descale API) against the
 CPU oracle, through the C ABI.  P enters the PV product as E4M3, so the
-output bound is relative L2 <= 2e-2; the lse is checked to 1e-3."""
+output bound is relative L2 <= 2e-2 with the elementwise max-abs 1e-2 of
+every attention path; the lse is checked to 1e-3."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +9,7 @@ import torch
 from oracle import attention as oatt
 from oracle import quant as oquant
 from quantized_paged_kv_varlen_gb300 import synth
-from tests.gpu_util import REL_L2_FP8_P, assert_lse_close, bf16_to_f64, rel_l2
+from tests.gpu_util import REL_L2_FP8_P, assert_attention_close, assert_lse_close, bf16_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -48,9 +49,7 @@ def _run(lib, q8, k8, v8, qd, kd, vd, scale, causal):
 
 
 def _check(got_o, got_lse, want_o, want_lse):
-    assert np.isfinite(got_o).all()
-    r = rel_l2(got_o, want_o)
-    assert r <= REL_L2_FP8_P, f"rel-L2 {r:.3e} > {REL_L2_FP8_P}"
+    assert_attention_close(got_o, want_o, rel=REL_L2_FP8_P)
     assert_lse_close(got_lse, want_lse)
 
 
@@ -105,6 +104,5 @@ def test_fp8_attn_full_size_sampled(lib):
             rows=[(0, s, 0) for s in rows])
         got_o = bf16_to_f64(out[b, rows, h])
         got_lse = lse[b, rows, h].cpu().numpy().astype(np.float64)
-        r = rel_l2(got_o, want_o[0, rows, 0])
-        assert r <= REL_L2_FP8_P, f"(b={b}, h={h}) rel-L2 {r:.3e}"
+        assert_attention_close(got_o, want_o[0, rows, 0], rel=REL_L2_FP8_P, what=f"O(b={b}, h={h})")
         assert_lse_close(got_lse, want_lse[0, rows, 0])

@@ -7,7 +7,7 @@ import torch
 from oracle import cache as ocache
 from oracle import mla as omla
 from quantized_paged_kv_varlen_gb300 import synth
-from tests.gpu_util import ATOL_P_BF16, assert_attention_close, assert_lse_close, bf16_to_f64
+from tests.gpu_util import assert_attention_close, assert_lse_close, bf16_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -139,7 +139,7 @@ def test_mla_shapes(lib, lengths, qps, QN, bs, S, n, mode):
     assert err == 0
     want_o, want_lse = omla.mla_sparse_decode(c["q"], _oracle_pool(c), c["idx"], c["bt"],
                                               c["lengths"], c["cu_q"], c["scale"], sparse_mode=mode)
-    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_attention_close(got_o, want_o)
     assert_lse_close(got_lse, want_lse)
 
 
@@ -157,7 +157,7 @@ def test_mla_empty_lists_and_bad_ids(lib):
     want_o, want_lse = omla.mla_sparse_decode(c["q"], _oracle_pool(c), c["idx"], c["bt"],
                                               c["lengths"], c["cu_q"], c["scale"])
     assert np.all(got_o[0] == 0.0) and np.all(np.isneginf(got_lse[0]))
-    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_attention_close(got_o, want_o)
     assert_lse_close(got_lse, want_lse)
     c["idx"][1, 0, 3] = 300              # = L_kv of sequence 1: out of range
     _, _, err = _run(lib, c, pool, 0)
@@ -189,7 +189,7 @@ def test_mla_full_size_sampled(lib):
             d["q"][t:t + 1].float().cpu().numpy(), mini,
             np.arange(n, dtype=np.int32).reshape(1, 1, n), np.arange(n, dtype=np.int32)[None],
             np.array([n], np.int32), np.array([1], np.int32), d["scale"])
-        assert_attention_close(bf16_to_f64(out[t:t + 1]), want_o, atol=ATOL_P_BF16)
+        assert_attention_close(bf16_to_f64(out[t:t + 1]), want_o)
         assert_lse_close(lse[t:t + 1].cpu().numpy().astype(np.float64), want_lse)
 
 
@@ -220,7 +220,7 @@ def test_mla_block_sparse(lib, lengths, qps, QN, bs, S, n_ids, sbs, mode):
     want_o, want_lse = omla.mla_sparse_decode(c["q"], _oracle_pool(c), idx, c["bt"], c["lengths"],
                                               c["cu_q"], c["scale"], sparse_mode=mode,
                                               sparse_block_size=sbs)
-    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_attention_close(bf16_to_f64(out), want_o)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
 
 
@@ -251,5 +251,5 @@ def test_mla_tnd_keys_through_block_size_one(lib):
     assert int(err.item()) == 0
     want_o, want_lse = omla.mla_sparse_decode(q, rows.reshape(KV_T, 1, 1, 656), idx, bt, lengths,
                                               cu_q, 1.0 / 24.0)
-    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_attention_close(bf16_to_f64(out), want_o)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)

@@ -8,7 +8,7 @@ from oracle import attention as oatt
 from oracle import cache as ocache
 from oracle import rope as orope
 from quantized_paged_kv_varlen_gb300 import synth
-from tests.gpu_util import (ATOL_P_BF16, ATOL_P_FP8, REL_L2_FP8_P, assert_attention_close,
+from tests.gpu_util import (REL_L2_FP8_P, assert_attention_close,
                             assert_lse_close, bf16_to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -122,7 +122,7 @@ def test_write_cache_int8_smooth_k_bit_exact_and_attention(lib):
     assert int(err.item()) == 0
     scale = 1.0 / np.sqrt(128.0)
     want_o, want_lse = oatt.paged_prefill_int8(q8w, qscale, kp, kscale, vp, bt, cu, lengths, scale)
-    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_attention_close(bf16_to_f64(out), want_o)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
     plain = ocache.write_int8_block128_rope(q, k, v, cu, bt, ps, cos, sin, nb, kp0, vp0)
     o_plain, _ = oatt.paged_prefill_int8(plain[3], plain[4], plain[0], plain[2], plain[1], bt, cu,
@@ -194,7 +194,7 @@ def test_prefill_shapes(lib, Lq, Lk, Hq, Hkv, ps, causal):
     got_o, got_lse, err = _run_prefill(lib, c, causal)
     assert err == 0
     want_o, want_lse = _oracle(c, causal)
-    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_attention_close(got_o, want_o)
     assert_lse_close(got_lse, want_lse)
     none = np.isneginf(want_lse)
     assert np.all(got_o[none] == 0.0)
@@ -236,7 +236,7 @@ def test_prefill_ragged_kv(lib, Lq, Lk, Hq, Hkv, causal):
     want_o, want_lse = oatt.paged_prefill_int8(q8, qs, k8.reshape(-1, 1, Hkv, 128), ks,
                                                v_bits.reshape(-1, 1, Hkv, 128), bt, cu_q, Lk,
                                                1.0 / np.sqrt(128.0), causal)
-    assert_attention_close(bf16_to_f64(out), want_o, atol=ATOL_P_BF16)
+    assert_attention_close(bf16_to_f64(out), want_o)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
 
 def test_prefill_zero_scale_blocks(lib):
@@ -248,7 +248,7 @@ def test_prefill_zero_scale_blocks(lib):
     got_o, got_lse, err = _run_prefill(lib, c, True)
     assert err == 0
     want_o, want_lse = _oracle(c, True)
-    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_attention_close(got_o, want_o)
     assert_lse_close(got_lse, want_lse)
 
 
@@ -261,7 +261,7 @@ def test_prefill_running_max_jumps(lib):
     got_o, got_lse, err = _run_prefill(lib, c, True)
     assert err == 0
     want_o, want_lse = _oracle(c, True)
-    assert_attention_close(got_o, want_o, atol=ATOL_P_BF16)
+    assert_attention_close(got_o, want_o)
     assert_lse_close(got_lse, want_lse)
 
 
@@ -309,7 +309,7 @@ def test_prefill_full_size_sampled(lib):
         hi = np.array([h for _, h in rows])
         got_o = bf16_to_f64(out[torch.from_numpy(begin[b] + ti).long(), torch.from_numpy(hi).long()])
         got_l = lse[torch.from_numpy(begin[b] + ti).long(), torch.from_numpy(hi).long()]
-        assert_attention_close(got_o, want_o[ti, hi], atol=ATOL_P_BF16)
+        assert_attention_close(got_o, want_o[ti, hi])
         assert_lse_close(got_l.cpu().numpy().astype(np.float64), want_lse[ti, hi])
 
 
@@ -354,7 +354,7 @@ def test_prefill_fp8_v(lib, Lq, Lk, Hq, Hkv, ps, causal):
     want_o, want_lse = oatt.paged_prefill_int8(c["q8"], c["qs"], c["k_pool"], c["ks"], c["v_codes"],
                                                c["bt"], c["cu"], c["Lk"], 1.0 / np.sqrt(128.0), causal,
                                                v_scale=c["vscale"])
-    assert_attention_close(bf16_to_f64(out), want_o, rel=REL_L2_FP8_P, atol=ATOL_P_FP8)
+    assert_attention_close(bf16_to_f64(out), want_o, rel=REL_L2_FP8_P)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
 
 
@@ -401,5 +401,5 @@ def test_write_cache_int8_v_fp8_bit_exact_and_ragged_prefill(lib):
     assert int(err.item()) == 0
     want_o, want_lse = oatt.paged_prefill_int8(q8w, qscale, kp, kscale, vp, bt, cu, lengths,
                                                1.0 / np.sqrt(128.0), True, v_scale=vscw)
-    assert_attention_close(bf16_to_f64(out), want_o, rel=REL_L2_FP8_P, atol=ATOL_P_FP8)
+    assert_attention_close(bf16_to_f64(out), want_o, rel=REL_L2_FP8_P)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
