@@ -6,55 +6,61 @@
 // tensor], O bf16 BSND, lse (natural log) fp32 [B, Sq, Hq].  Causal masking
 // is bottom-right aligned: key j is visible to query i iff j <= i + Sk - Sq.
 //
-// One persistent CTA per SM, 10 warps:
-//   warp 0     TMA loads: the work item's 128-row Q tile, then its K and V
-//              tiles in the ring order K(0) K(1) K(2) | V(0) K(3) | V(1) ...
-//   warps 1, 10  tcgen05 MMAs, one issuing lane each (QK on warp 1, PV on
-//              warp 10):
-//                S[128 q x 128 k] = Q[128 x D] . K_tile[128 x D]^T   (FP8)
-//                O[128 q x D]   += P[128 q x 128 k] . V_tile[128 k x D]
-//              P is read straight from tensor memory, where the softmax
-//              wrote it into a P buffer as two E4M3 terms hi + lo (K = 256: hi rows, then lo rows, each
-//              against the same V tile), about 8 significant bits;
-//   warps 2-9  online softmax, two threads per query row (TMEM lane): warps
-//              2-5 take the row's keys [0, 64), warps 6-9 keys [64, 128);
-//              the pair combines its maxima through shared memory at a
-//              64-thread named barrier.  The running maximum moves only
-//              when a tile beats it by more than 2^8, then the row's O is
-//              rescaled.  At the end of a work item the same threads write
-//              O / l * vd as bf16 and the lse.
-// TMEM holds two S buffers, two P buffers (64 columns each) and O: QK(t)
-// waits only for the softmax to have read S(t-2), and the softmax writes
-// P(t) once PV(t-2) has read that P buffer, so the in-order tensor pipe
-// never holds QK back behind a late PV.
+// Each persistent CTA (one per SM) runs two 128-row query tiles of one
+// (batch, head) side by side, tiles A = 2p and B = 2p + 1 of a pair, over
+// the same stream of K/V tiles: while one tile's softmax computes its
+// exponentials, the tensor core works on the other tile, and each K/V tile
+// is fetched once for both.  12 warps:
+//   warp 0      TMA: the pair's Q tiles (two slots), K tiles (4-stage ring),
+//               V tiles (2-stage ring), K one step ahead of V
+//   warp 1      tcgen05 MMAs from one thread, per step g of the K/V stream:
+//                 PV_A(g-1) QK_A(g) PV_B(g-1) QK_B(g)
+//               QK: S[128 q x 128 k] = Q . K^T, E4M3 operands (kind::f8f6f4);
+//               PV: O[128 q x 128 d] += P . V, f16 operands (kind::f16) with P
+//               read from tensor memory and V widened from E4M3 (exact)
+//   warps 2-3   widen each V tile from E4M3 to f16, written in the MN-major
+//               operand layout of the PV product (two 64-column halves)
+//   warps 4-7   softmax and epilogue of tile A, one thread per query row
+//   warps 8-11  the same for tile B
+// P is f16 (11 significant bits, range 2^-24 .. 65504): with the lazy
+// running maximum below, p <= 2^8.  The softmax keeps the running maximum
+// until a tile beats it by more than 2^8 (then the row's O is rescaled).
+// TMEM: S_A, S_B, O_A, O_B, 128 columns each; a tile's P (two f16 per
+// column) overwrites the first 64 columns of its S buffer.  The MMAs of the
+// issuing thread run in issue order, so QK_X(g+1) overwrites S_X only after
+// PV_X(g) has read P_X(g), and the commit behind QK_X(g+1) tells the
+// softmax that PV_X(g) is done before it may rescale O_X.
 //
-// Work: a unit is the pair of q tiles (t, n-1-t) of one (batch, head), so
-// every unit costs the same number of causal K/V tiles; units are dealt to
-// the CTAs round-robin in (batch, head) order, so the CTAs running at the
-// same time share a few heads' K/V through L2.
+// Work: a unit is a pair of q tiles of one (batch, head); units are taken
+// in (batch, head)-major order (the CTAs running at the same time share a
+// few heads' K/V through L2) and dealt to the CTAs in a snake order, which
+// evens out the pairs' different causal lengths.
 #include <cmath>
 
 #include "common.cuh"
 #include "internal.h"
-#include "ring_sched.cuh"
 
 namespace qpkv {
 namespace {
 
-constexpr int kT = 128;             // q rows per tile = keys per tile = MMA M and N
-constexpr int kD = 128;             // head dim
-constexpr int kThreads = 352;       // 11 warps
-constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpPv = 10;   // softmax + epilogue: warps 2..9
-constexpr int kSoftmax = 256;       // two threads per query row
-constexpr int kStages = 8;         // K/V ring, 16 KB each
-constexpr int kTileBytes = kT * kD; // one E4M3 tile
-constexpr int kSmem = (2 + kStages) * kTileBytes + 1024;
+constexpr int kT = 128;               // q rows per tile = keys per tile = MMA M and N
+constexpr int kD = 128;               // head dim
+constexpr int kThreads = 384;         // 12 warps
+constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpSoftA = 4, kWarpSoftB = 8;
+constexpr int kConvThreads = 64;
+constexpr int kKStages = 4;           // E4M3 K tiles, 16 KB each
+constexpr int kVStages = 2;           // E4M3 V tiles, 16 KB each
+constexpr int kV16Bufs = 2;           // f16 V tiles, 32 KB each
+constexpr int kTile8 = kT * kD;       // 16 KB
+constexpr int kTile16 = 2 * kT * kD;  // 32 KB: two halves of 64 columns
+constexpr int kHalf16 = kT * 128;     // 16 KB: one half (128 rows of 128 bytes)
+constexpr int kOffQ = 0;                                  // [2 slots][2 tiles] Q
+constexpr int kOffK = kOffQ + 4 * kTile8;
+constexpr int kOffV8 = kOffK + kKStages * kTile8;
+constexpr int kOffV16 = kOffV8 + kVStages * kTile8;
+constexpr int kSmem = kOffV16 + kV16Bufs * kTile16 + 1024;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kSBufs = 2;           // S ring in TMEM: QK(t) waits for the softmax to read S(t-2)
-constexpr int kPBufs = 2;           // P ring in TMEM: P(t) waits for PV(t-2)
-constexpr uint32_t kColS = 0;       // S buffers: columns [0, 128), [128, 256)
-constexpr uint32_t kColP = 256;     // P buffers: columns [256, 320), [320, 384)
-constexpr uint32_t kColO = 384;     // O: columns [384, 512)
+constexpr uint32_t kColS0 = 0, kColO0 = 256;   // S_A, S_B at 0, 128; O_A, O_B at 256, 384
 
 struct AttnArgs {
   int B, Sq, Sk, Hq, Hkv, G;
@@ -72,15 +78,12 @@ struct AttnArgs {
 };
 
 struct Shared {
-  uint64_t full[kStages], empty[kStages];
   uint64_t q_full[2], q_free[2];
-  uint64_t s_full[kSBufs], s_free[kSBufs];   // QK(t) written / read by the softmax
-  uint64_t p_ready[kPBufs];
-  uint64_t pv_done[kPBufs];    // PV step t completes a phase of pv_done[t % 2]
-  uint64_t o_full, o_free;      // one phase per work item
-  uint64_t mma_done[2];         // QK and PV issuers' MMAs complete
-  float pmax[2][2][kT];        // [tile parity][column half][row] partial row maxima
-  float psum[2][kT];           // [column half][row] partial softmax denominators
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t v16_full[kV16Bufs], v16_empty[kV16Bufs];
+  uint64_t s_full[2], p_ready[2], o_full[2];   // per tile A / B
+  uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -112,38 +115,22 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity, int* err) 
   }
 }
 
+// Lane 0 waits, the warp learns the outcome and is ordered after the wait.
+__device__ __forceinline__ bool warp_await(uint64_t* bar, uint32_t parity, Shared& sh, int* err,
+                                           int lane) {
+  int ok = 1;
+  if (lane == 0) ok = awaitb(bar, parity, sh, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 // 2^x by the hardware approximation (relative error ~2^-22; -inf -> 0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-// This CTA's work items in order: units blockIdx.x, +grid, ...; a unit is
-// q tiles t and nq-1-t (t once when they coincide) of one (batch, head).
-struct Items {
-  int unit, second;
-  __device__ __forceinline__ void start() {
-    unit = static_cast<int>(blockIdx.x);
-    second = 0;
-  }
-  __device__ __forceinline__ bool valid(const AttnArgs& a) const { return unit < a.units; }
-  __device__ __forceinline__ void get(const AttnArgs& a, int& b, int& h, int& qt) const {
-    const int bh = unit / a.pairs, t = unit % a.pairs;
-    b = bh / a.Hq;
-    h = bh % a.Hq;
-    qt = a.qt_lo + (second ? a.nq - 1 - t : t);
-  }
-  __device__ __forceinline__ void advance(const AttnArgs& a) {
-    const int t = unit % a.pairs;
-    if (!second && a.nq - 1 - t != t) {
-      second = 1;
-    } else {
-      second = 0;
-      unit += static_cast<int>(gridDim.x);
-    }
-  }
-};
 
 // K/V tiles of q tile qt: keys [0, last] with last the final key any of its
 // rows sees.
@@ -153,38 +140,86 @@ __device__ __forceinline__ int kv_tiles(const AttnArgs& a, int qt) {
   return last < 0 ? 0 : last / kT + 1;
 }
 
+// This CTA's units in order (round r takes unit r * grid + c on even
+// rounds, r * grid + grid - 1 - c on odd ones) and the K/V steps of each.
+struct Walk {
+  int r;                // round of the current unit
+  int u;                // unit index, >= a.units at the end
+  int uc;               // units of this CTA before the current one
+  int b, h, qt;         // qt: tile A; tile B = qt + 1 when has_b
+  int has_b, na, nb, ns;
+  int j;                // step within the unit
+  int g;                // step of this CTA's K/V stream
+  __device__ __forceinline__ void load_unit(const AttnArgs& a) {
+    const int grid = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    u = r * grid + ((r & 1) ? grid - 1 - c : c);
+    if (u >= a.units) return;
+    const int bh = u / a.pairs, p = u % a.pairs;
+    b = bh / a.Hq;
+    h = bh % a.Hq;
+    qt = a.qt_lo + 2 * p;
+    has_b = 2 * p + 1 < a.nq;
+    na = kv_tiles(a, qt);
+    nb = has_b ? kv_tiles(a, qt + 1) : 0;
+    ns = has_b ? nb : na;
+  }
+  __device__ __forceinline__ void start(const AttnArgs& a) {
+    r = 0;
+    uc = 0;
+    j = 0;
+    g = 0;
+    load_unit(a);
+  }
+  __device__ __forceinline__ bool valid(const AttnArgs& a) const { return u < a.units; }
+  __device__ __forceinline__ bool active(int x) const { return x == 0 ? j < na : (has_b && j < nb); }
+  __device__ __forceinline__ int nx(int x) const { return x == 0 ? na : nb; }
+  // advance one step of the stream
+  __device__ __forceinline__ void next(const AttnArgs& a) {
+    ++g;
+    if (++j < ns) return;
+    j = 0;
+    ++r;
+    ++uc;
+    load_unit(a);
+  }
+  // advance to the next step where tile x is active
+  __device__ __forceinline__ void next_active(const AttnArgs& a, int x) {
+    do {
+      next(a);
+    } while (valid(a) && !active(x));
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_attn_kernel(const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* sQ = smem;                       // [2] Q tiles
-  uint8_t* sRing = smem + 2 * kTileBytes;   // [kStages] K or V tiles
   __shared__ Shared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.q_full[i], 1);
+      mbar_init(&sh.q_free[i], 1);
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.p_ready[i], 128);
+      mbar_init(&sh.o_full[i], 1);
     }
-    for (int d = 0; d < 2; ++d) {
-      mbar_init(&sh.q_full[d], 1);
-      mbar_init(&sh.q_free[d], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.k_empty[s], 1);
     }
-    for (int b = 0; b < kSBufs; ++b) {
-      mbar_init(&sh.s_full[b], 1);
-      mbar_init(&sh.s_free[b], kSoftmax);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&sh.v_full[s], 1);
+      mbar_init(&sh.v_empty[s], kConvThreads / 32);
     }
-    for (int b = 0; b < kPBufs; ++b) {
-      mbar_init(&sh.p_ready[b], kSoftmax);
+    for (int s = 0; s < kV16Bufs; ++s) {
+      mbar_init(&sh.v16_full[s], kConvThreads / 32);
+      mbar_init(&sh.v16_empty[s], 1);
     }
-    mbar_init(&sh.o_full, 1);
-    mbar_init(&sh.o_free, kSoftmax);
-    for (int b = 0; b < kPBufs; ++b) mbar_init(&sh.pv_done[b], 1);
-    mbar_init(&sh.mma_done[0], 1);
-    mbar_init(&sh.mma_done[1], 1);
+    mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -200,328 +235,309 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&k_map);
       tma_prefetch_desc(&v_map);
-      Items it;
-      it.start();
-      int ib0 = 0, ib1 = 0, ih0 = 0, ih1 = 0;   // batch and kv head of the items in flight
-      auto open_item = [&](int o) -> int {
-        if (!it.valid(a)) return 0;
-        int b, h, qt;
-        it.get(a, b, h, qt);
-        it.advance(a);
-        if (o & 1) { ib1 = b; ih1 = h / a.G; } else { ib0 = b; ih0 = h / a.G; }
-        const int qb = o & 1;
-        if (!awaitb(&sh.q_free[qb], ((o >> 1) & 1) ^ 1, sh, a.err)) return -1;
-        mbar_arrive_expect_tx(&sh.q_full[qb], kTileBytes);
-        tma_load_4d(sQ + qb * kTileBytes, &q_map, &sh.q_full[qb], 0, h, qt * kT, b);
-        return kv_tiles(a, qt);
-      };
-      int pos = 0;
-      auto emit = [&](int o, int j, bool is_v) -> bool {
-        const int s = pos % kStages;
-        if (!awaitb(&sh.empty[s], ((pos / kStages) & 1) ^ 1, sh, a.err)) return false;
-        mbar_arrive_expect_tx(&sh.full[s], kTileBytes);
-        const int b = (o & 1) ? ib1 : ib0, hk = (o & 1) ? ih1 : ih0;
-        tma_load_4d(sRing + s * kTileBytes, is_v ? &v_map : &k_map, &sh.full[s], 0, hk, j * kT, b);
-        ++pos;
+      Walk kw, vw;
+      kw.start(a);
+      vw.start(a);
+      int ncopies_k = 0, ncopies_v = 0, nq_slots = 0;
+      bool ok = true;
+      // K of step kw (with the unit's Q tiles at its first step)
+      auto issue_k = [&]() -> bool {
+        if (kw.j == 0) {
+          const int slot = kw.uc & 1;
+          if (!awaitb(&sh.q_free[slot], ((kw.uc >> 1) & 1) ^ 1, sh, a.err)) return false;
+          mbar_arrive_expect_tx(&sh.q_full[slot], (1 + kw.has_b) * kTile8);
+          uint8_t* dst = smem + kOffQ + slot * 2 * kTile8;
+          tma_load_4d(dst, &q_map, &sh.q_full[slot], 0, kw.h, kw.qt * kT, kw.b);
+          if (kw.has_b)
+            tma_load_4d(dst + kTile8, &q_map, &sh.q_full[slot], 0, kw.h, (kw.qt + 1) * kT, kw.b);
+          ++nq_slots;
+        }
+        const int s = kw.g % kKStages;
+        if (!awaitb(&sh.k_empty[s], ((kw.g / kKStages) & 1) ^ 1, sh, a.err)) return false;
+        mbar_arrive_expect_tx(&sh.k_full[s], kTile8);
+        tma_load_4d(smem + kOffK + s * kTile8, &k_map, &sh.k_full[s], 0, kw.h / a.G, kw.j * kT, kw.b);
+        ++ncopies_k;
+        kw.next(a);
         return true;
       };
-      RingSched q{0, 0, 0, 0, 0, 0, 0, false, 3};
-      q.ntl0 = open_item(0);
-      if (q.ntl0 > 0) {
-        while (true) {
-          const int step = ring_next(q, open_item);
-          if (step == kStepK) {
-            if (!emit(q.ko, q.kj, false)) break;
-            ++q.kj;
-            ++q.lead;
-          } else if (step == kStepV) {
-            if (!emit(q.vo, q.vj, true)) break;
-            ++q.vj;
-            --q.lead;
-          } else {
-            break;
-          }
-        }
+      auto issue_v = [&]() -> bool {
+        const int s = vw.g % kVStages;
+        if (!awaitb(&sh.v_empty[s], ((vw.g / kVStages) & 1) ^ 1, sh, a.err)) return false;
+        mbar_arrive_expect_tx(&sh.v_full[s], kTile8);
+        tma_load_4d(smem + kOffV8 + s * kTile8, &v_map, &sh.v_full[s], 0, vw.h / a.G, vw.j * kT, vw.b);
+        ++ncopies_v;
+        vw.next(a);
+        return true;
+      };
+      if (kw.valid(a)) ok = issue_k();
+      while (ok && vw.valid(a)) {
+        if (kw.valid(a)) ok = issue_k();
+        if (ok) ok = issue_v();
       }
-      // this CTA's copies in flight land before it exits
-      for (int i = pos > kStages ? pos - kStages : 0; i < pos; ++i)
-        drain(&sh.full[i % kStages], (i / kStages) & 1, a.err);
+      // this CTA's copies still in flight land before it exits
+      for (int i = ncopies_k > kKStages ? ncopies_k - kKStages : 0; i < ncopies_k; ++i)
+        drain(&sh.k_full[i % kKStages], (i / kKStages) & 1, a.err);
+      for (int i = ncopies_v > kVStages ? ncopies_v - kVStages : 0; i < ncopies_v; ++i)
+        drain(&sh.v_full[i % kVStages], (i / kVStages) & 1, a.err);
+      for (int i = nq_slots > 2 ? nq_slots - 2 : 0; i < nq_slots; ++i)
+        drain(&sh.q_full[i & 1], (i >> 1) & 1, a.err);
     }
     __syncwarp();
-  } else if (warp == kWarpMma || warp == kWarpPv) {
+  } else if (warp == kWarpMma) {
     // -------------------------------------------------------------- MMA
-    // Lane 0 of warp 1 issues the QK MMAs, lane 0 of warp 10 the PV MMAs;
-    // both walk the ring schedule and skip the other side's stages.  QK(t)
-    // overwrites the S buffer that held P(t-3), so it first waits for
-    // PV(t-3) to complete.
-    const bool is_qk = warp == kWarpMma;
     if (lane == 0) {
       const uint32_t idesc_qk = make_idesc(kFmtE4M3, kFmtE4M3, 0, 0, kT, kT);
-      const uint32_t idesc_pv = make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, kT, kD);
-      // descriptors at offset 0 of each region; an operand at byte offset x
-      // adds x >> 4 to the start-address field
-      const uint64_t qdesc0 = make_smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
-      const uint64_t kdesc0 = make_smem_desc(smem_u32(sRing), 16, 1024, kSwizzle128B);
-      const uint64_t vdesc0 = make_smem_desc(smem_u32(sRing), 0, 1024, kSwizzle128B);
-      Items it;
-      it.start();
-      auto open_item = [&](int o) -> int {
-        if (!it.valid(a)) return 0;
-        int b, h, qt;
-        it.get(a, b, h, qt);
-        it.advance(a);
-        if (is_qk && !awaitb(&sh.q_full[o & 1], (o >> 1) & 1, sh, a.err)) return -1;
-        return kv_tiles(a, qt);
-      };
-      int pos = 0, st = 0, pvc = 0;
-      auto qk = [&](int o, int j, int ntl) -> bool {
-        const int sb = st % kSBufs;
-        const int s = pos % kStages;
-        if (st >= kSBufs &&
-            !awaitb(&sh.s_free[sb], ((st - kSBufs) / kSBufs) & 1, sh, a.err))   // S(st - 2) read
-          return false;
-        if (!awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err)) return false;
+      const uint32_t idesc_pv = make_idesc(kFmtF16, kFmtF16, 0, 1, kT, kD);
+      const uint64_t qdesc0 = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024, kSwizzle128B);
+      const uint64_t kdesc0 = make_smem_desc(smem_u32(smem + kOffK), 16, 1024, kSwizzle128B);
+      // MN-major f16 V: two 64-column atoms 16 KB apart, 16 key rows (2 KB)
+      // per K = 16 step
+      const uint64_t vdesc0 = make_smem_desc(smem_u32(smem + kOffV16), kHalf16, 1024, kSwizzle128B);
+      Walk w;
+      w.start(a);
+      int cnt_p[2] = {0, 0};    // PVs issued per tile (p_ready phases)
+      // the pending PV of each tile: its step's g and j, whether it ends the
+      // tile's unit, whether it is the last reader of its V buffer
+      int pend_g[2] = {-1, -1}, pend_j[2] = {0, 0}, pend_last[2] = {0, 0}, pend_rel[2] = {0, 0};
+      bool ok = true;
+      auto pv = [&](int x) -> bool {
+        const int g = pend_g[x];
+        if (!awaitb(&sh.p_ready[x], cnt_p[x] & 1, sh, a.err)) return false;
+        if (!awaitb(&sh.v16_full[g % kV16Bufs], (g / kV16Bufs) & 1, sh, a.err)) return false;
         tc_fence_after_sync();
-        const uint64_t da0 = qdesc0 + static_cast<uint64_t>(((o & 1) * kTileBytes) >> 4);
-        const uint64_t db0 = kdesc0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
+        const uint64_t db = vdesc0 + static_cast<uint64_t>(((g % kV16Bufs) * kTile16) >> 4);
+        const uint32_t cs = kColS0 + 128u * x, co = kColO0 + 128u * x;
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          tc_mma_f16_tmem_a(tmem + co, tmem + cs + 8 * kk,
+                            db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
+                            (pend_j[x] > 0 || kk > 0) ? 1u : 0u);
+        if (pend_rel[x]) tc_commit(&sh.v16_empty[g % kV16Bufs]);
+        if (pend_last[x]) tc_commit(&sh.o_full[x]);
+        ++cnt_p[x];
+        pend_g[x] = -1;
+        return true;
+      };
+      auto qk = [&](int x) -> bool {
+        const int slot = w.uc & 1, s = w.g % kKStages;
+        if (w.j == 0 && !awaitb(&sh.q_full[slot], (w.uc >> 1) & 1, sh, a.err)) return false;
+        if (!awaitb(&sh.k_full[s], (w.g / kKStages) & 1, sh, a.err)) return false;
+        tc_fence_after_sync();
+        const uint64_t da = qdesc0 + static_cast<uint64_t>(((slot * 2 + x) * kTile8) >> 4);
+        const uint64_t db = kdesc0 + static_cast<uint64_t>((s * kTile8) >> 4);
+        const uint32_t cs = kColS0 + 128u * x;
 #pragma unroll
         for (int kk = 0; kk < kD / 32; ++kk)
-          tc_mma_f8(tmem + kColS + sb * kT, da0 + 2 * kk, db0 + 2 * kk, idesc_qk, kk > 0);
-        tc_commit(&sh.empty[s]);
-        tc_commit(&sh.s_full[sb]);
-        if (j == ntl - 1) tc_commit(&sh.q_free[o & 1]);
-        ++pos;
-        ++st;
-        return true;
-      };
-      auto pv = [&](int o, int j, int ntl) -> bool {
-        const int sb = pvc % kPBufs;
-        const int s = pos % kStages;
-        // O is single-buffered: item o-1's epilogue has read it
-        if (j == 0 && !awaitb(&sh.o_free, (o & 1) ^ 1, sh, a.err)) return false;
-        if (!awaitb(&sh.p_ready[sb], (pvc / kPBufs) & 1, sh, a.err) ||
-            !awaitb(&sh.full[s], (pos / kStages) & 1, sh, a.err))
-          return false;
-        tc_fence_after_sync();
-        const uint64_t db0 = vdesc0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
-        // K = 256: the hi terms of keys 0..127, then the lo terms, both
-        // against the same V rows
-#pragma unroll
-        for (int kk = 0; kk < 2 * kT / 32; ++kk)
-          tc_mma_f8_tmem_a(tmem + kColO, tmem + kColP + sb * 64 + 8 * kk,
-                           db0 + (32 * kD / 16) * (kk & 3), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&sh.empty[s]);
-        tc_commit(&sh.pv_done[sb]);
-        if (j == ntl - 1) tc_commit(&sh.o_full);
-        ++pos;
-        ++pvc;
-        return true;
-      };
-      RingSched q{0, 0, 0, 0, 0, 0, 0, false, 3};
-      q.ntl0 = open_item(0);
-      if (q.ntl0 > 0) {
-        while (true) {
-          const int step = ring_next(q, open_item);
-          if (step == kStepK) {
-            if (is_qk) {
-              if (!qk(q.ko, q.kj, q.ntl(q.ko))) break;
-            } else {
-              ++pos;
-            }
-            ++q.kj;
-            ++q.lead;
-          } else if (step == kStepV) {
-            if (!is_qk) {
-              if (!pv(q.vo, q.vj, q.ntl(q.vo))) break;
-            } else {
-              ++pos;
-            }
-            ++q.vj;
-            --q.lead;
-          } else {
-            break;
-          }
+          tc_mma_f8(tmem + cs, da + 2 * kk, db + 2 * kk, idesc_qk, kk > 0);
+        tc_commit(&sh.s_full[x]);
+        // the last reader of this K stage (and, at the unit's end, of the Q slot)
+        const bool last_reader = x == 1 || !w.active(1);
+        if (last_reader) {
+          tc_commit(&sh.k_empty[s]);
+          if (w.j == w.ns - 1) tc_commit(&sh.q_free[slot]);
         }
+        pend_g[x] = w.g;
+        pend_j[x] = w.j;
+        pend_last[x] = w.j == w.nx(x) - 1;
+        pend_rel[x] = last_reader;
+        return true;
+      };
+      // step g: PV_A(pending) QK_A(g) PV_B(pending) QK_B(g)
+      while (ok && w.valid(a)) {
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (pend_g[x] >= 0) ok = pv(x);
+          if (ok && w.active(x)) ok = qk(x);
+        }
+        if (ok) w.next(a);
       }
+      for (int x = 0; x < 2 && ok; ++x)
+        if (pend_g[x] >= 0) ok = pv(x);
       // every MMA issued here completes before TMEM is released
-      tc_commit(&sh.mma_done[is_qk ? 0 : 1]);
-      drain(&sh.mma_done[is_qk ? 0 : 1], 0, a.err);
+      tc_commit(&sh.mma_done);
+      drain(&sh.mma_done, 0, a.err);
     }
     __syncwarp();
-  } else if (warp < kWarpPv) {
+  } else if (warp < kWarpSoftA) {
+    // ---------------------------------------- V: E4M3 -> f16 (exact)
+    // Input: a TMA tile [128 keys][128 bytes], 128-byte swizzle.  Output:
+    // two halves [128 keys][64 f16] (dims 0-63, 64-127), 128-byte swizzle.
+    const int ct = tid - kWarpConv0 * 32;   // 0..63
+    Walk w;
+    w.start(a);
+    while (w.valid(a)) {
+      const int g = w.g, s = g % kVStages, bsel = g % kV16Bufs;
+      if (!warp_await(&sh.v_full[s], (g / kVStages) & 1, sh, a.err, lane)) break;
+      if (!warp_await(&sh.v16_empty[bsel], ((g / kV16Bufs) & 1) ^ 1, sh, a.err, lane)) break;
+      const uint8_t* src = smem + kOffV8 + s * kTile8;
+      uint8_t* dst = smem + kOffV16 + bsel * kTile16;
+#pragma unroll 4
+      for (int k = 0; k < (kT * 8) / kConvThreads; ++k) {
+        const int i = ct + kConvThreads * k;
+        const int row = i >> 3, c = i & 7;
+        const uint4 xv = *reinterpret_cast<const uint4*>(src + row * 128 + (((c ^ row) & 7) << 4));
+        const uint32_t wv[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          o[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(wv[q] & 0xFFFFu));
+          o[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wv[q] >> 16));
+        }
+        uint8_t* base = dst + (c >> 2) * kHalf16 + row * 128;
+        const int c0 = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(base + (((c0 ^ row) & 7) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(base + ((((c0 + 1) ^ row) & 7) << 4)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();   // generic stores, read by the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh.v_empty[s]);
+        mbar_arrive(&sh.v16_full[bsel]);
+      }
+      w.next(a);
+    }
+  } else {
     // ---------------------------------------------- softmax and epilogue
-    // Two threads per query row: warps 2-5 take columns [0, 64), warps
-    // 6-9 columns [64, 128) of the same TMEM lanes; a row's pair meets at a
-    // 64-thread named barrier to combine the row maximum.
-    const int sw = warp & 3;                      // TMEM lane quarter
-    const int half = (warp - 2) >> 2;             // column half
-    const int r = sw * 32 + lane;                 // tile row = TMEM lane
-    const uint32_t bar_id = 1 + sw;               // the pair's named barrier
-    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-    Items it;
-    it.start();
-    int st = 0;
-    for (int o = 0; it.valid(a); ++o) {
-      int b, h, qt;
-      it.get(a, b, h, qt);
-      it.advance(a);
-      const int nkv = kv_tiles(a, qt);
-      const int hk = h / a.G;
-      // logit multiplier (log2 units); kept above 0 so that -inf * sc stays -inf
-      const float sc = fmaxf(a.scale_log2 * __ldg(a.qd + b * a.Hq + h) * __ldg(a.kd + b * a.Hkv + hk),
-                             1e-30f);
+    const int x = warp < kWarpSoftB ? 0 : 1;      // tile A or B
+    const int r = (warp & 3) * 32 + lane;         // tile row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t srow = tmem + lane_base + kColS0 + 128u * x;
+    const uint32_t orow = tmem + lane_base + kColO0 + 128u * x;
+    Walk w;
+    w.start(a);
+    if (w.valid(a) && !w.active(x)) w.next_active(a, x);
+    int cnt = 0, units = 0;
+    float m = -INFINITY, l = 0.f;
+    while (w.valid(a)) {
+      const int qt = w.qt + x;
       const int row = qt * kT + r;
+      const int hk = w.h / a.G;
       // last key this row sees (may be negative: none)
       const int lim = a.causal ? min(a.Sk - 1, row + a.Sk - a.Sq) : a.Sk - 1;
-      float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nkv; ++j) {
-        const int sb = st % kSBufs;
-        awaitb(&sh.s_full[sb], (st / kSBufs) & 1, sh, a.err);
-        __syncwarp();   // converged before the .sync.aligned TMEM accesses
-        tc_fence_after_sync();
-        const uint32_t srow = tmem + lane_base + kColS + sb * kT;
-        const int climit = lim - j * kT - 64 * half;   // this half's columns c <= climit are visible
-        const bool whole = climit >= 63;
-        uint32_t v0[32], v1[32];
-        tmem_ld32(srow + 64 * half, v0);
-        tmem_ld32(srow + 64 * half + 32, v1);
-        tmem_ld_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&sh.s_free[sb]);   // QK(st + 2) may overwrite this S buffer
-        // raw logits; masked keys -inf (sc > 0, so max and order carry over)
-        float x[64];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(v0[i]);
-          x[32 + i] = __uint_as_float(v1[i]);
-        }
-        if (!whole) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c > climit) x[c] = -INFINITY;
-        }
-        // row maximum in eight independent chains (a single chain of 64
-        // dependent max operations is latency-bound)
-        float xm8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xm8[i] = x[i];
-#pragma unroll
-        for (int c = 8; c < 64; ++c) xm8[c & 7] = fmaxf(xm8[c & 7], x[c]);
-        float xm = fmaxf(fmaxf(fmaxf(xm8[0], xm8[1]), fmaxf(xm8[2], xm8[3])),
-                         fmaxf(fmaxf(xm8[4], xm8[5]), fmaxf(xm8[6], xm8[7])));
-        sh.pmax[st & 1][half][r] = xm;
-        named_barrier(bar_id, 64);
-        xm = fmaxf(xm, sh.pmax[st & 1][half ^ 1][r]);
-        const float mx = xm * sc;   // the row's tile maximum in log2 units
-        // ---- running maximum, moved only by more than 2^8; then O is
-        // rescaled.  Both threads of a row take the same decision; the
-        // TMEM access is warp-wide (.sync.aligned), rows that keep their
-        // maximum use the factor 1.
-        float f = 1.f;
-        bool need = false;
-        if (mx > m + kRescaleLog2) {
-          if (m > -INFINITY) {
-            f = exp2f(m - mx);
-            l *= f;
-            need = true;
-          }
-          m = mx;
-        }
-        if (__any_sync(0xffffffffu, need)) {
-          // the previous PV of this item must have finished writing O (PV
-          // step t-1 may still be in flight; t+1 cannot be done)
-          awaitb(&sh.pv_done[(st - 1) % kPBufs], ((st - 1) / kPBufs) & 1, sh, a.err);
-          __syncwarp();
-          tc_fence_after_sync();
-          const uint32_t orow = tmem + lane_base + kColO + 64 * half;
-#pragma unroll 1
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t w[32];
-            tmem_ld32(orow + 32 * c2, w);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * f);
-            tmem_st32(orow + 32 * c2, w);
-            tmem_st_wait();
-          }
-        }
-        // ---- P = 2^(x sc - m) as two E4M3 terms hi + lo (about 8
-        // significant bits, built in f16x2), packed four keys per column
-        const float nm = m > -INFINITY ? -m : 0.f;   // a row that sees no key gets p = 0
-        uint32_t pk[16], pl[16];
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sum chains
-#pragma unroll
-        for (int wq = 0; wq < 16; ++wq) {
-          float p[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            p[e] = fast_exp2(fmaf(x[4 * wq + e], sc, nm));
-            ls[e] += p[e];
-          }
-          const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
-          const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
-          const uint16_t h01 = f16x2_to_e4m3x2(f01);
-          const uint16_t h23 = f16x2_to_e4m3x2(f23);
-          const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(f01, e4m3x2_to_f16x2(h01)));
-          const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(f23, e4m3x2_to_f16x2(h23)));
-          pk[wq] = h01 | (static_cast<uint32_t>(h23) << 16);
-          pl[wq] = l01 | (static_cast<uint32_t>(l23) << 16);
-        }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // the P buffer of step st was read by PV(st - 2)
-        const int pb = st % kPBufs;
-        if (st >= kPBufs) {
-          awaitb(&sh.pv_done[pb], ((st - kPBufs) / kPBufs) & 1, sh, a.err);
-          __syncwarp();
-          tc_fence_after_sync();
-        }
-        const uint32_t prow = tmem + lane_base + kColP + pb * 64;
-        tmem_st16(prow + 16 * half, pk);        // columns [0, 32): hi terms
-        tmem_st16(prow + 32 + 16 * half, pl);   // columns [32, 64): lo terms
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&sh.p_ready[pb]);
-        ++st;
+      if (w.j == 0) {
+        m = -INFINITY;
+        l = 0.f;
       }
-      // ---- the row's denominator: this half's partial sum plus the other's
-      sh.psum[half][r] = l;
-      named_barrier(bar_id, 64);
-      const float lt = l + sh.psum[half ^ 1][r];
-      named_barrier(bar_id, 64);   // psum may be rewritten at the next item
-      // ---- epilogue: this half's 64 columns of O / l * vd -> bf16, and the
-      // lse, once the item's last PV has landed; then O is free for item o+2
-      const float vd = __ldg(a.vd + b * a.Hkv + hk);
-      const float so = lt > 0.f ? vd / lt : 0.f;
-      awaitb(&sh.o_full, o & 1, sh, a.err);
-      __syncwarp();
+      // logit multiplier (log2 units); kept above 0 so that -inf * sc stays -inf
+      const float sc = fmaxf(a.scale_log2 * __ldg(a.qd + w.b * a.Hq + w.h) *
+                                 __ldg(a.kd + w.b * a.Hkv + hk),
+                             1e-30f);
+      const int climit = lim - w.j * kT;          // columns c <= climit are visible
+      if (!awaitb(&sh.s_full[x], cnt & 1, sh, a.err)) break;
+      __syncwarp();   // converged before the .sync.aligned TMEM accesses
       tc_fence_after_sync();
-      const bool write = row < a.Sq;
-      uint16_t* out = a.o + ((static_cast<size_t>(b) * a.Sq + row) * a.Hq + h) * kD + 64 * half;
-      const uint32_t orow = tmem + lane_base + kColO + 64 * half;
+      const bool whole = __all_sync(0xffffffffu, climit >= kT - 1);
+      // pass 1: the row maximum of the raw scores (masked keys -inf; sc > 0
+      // keeps the order)
+      float xm = -INFINITY;
 #pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(orow + 32 * c2, v);
+        tmem_ld32(srow + 32 * c, v);
+        tmem_ld_wait();
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (whole) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            m4[i & 3] = fmaxf(m4[i & 3], 32 * c + i <= climit ? __uint_as_float(v[i]) : -INFINITY);
+        }
+        xm = fmaxf(xm, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+      }
+      const float mx = xm * sc;   // the row's tile maximum in log2 units
+      float f = 1.f;
+      bool need = false;
+      if (mx > m + kRescaleLog2) {
+        if (m > -INFINITY) {
+          f = exp2f(m - mx);
+          l *= f;
+          need = true;
+        }
+        m = mx;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        // the previous PV of this tile is complete (it was issued before the
+        // QK whose commit the s_full wait saw); rows that keep their maximum
+        // use the factor 1
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(orow + 32 * c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+          tmem_st32(orow + 32 * c, v);
+          tmem_st_wait();
+        }
+      }
+      // pass 2: P = 2^(x sc - m) as f16 pairs into the first 64 columns of S
+      // (chunk c of 32 keys -> columns [16c, 16c + 16), all already read)
+      const float nm = m > -INFINITY ? -m : 0.f;   // a row that sees no key gets p = 0
+      float ls[2] = {0.f, 0.f};
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(srow + 32 * c, v);
         tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 t =
-              __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * so, __uint_as_float(v[2 * i + 1]) * so);
-          pk[i] = *reinterpret_cast<const uint32_t*>(&t);
+          float x0 = fmaf(__uint_as_float(v[2 * i]), sc, nm);
+          float x1 = fmaf(__uint_as_float(v[2 * i + 1]), sc, nm);
+          if (!whole) {
+            x0 = 32 * c + 2 * i <= climit ? x0 : -INFINITY;
+            x1 = 32 * c + 2 * i + 1 <= climit ? x1 : -INFINITY;
+          }
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          ls[0] += p0;
+          ls[1] += p1;
+          pk[i] = f32x2_to_f16x2(p1, p0);
         }
-        if (write) {
-          uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        tmem_st16(srow + 16 * c, pk);
       }
+      l += ls[0] + ls[1];
+      tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&sh.o_free);
-      if (write && half == 0 && a.lse != nullptr)
-        a.lse[(static_cast<size_t>(b) * a.Sq + row) * a.Hq + h] =
-            lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+      mbar_arrive(&sh.p_ready[x]);
+      ++cnt;
+      if (w.j == w.nx(x) - 1) {
+        // ---- epilogue: O / l * vd -> bf16, and the lse, once the tile's
+        // last PV has landed
+        const float vd = __ldg(a.vd + w.b * a.Hkv + hk);
+        const float so = l > 0.f ? vd / l : 0.f;
+        if (!awaitb(&sh.o_full[x], units & 1, sh, a.err)) break;
+        __syncwarp();
+        tc_fence_after_sync();
+        const bool write = row < a.Sq;
+        uint16_t* out = a.o + ((static_cast<size_t>(w.b) * a.Sq + row) * a.Hq + w.h) * kD;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(orow + 32 * c, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * so,
+                                                            __uint_as_float(v[2 * i + 1]) * so);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&t2);
+          }
+          if (write) {
+            uint4* o4 = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        tc_fence_before_sync();
+        if (write && a.lse != nullptr)
+          a.lse[(static_cast<size_t>(w.b) * a.Sq + row) * a.Hq + w.h] =
+              l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        ++units;
+      }
+      w.next_active(a, x);
     }
   }
   tc_fence_before_sync();
