@@ -211,6 +211,8 @@ class DecodeBench:
         self.plan.replan(stream=self.copy_stream)
         q.write_cache_fp8(self.k_new, self.v_new, self.cu_new, self.bt, self.k_pool, self.v_pool,
                           self.ks, self.vs, start_pos=self.start_pos, error_word=self.err)
+        # the stream waits for the plan copy before the timed attend launch
+        self.plan.wait_ready()
         if ev_attend is not None:
             ev_attend[0].record()
         self.plan.attend(self.qry, self.k_pool, self.v_pool, self.ks, self.vs, self.bt,

@@ -400,10 +400,14 @@ class DecodePlan:
     """Plan/run split for paged FP8 decode (one query token per request).
 
     ``DecodePlan(seqlens_kv, Hq, Hkv, page_size, head_dim)`` sizes and
-    allocates the workspaces (torch device memory plus a page-locked host
-    buffer) and runs the library's host planner, which copies the work list
-    to the device on the current stream.  ``run`` launches the split-KV
-    kernel and the log-sum-exp merge.
+    allocates the workspaces (torch device memory plus page-locked host
+    buffers) and runs the library's host planner, which copies the work list
+    to the device.  ``run`` launches the split-KV kernel and the log-sum-exp
+    merge (``attend`` and ``merge`` launch them one at a time).
+
+    The work list lives in one of two device buffers that alternate between
+    plans, so the copy of a new plan never waits for, nor overwrites, the
+    list that the previous run's kernels are still reading.
     """
 
     def __init__(self, seqlens_kv, num_qo_heads, num_kv_heads, page_size, head_dim,
@@ -426,56 +430,82 @@ class DecodePlan:
                                                self.D, self.num_sms, ctypes.byref(ib),
                                                ctypes.byref(fb)), "qpkv_decode_workspace_sizes")
         self.int_bytes, self.float_bytes = ib.value, fb.value
-        self.int_ws = torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, device=device)
+        n = max(self.int_bytes, 256)
+        self._int_ws = [torch.empty(n, dtype=torch.uint8, device=device) for _ in range(2)]
         self.float_ws = torch.empty(max(self.float_bytes, 256), dtype=torch.uint8, device=device)
-        # two page-locked staging buffers: the host rewrites one only after the
-        # stream has copied out of it (an event recorded behind the copy)
-        self._pinned = [torch.empty(max(self.int_bytes, 256), dtype=torch.uint8, pin_memory=True)
-                        for _ in range(2)]
+        # per buffer i: the page-locked staging of its plan (rewritten only
+        # after the copy out of it is done), the plan_info, the event behind
+        # that copy, and the event behind the last launch that read it
+        self._pinned = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        self._info = [(ctypes.c_int64 * PLAN_INFO_LEN)() for _ in range(2)]
         self._copied = [None, None]
-        self._which = 0
-        self._ready = None                   # copy to wait for before the next run
-        self._released = torch.cuda.Event()  # the last run / attend / merge done with int_ws
-        self._released_set = False
-        self.plan_info = (ctypes.c_int64 * PLAN_INFO_LEN)()
+        self._released = [None, None]
+        self._ready = None        # a side-stream copy the next launch must wait for
+        self._cur = 1
         self.replan()
 
-    def replan(self, stream=None):
-        """Run the host planner again and copy the work list to the device
+    @property
+    def plan_info(self):
+        return self._info[self._cur]
+
+    @property
+    def int_ws(self):
+        return self._int_ws[self._cur]
+
+    def replan(self, seqlens_kv=None, stream=None):
+        """Run the host planner again (for new per-request lengths when
+        ``seqlens_kv`` is given; they must fit the workspaces sized at
+        construction) and copy the work list into the other device buffer
         (the per-step cost of the plan/run split).  The copy runs on the
-        current stream, or on ``stream`` (a torch.cuda.Stream): there it
-        waits until the previous run / attend / merge is done with the int
-        workspace, and the next run / attend waits for it, so the copy can
-        overlap other work on the current stream."""
+        current stream, or on ``stream`` (a torch.cuda.Stream), where it
+        overlaps other work on the current stream: it waits only for the
+        launches that read that buffer two plans ago, and the next attend /
+        merge / run waits for it."""
         torch = _torch()
+        import numpy as np
         lib = load()
-        buf = self._pinned[self._which]
-        if self._copied[self._which] is not None:
-            self._copied[self._which].synchronize()
+        if seqlens_kv is not None:
+            lens = np.ascontiguousarray(np.asarray(seqlens_kv, dtype=np.int32))
+            if lens.shape != self.lens.shape:
+                raise ValueError("seqlens_kv must keep the batch size")
+            ib, fb = ctypes.c_size_t(), ctypes.c_size_t()
+            _check(lib.qpkv_decode_workspace_sizes(lens.ctypes.data, self.B, self.Hq, self.Hkv,
+                                                   self.D, self.num_sms, ctypes.byref(ib),
+                                                   ctypes.byref(fb)), "qpkv_decode_workspace_sizes")
+            if ib.value > self._int_ws[0].numel() or fb.value > self.float_ws.numel():
+                raise ValueError("new lengths need larger workspaces than this plan holds")
+            self.lens = lens
+        i = self._cur ^ 1
+        if self._copied[i] is not None:
+            self._copied[i].synchronize()       # the host may rewrite pinned[i]
         s = stream if stream is not None else torch.cuda.current_stream()
-        if stream is not None and self._released_set:
-            stream.wait_event(self._released)
+        if self._released[i] is not None:
+            s.wait_event(self._released[i])     # the readers of int_ws[i] are done
+        buf, info = self._pinned[i], self._info[i]
         _check(lib.qpkv_decode_plan(self.lens.ctypes.data, self.B, self.Hq, self.Hkv,
                                     self.page_size, self.D, self.num_sms,
                                     ctypes.c_void_p(buf.data_ptr()), buf.numel(),
-                                    _ptr(self.int_ws), self.int_ws.numel(), self.plan_info,
+                                    _ptr(self._int_ws[i]), self._int_ws[i].numel(), info,
                                     ctypes.c_void_p(s.cuda_stream)), "qpkv_decode_plan")
-        _check(lib.qpkv_decode_plan_set_kv_layout(self.plan_info, KV_LAYOUTS[self.kv_layout]),
+        _check(lib.qpkv_decode_plan_set_kv_layout(info, KV_LAYOUTS[self.kv_layout]),
                "qpkv_decode_plan_set_kv_layout")
         ev = torch.cuda.Event()
         ev.record(s)
-        self._copied[self._which] = ev
+        self._copied[i] = ev
         self._ready = ev if stream is not None else None
-        self._which ^= 1
+        self._cur = i
 
-    def _before_run(self):
+    def wait_ready(self):
+        """Make the current stream wait for a pending side-stream plan copy
+        (attend, merge and run do this themselves)."""
         if self._ready is not None:
             _torch().cuda.current_stream().wait_event(self._ready)
             self._ready = None
 
     def _after_run(self):
-        self._released.record()
-        self._released_set = True
+        ev = _torch().cuda.Event()
+        ev.record()
+        self._released[self._cur] = ev
 
     @property
     def num_items(self):
@@ -515,7 +545,7 @@ class DecodePlan:
         self._check_run(q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table)
         if out is None:
             out = torch.empty_like(q)
-        self._before_run()
+        self.wait_ready()
         _check(lib.qpkv_decode_run(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
                                    _ptr(self.int_ws), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                    _ptr(k_scale_pool), _ptr(v_scale_pool), k_pool.shape[0],
@@ -529,7 +559,7 @@ class DecodePlan:
                error_word=None):
         lib = load()
         self._check_run(q, k_pool, v_pool, k_scale_pool, v_scale_pool, block_table)
-        self._before_run()
+        self.wait_ready()
         _check(lib.qpkv_decode_attend(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
                                       _ptr(self.int_ws), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                       _ptr(k_scale_pool), _ptr(v_scale_pool), k_pool.shape[0],
@@ -540,6 +570,7 @@ class DecodePlan:
 
     def merge(self, out, lse=None):
         lib = load()
+        self.wait_ready()
         _check(lib.qpkv_decode_merge(self.plan_info, _ptr(self.float_ws), self.float_ws.numel(),
                                      _ptr(self.int_ws), _ptr(out), _ptr(lse), _stream()),
                "qpkv_decode_merge")

@@ -29,13 +29,12 @@
 //   warp 1     QK MMAs  S[128 q x 128 k] = Q16 . K16^T        (kind::f16)
 //   warp 10    PV MMAs  O[128 q x 128 d] += P . V, and the V copies (one
 //              box per page and 64-column half for bf16 V, one per page
-//              for E4M3 V), one key tile ahead.  bf16 V: kind::f16 with P
-//              (bf16) read from tensor memory, where the softmax wrote it
-//              over columns [0, 32) and [64, 96) of its S buffer.  E4M3 V
-//              (the V8 instantiation): kind::f8f6f4 with P as two E4M3
-//              terms hi + lo in columns [64 h, 64 h + 16) and
-//              [64 h + 16, 64 h + 32) of column half h, the per-channel V
-//              scales applied in the epilogue
+//              for E4M3 V), one key tile ahead.  kind::f16 with P read from
+//              tensor memory, where the softmax wrote it over columns
+//              [0, 32) and [64, 96) of its S buffer: bf16 P against bf16 V,
+//              or (the V8 instantiation, E4M3 V) f16 P against V widened
+//              in place from E4M3 to f16 (exact) by this warp, with the
+//              per-channel V scales applied in the epilogue
 //   warps 2-9  online softmax, two threads per query row (columns [0, 64)
 //              on warps 2-5, [64, 128) on warps 6-9), lazy maximum (moves
 //              only by more than 2^8, then O is rescaled), and the epilogue
@@ -358,8 +357,8 @@ struct TileWalk {
   }
 };
 
-// V8: V is E4M3 with per-(sequence, head, channel) scales and P.V runs as
-// an FP8 product (P as two E4M3 terms hi + lo); else V is bf16 and P bf16.
+// V8: V is E4M3 with per-(sequence, head, channel) scales, widened to f16
+// in shared memory, and P is f16; else V is bf16 and P bf16.
 template <bool V8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_int8_kernel(const __grid_constant__ CUtensorMap q_map,
@@ -540,13 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waits; rows of a V tile past L_kv (the unwritten rest of a sequence's
     // last page, whose bits may be NaN) are zeroed first, since P = 0 there
     // does not cancel a NaN.  Lane 0 issues the MMAs.
-    const uint32_t idesc_pv = V8 ? make_idesc(kFmtE4M3, kFmtE4M3, 0, 1, kT, kD)
+    const uint32_t idesc_pv = V8 ? make_idesc(kFmtF16, kFmtF16, 0, 1, kT, kD)
                                  : make_idesc(kFmtBF16, kFmtBF16, 0, 1, kT, kD);
-    // MN-major V.  bf16: two 64-column atoms 16 KB apart (leading byte
-    // offset), 16 key rows (2 KB) per K = 16 step.  E4M3: one 128-byte atom
-    // per key row, 32 key rows (4 KB) per K = 32 step
-    const uint64_t vdesc0 = V8 ? make_smem_desc(smem_u32(smem + kOffV), 0, 1024, kSwizzle128B)
-                               : make_smem_desc(smem_u32(smem + kOffV), kHalf, 1024, kSwizzle128B);
+    // MN-major 16-bit V: two 64-column atoms 16 KB apart (leading byte
+    // offset), 16 key rows (2 KB) per K = 16 step
+    const uint64_t vdesc0 = make_smem_desc(smem_u32(smem + kOffV), kHalf, 1024, kSwizzle128B);
     Items it;
     it.start(a);
     TileWalk vw;
@@ -629,27 +626,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
+        if (V8) {
+          // E4M3 [128 keys][128 bytes] in the stage's first 16 KB -> f16 in two
+          // halves [128 keys][64], 128-byte swizzle.  Half 0 of key row r
+          // takes exactly the bytes of source row r: each lane reads its
+          // whole row into registers, the warp syncs, then every lane writes.
+#pragma unroll 1
+          for (int r0 = 0; r0 < kT; r0 += 32) {
+            const int r = r0 + lane;
+            uint4 src[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              src[c] = *reinterpret_cast<const uint4*>(vt + r * 128 + (((c ^ r) & 7) << 4));
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t wv[4] = {src[c].x, src[c].y, src[c].z, src[c].w};
+              uint32_t o[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                o[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(wv[q] & 0xFFFFu));
+                o[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wv[q] >> 16));
+              }
+              uint8_t* base = vt + (c >> 2) * kHalf + r * 128;
+              const int c0 = 2 * (c & 3);
+              *reinterpret_cast<uint4*>(base + (((c0 ^ r) & 7) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(base + ((((c0 + 1) ^ r) & 7) << 4)) =
+                  make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            __syncwarp();
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
         if (lane == 0) {
           tc_fence_after_sync();
           const uint64_t db = vdesc0 + static_cast<uint64_t>((s * kH16Tile) >> 4);
-          if (V8) {
-            // key chunk q (32 keys): the hi terms of half q / 2 sit in its S
-            // columns [64 (q / 2) + 8 (q % 2), +8), the lo terms 16 further
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const int q = kk & 3, term = kk >> 2;
-              tc_mma_f8_tmem_a(tmem + kColO,
-                               tmem + kColS + sb * kT + (q >> 1) * 64 + (q & 1) * 8 + term * 16,
-                               db + static_cast<uint64_t>((q * 32 * 128) >> 4), idesc_pv,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk)
-              tc_mma_f16_tmem_a(tmem + kColO, tmem + kColS + sb * kT + (kk >> 2) * 64 + 8 * (kk & 3),
-                                db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kT / 16; ++kk)
+            tc_mma_f16_tmem_a(tmem + kColO, tmem + kColS + sb * kT + (kk >> 2) * 64 + 8 * (kk & 3),
+                              db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sh.v_empty[s]);
           tc_commit(&sh.pv_done[sb]);
           if (j == t.nkv - 1) tc_commit(&sh.o_full);
@@ -728,11 +745,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(bar_id, 64);
       const float corr = 128.f * (static_cast<float>(qhalf) + sh.pair[half ^ 1][r]);
       named_barrier(bar_id, 64);
-      // l: the sum of the unrounded p (for the lse, and the E4M3-P
-      // instantiation's normaliser: E4M3 flushes p below 2^-10 to zero, and
-      // that lost mass would bias a sum of the rounded terms); lr: the sum of
-      // the bf16 P the P.V product sees, which normalises O in the bf16
-      // instantiation so that P's rounding cancels where one key dominates
+      // l: the sum of the unrounded p (for the lse); lr: the sum of the
+      // 16-bit P the P.V product sees (bf16, or f16 in the V8
+      // instantiation), which normalises O so that P's rounding cancels
+      // where one key dominates
       float m = -INFINITY, l = 0.f, lr = 0.f;
       float sk_next = __ldg(skp);
       for (int j = 0; j < t.nkv; ++j) {
@@ -803,31 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(srow + 64 * half + 32 * c2, v);
           tmem_ld_wait();
           const int lim2 = climit - 32 * c2;
-          if (V8) {
-            // P as two E4M3 terms (built in f16x2), four keys per column:
-            // hi to columns [64 half + 8 c2, +8), lo 16 columns further
-            uint32_t ph[8], pl[8];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              float p[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x = 4 * w + e <= lim2 ? __uint_as_float(v[4 * w + e]) : -INFINITY;
-                p[e] = fast_exp2(fmaf(x, sc24, nm));
-              }
-              l += (p[0] + p[1]) + (p[2] + p[3]);
-              const uint32_t f01 = f32x2_to_f16x2(p[1], p[0]);
-              const uint32_t f23 = f32x2_to_f16x2(p[3], p[2]);
-              const uint16_t h01 = f16x2_to_e4m3x2(f01);
-              const uint16_t h23 = f16x2_to_e4m3x2(f23);
-              const uint16_t l01 = f16x2_to_e4m3x2(f16x2_sub(f01, e4m3x2_to_f16x2(h01)));
-              const uint16_t l23 = f16x2_to_e4m3x2(f16x2_sub(f23, e4m3x2_to_f16x2(h23)));
-              ph[w] = h01 | (static_cast<uint32_t>(h23) << 16);
-              pl[w] = l01 | (static_cast<uint32_t>(l23) << 16);
-            }
-            tmem_st8(srow + 64 * half + 8 * c2, ph);
-            tmem_st8(srow + 64 * half + 16 + 8 * c2, pl);
-          } else {
+          {
             uint32_t pk[16];
 #pragma unroll
             for (int w = 0; w < 16; ++w) {
@@ -836,9 +828,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float p0 = fast_exp2(fmaf(x0, sc24, nm));
               const float p1 = fast_exp2(fmaf(x1, sc24, nm));
               l += p0 + p1;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
-              lr += __uint_as_float(pk[w] << 16) + __uint_as_float(pk[w] & 0xFFFF0000u);
+              if (V8) {
+                // f16 pairs (11 significant bits) for the f16 P.V product
+                pk[w] = f32x2_to_f16x2(p1, p0);
+                lr = add_f16x2_to_f32(lr, pk[w]);
+              } else {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+                lr += __uint_as_float(pk[w] << 16) + __uint_as_float(pk[w] & 0xFFFF0000u);
+              }
             }
             tmem_st16(srow + 64 * half + 16 * c2, pk);
           }
@@ -852,13 +850,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(bar_id, 64);
       const float lt = l + sh.pair[half ^ 1][r];
       named_barrier(bar_id, 64);
-      float ln = lt;                 // the normaliser of O
-      if (!V8) {
-        sh.pair[half][r] = lr;
-        named_barrier(bar_id, 64);
-        ln = lr + sh.pair[half ^ 1][r];
-        named_barrier(bar_id, 64);
-      }
+      sh.pair[half][r] = lr;
+      named_barrier(bar_id, 64);
+      const float ln = lr + sh.pair[half ^ 1][r];   // the normaliser of O
+      named_barrier(bar_id, 64);
       const float so = ln > 0.f ? 1.f / ln : 0.f;
       // the next item's q row half loads while this item's O is written
       uint4 qn[4];

@@ -287,3 +287,58 @@ def test_decode_full_batch_sampled(lib):
     order = np.argsort(wl.lengths)
     reqs = sorted({int(order[0]), int(order[-1]), 5, 40})
     _check_decode(lib, wl, reqs=reqs)
+
+
+def test_decode_steps_with_side_stream_replan_and_growing_lengths(lib):
+    """Three decode steps as a server runs them: append one token per
+    request, re-plan on a side stream for the grown lengths (crossing a
+    256-token chunk boundary), attend, merge; every step against the oracle."""
+    rng = np.random.default_rng(41)
+    B, Hq, Hkv, D, ps = 3, 32, 8, 128, 16
+    L0 = np.array([254, 255, 90], np.int32)
+    steps = 3
+    Lmax = L0 + steps
+    bt, P = synth.page_tables(rng, Lmax, ps)
+    k_all = [synth.bf16_normal(rng, (int(Lmax[b]), Hkv, D)) for b in range(B)]
+    v_all = [synth.bf16_normal(rng, (int(Lmax[b]), Hkv, D)) for b in range(B)]
+    qv = synth.bf16_normal(rng, (B, Hq, D))
+    dev = "cuda"
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    k_pool = torch.zeros((P, ps, Hkv, D), dtype=torch.uint8, device=dev)
+    v_pool = torch.zeros_like(k_pool)
+    ks = torch.zeros((P, ps, Hkv), dtype=torch.float32, device=dev)
+    vs = torch.zeros_like(ks)
+    btd = tt(bt)
+    # the cache before the first step: L0 - 1 tokens of each request
+    prev = L0 - 1
+    lib.write_cache_fp8(tt(np.concatenate([k_all[b][:prev[b]] for b in range(B)])).bfloat16(),
+                        tt(np.concatenate([v_all[b][:prev[b]] for b in range(B)])).bfloat16(),
+                        tt(np.cumsum(prev).astype(np.int32)), btd, k_pool, v_pool, ks, vs)
+    plan = lib.DecodePlan(Lmax, Hq, Hkv, ps, D)     # workspaces sized for the longest step
+    side = torch.cuda.Stream()
+    q = tt(qv).bfloat16()
+    outs = []
+    for step in range(steps):
+        L = L0 + step
+        plan.replan(seqlens_kv=L, stream=side)
+        newk = tt(np.stack([k_all[b][L[b] - 1] for b in range(B)])).bfloat16()
+        newv = tt(np.stack([v_all[b][L[b] - 1] for b in range(B)])).bfloat16()
+        lib.write_cache_fp8(newk, newv, tt(np.arange(1, B + 1, dtype=np.int32)), btd, k_pool, v_pool,
+                            ks, vs, start_pos=tt((L - 1).astype(np.int32)))
+        plan.attend(q, k_pool, v_pool, ks, vs, btd, 1.0 / np.sqrt(D))
+        out = torch.empty_like(q)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+        plan.merge(out, lse)
+        outs.append((L.copy(), out, lse))
+    torch.cuda.synchronize()
+    lib.check_errors()
+    for L, out, lse in outs:
+        kk = np.concatenate([k_all[b][:L[b]] for b in range(B)])
+        vv = np.concatenate([v_all[b][:L[b]] for b in range(B)])
+        z8 = np.zeros((P, ps, Hkv, D), np.uint8)
+        zs = np.zeros((P, ps, Hkv), np.float32)
+        kp, vp, ksp, vsp, _, _ = ocache.write_fp8_token_head(
+            kk, vv, np.cumsum(L), np.zeros(B, np.int64), bt, ps, z8, z8, zs, zs)
+        want_o, want_lse = oatt.paged_decode_fp8(qv, kp, vp, ksp, vsp, bt, L, 1.0 / np.sqrt(D))
+        assert_attention_close(bf16_to_f64(out), want_o, tight=DECODE_TIGHT)
+        assert_lse_close(lse.cpu().numpy(), want_lse)
