@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(int B, int Hq,
   constexpr int EPL = D / 32, kGroup = 8;
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_wait();   // the partials of the split-KV launch before this one
   if (w >= B * Hq) return;
   const int b = w / Hq, h = w % Hq;
   const int s0 = split_off[b], n = split_off[b + 1] - s0;
@@ -819,13 +820,23 @@ cudaError_t launch_decode_merge(const DecodePlan& plan, const float* float_ws, c
       static_cast<const uint8_t*>(int_ws) + plan.split_off_offset);
   const float* part_lse = float_ws + plan.total_splits * plan.num_qo_heads * plan.head_dim;
   const int grid = (warps * 32 + 127) / 128;
+  // a programmatic dependent of the split-KV launch: it is scheduled while
+  // that launch drains and waits for it before reading the partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t* out = static_cast<uint16_t*>(o);
   if (plan.head_dim == 128)
-    decode_merge_kernel<128><<<grid, 128, 0, stream>>>(B, Hq, split_off, float_ws, part_lse,
-                                                       static_cast<uint16_t*>(o), lse);
-  else
-    decode_merge_kernel<64><<<grid, 128, 0, stream>>>(B, Hq, split_off, float_ws, part_lse,
-                                                      static_cast<uint16_t*>(o), lse);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, B, Hq, split_off, float_ws, part_lse,
+                              out, lse);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, B, Hq, split_off, float_ws, part_lse, out,
+                            lse);
 }
 
 }  // namespace qpkv

@@ -299,6 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // k- and v-scales of every tile (one 512-byte piece each)
       float* ks = sKS + d * (kMaxTilesItem * kTile);
       float* vs = sVS + d * (kMaxTilesItem * kTile);
+      // the scale pools may have been written by the launch before this one
+      if (o == 0) griddep_wait();
       const bool load = lane < ntl && row >= 0;
       const int total = __popc(__ballot_sync(0xffffffffu, load)) * (2 * kTile * 4);
       if (lane == 0) mbar_arrive_expect_tx(&sh.scl_full[d], total);
@@ -339,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&k_map);
       tma_prefetch_desc(&v_map);
     }
+    // the K/V pools may have been written by the launch before this one
+    griddep_wait();
     int pos = 0;
     // one tile into the next ring stage: a whole box by TMA (lane 0), or the
     // valid rows of a partial tail tile by 16-byte copies (whole warp)
@@ -822,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  griddep_launch_dependents();   // the merge may start launching
   if (warp == kWarpMma) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -847,8 +852,20 @@ cudaError_t launch_heads_t(const CUtensorMap& km, const CUtensorMap& vm, const H
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.num_items < sms ? a.num_items : sms;
-  kern<<<grid, kThreads, C::kSmem, stream>>>(km, vm, a);
-  return cudaGetLastError();
+  // launched as a programmatic dependent: the prologue (barriers, tensor
+  // memory, the first work item's pages and queries) overlaps the end of the
+  // launch before it; the K/V and scale reads wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, km, vm, a);
 }
 
 }  // namespace

@@ -94,6 +94,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends
+// on have completed and their memory is visible (returns at once when the
+// launch has no such dependency), and let the dependents of this grid start
+// their launch once every CTA has signalled or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA, tensor core) before a barrier hands the data over.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -81,6 +81,9 @@ __global__ void __launch_bounds__(256) write_fp8_token_head_kernel(
     int32_t* __restrict__ slots, int hnd, const float* __restrict__ rope_cos,
     const float* __restrict__ rope_sin, int rope_max_pos, int* err) {
   constexpr int EPL = D / 32;  // 2 or 4 elements per lane
+  // a programmatic dependent launch (the decode) may start its prologue now;
+  // it waits for this grid to complete before it reads the pools
+  griddep_launch_dependents();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= T * H) return;
