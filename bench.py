@@ -222,27 +222,32 @@ class DecodeBench:
         self.plan.merge(self.out, self.lse)
 
 
-def kernel_source_hash():
-    with open(KERNEL_SOURCE, "rb") as f:
+def kernel_source_hash(source=KERNEL_SOURCE):
+    with open(source, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per attend launch from the committed ncu summary, or None
-    when the kernel source changed since that capture."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def profiled_traffic(summary=PROFILE_SUMMARY, source=KERNEL_SOURCE):
+    """DRAM bytes (read + write) per launch from a committed ncu summary, or
+    None when the kernel source changed since that capture."""
+    if not os.path.exists(summary):
         return None
     vals = {}
-    for line in open(PROFILE_SUMMARY):
+    for line in open(summary):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(source):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+def _extra_traffic(profile, source):
+    return profiled_traffic(os.path.join(ROOT, "profiles", profile),
+                            os.path.join(ROOT, "quantized_paged_kv_varlen_gb300", "csrc", source))
 
 
 def peaks():
@@ -305,6 +310,97 @@ def cpu_worker(seconds, n_req):
             "sample": f"{n_req} requests of the workload (lengths {lens}), all 32 heads, "
                       f"{passes} passes in {dt:.1f} s, one thread",
             "seconds_per_pass": dt / passes, "tokens_per_s": len(lens) * passes / dt}
+
+
+def cpu_worker_extras(seconds):
+    """Child process, one thread: the oracle on bounded samples of the three
+    other workloads, each for about `seconds`, in the units of their lines
+    (useful causal FLOP of the sampled rows per second)."""
+    import numpy as np
+    from quantized_paged_kv_varlen_gb300 import synth
+    from oracle import attention as oatt
+    from oracle import cache as ocache
+    from oracle import mla as omla
+    from oracle import quant as oquant
+    from oracle import rope as orope
+    out = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= seconds:
+                return n, dt
+
+    # dense FP8 causal: rows of one (batch, head) slice of the workload
+    dw = synth.dense_fp8(0)
+    S, Dd = dw.S, dw.D
+    codes, desc = [], []
+    for which in ("q", "k", "v"):
+        x = dw.slice(which, 0, 0)[None, :, None, :]
+        s = oquant.absmax_scale(np.abs(x).max(axis=(1, 3)), oquant.FP8_QMAX)
+        codes.append(oquant.quant_fp8(x, s[:, None, :, None]))
+        desc.append(s)
+    rows = list(range(0, S, S // 64))
+    flops = float(sum(4.0 * Dd * (i + 1) for i in rows))
+    n, dt = timed(lambda: oatt.dense_fp8(*codes, *desc, dw.scale, True,
+                                         rows=[(0, i, 0) for i in rows]))
+    out["fp8_attn_causal"] = {"value": flops * n / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "kind": "oracle",
+                              "sample": f"{len(rows)} query rows (every {S // 64}th) of one "
+                                        f"(batch, head) slice, S={S}, {n} passes in {dt:.1f} s"}
+    # INT8 varlen prefill: one sequence of the workload, two heads, all rows
+    pw = synth.varlen_prefill(0)
+    b = int(np.argsort(pw.lengths)[len(pw.lengths) // 2])
+    L = int(pw.lengths[b])
+    beg = int(np.sum(pw.lengths[:b]))
+    H2 = 2
+    sl = lambda a: a[beg:beg + L, :H2]
+    cos, sin = orope.cos_sin_table(L, pw.D, pw.theta)
+    nbk = (L + 127) // 128
+    P = (L + pw.page_size - 1) // pw.page_size
+    bt = np.arange(P, dtype=np.int32)[None]
+    kp0 = np.zeros((P, pw.page_size, H2, pw.D), np.int8)
+    vp0 = np.zeros((P, pw.page_size, H2, pw.D), np.uint16)
+    kp, vp, ksc, q8, qsc, _ = ocache.write_int8_block128_rope(
+        sl(pw.q), sl(pw.k), sl(pw.v), np.array([L]), bt, pw.page_size, cos, sin, nbk, kp0, vp0)
+    flops = 4.0 * pw.D * H2 * L * (L + 1) / 2
+    n, dt = timed(lambda: oatt.paged_prefill_int8(q8, qsc, kp, ksc, vp, bt, np.array([L]),
+                                                   np.array([L]), pw.scale, causal=True))
+    out["int8_prefill_varlen"] = {"value": flops * n / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                  "kind": "oracle",
+                                  "sample": f"sequence {b} (L={L}) of the workload, {H2} of 32 "
+                                            f"heads, all rows, {n} passes in {dt:.1f} s"}
+    # MLA sparse decode: two query tokens of the workload, all 128 heads
+    mw = synth.mla_sparse(0, B=2, QN=128, lengths=[32768, 40000])
+    pool = np.zeros((mw.num_pages, mw.block_size, 1, 656), np.uint8)
+    for bb in range(mw.B):
+        pool, _ = ocache.write_mla_rows(mw.kv(bb), np.array([mw.lengths[bb]]), np.array([0]),
+                                        mw.block_table[bb:bb + 1], mw.block_size, pool)
+    flops = 2 * 128.0 * 2048 * 2 * (576 + 512)
+    n, dt = timed(lambda: omla.mla_sparse_decode(mw.q, pool, mw.sparse_indices, mw.block_table,
+                                                 mw.lengths, mw.cu_seqlens_q, mw.scale))
+    out["mla_sparse_decode"] = {"value": flops * n / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"2 query tokens (L = 32768, 40000), 128 heads, 2048 "
+                                          f"ids each, {n} passes in {dt:.1f} s"}
+    return out
+
+
+def run_cpu_baseline_extras(seconds):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker-extras", str(seconds)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        why = (r.stderr.strip().splitlines() or ["?"])[-1][:200]
+        return {k: {"value": None, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                    "sample": "failed: " + why}
+                for k in ("fp8_attn_causal", "int8_prefill_varlen", "mla_sparse_decode")}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def run_cpu_baseline(seconds, n_req):
@@ -492,6 +588,10 @@ def run_qpkv(args):
     }
     if world == 1 and not args.no_extras:
         line["also"] = run_extras(device)
+        if not args.no_cpu_baseline:
+            cpu_x = run_cpu_baseline_extras(args.cpu_seconds / 3)
+            for k, v in line["also"].items():
+                v["cpu_baseline"] = cpu_x.get(k)
     print(json.dumps(line), flush=True)
 
 
@@ -543,7 +643,9 @@ def run_extras(device, iters=10):
         "workload": f"dense FP8 causal B={B4} S={S4} H={H4} D={D4} (BSND e4m3, per-(b,h) descales)",
         "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8, "unit": "TFLOP/s",
-                     "frac": tf / fp8, "peak_source": "measured bf16_tflops x 2 (fp8 nominal ratio)"}}
+                     "frac": tf / fp8, "peak_source": "measured bf16_tflops x 2 (fp8 nominal ratio)",
+                     "traffic": _extra_traffic("fp8_attn_causal_b4_s8192_h32.txt", "fp8_attn.cu"),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"}}
     del q8, k8, v8, o4
 
     # varlen INT8-QK paged prefill (cache written by the library)
@@ -578,7 +680,10 @@ def run_extras(device, iters=10):
                     "INT8 Q/K block-128 scales, bf16 V",
         "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops, "write_cache_ms": ms_w,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": tf / bf16, "peak_source": "measured bf16_tflops (f16/bf16 MMAs)"}}
+                     "frac": tf / bf16, "peak_source": "measured bf16_tflops (f16/bf16 MMAs)",
+                     "traffic": _extra_traffic("prefill_int8_8seqs_h32_page64.txt",
+                                               "prefill_int8.cu"),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"}}
     # the same prefill over ragged (packed, non-paged) K/V of the same sizes
     gk = torch.Generator(device=device)
     gk.manual_seed(13)
@@ -651,6 +756,9 @@ def set_batch(n):
 def main():
     if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-worker":
         print(json.dumps(cpu_worker(float(sys.argv[2]), int(sys.argv[3]))))
+        return
+    if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-worker-extras":
+        print(json.dumps(cpu_worker_extras(float(sys.argv[2]))))
         return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
