@@ -731,6 +731,9 @@ def run_extras(device, iters=10):
     row_bytes = 32 * 2048 * 656 + 32 * 128 * 576 * 2 + 32 * 128 * 512 * 2 + 32 * 2048 * 4
     tf = flops / (ms / 1e3) / 1e12
     gbs = row_bytes / (ms / 1e3) / 1e9
+    t_qk = _extra_traffic("mla_qk_b32.txt", "mla_sparse.cu")
+    t_pv = _extra_traffic("mla_pv_b32.txt", "mla_sparse.cu")
+    mla_traffic = t_qk + t_pv if t_qk is not None and t_pv is not None else None
     out["mla_sparse_decode"] = {
         "workload": "MLA-absorb sparse decode B=32 QN=128 D=576/512, 2048 ids of "
                     "L~U{32768..65536}, block 64, INT8 nope + bf16 rope rows",
@@ -738,7 +741,10 @@ def run_extras(device, iters=10):
         "l2": "flushed (256 MB write) before each run",
         "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s",
                      "frac": tf / bf16, "hbm_frac": gbs / pk["hbm_gbs"],
-                     "peak_source": "measured bf16_tflops; hbm_frac of measured hbm_gbs"}}
+                     "peak_source": "measured bf16_tflops; hbm_frac of measured hbm_gbs",
+                     "traffic": mla_traffic,
+                     "traffic_unit": "bytes per call (ncu dram read + write of the QK and PV "
+                                     "kernels)"}}
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the extra workloads")
