@@ -10,7 +10,7 @@
 // (batch, head) side by side, tiles A = 2p and B = 2p + 1 of a pair, over
 // the same stream of K/V tiles: while one tile's softmax computes its
 // exponentials, the tensor core works on the other tile, and each K/V tile
-// is fetched once for both.  12 warps:
+// is fetched once for both.  14 warps:
 //   warp 0      TMA: the pair's Q tiles (two slots), K tiles (4-stage ring),
 //               V tiles (2-stage ring), K one step ahead of V
 //   warp 1      tcgen05 MMAs from one thread, per step g of the K/V stream:
@@ -18,8 +18,9 @@
 //               QK: S[128 q x 128 k] = Q . K^T, E4M3 operands (kind::f8f6f4);
 //               PV: O[128 q x 128 d] += P . V, f16 operands (kind::f16) with P
 //               read from tensor memory and V widened from E4M3 (exact)
-//   warps 2-3   widen each V tile from E4M3 to f16, written in the MN-major
-//               operand layout of the PV product (two 64-column halves)
+//   warps 2, 3, 12, 13  widen each V tile from E4M3 to f16, written in the
+//               MN-major operand layout of the PV product (two 64-column
+//               halves); one such warp on each scheduler
 //   warps 4-7   softmax and epilogue of tile A, one thread per query row
 //   warps 8-11  the same for tile B
 // P is f16 (11 significant bits, range 2^-24 .. 65504): with the lazy
@@ -45,9 +46,10 @@ namespace {
 
 constexpr int kT = 128;               // q rows per tile = keys per tile = MMA M and N
 constexpr int kD = 128;               // head dim
-constexpr int kThreads = 384;         // 12 warps
-constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpSoftA = 4, kWarpSoftB = 8;
-constexpr int kConvThreads = 64;
+constexpr int kThreads = 448;         // 14 warps
+constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpConv0 = 2, kWarpSoftA = 4, kWarpSoftB = 8,
+              kWarpConv2 = 12;
+constexpr int kConvThreads = 128;
 constexpr int kKStages = 4;           // E4M3 K tiles, 16 KB each
 constexpr int kVStages = 2;           // E4M3 V tiles, 16 KB each
 constexpr int kV16Bufs = 2;           // f16 V tiles, 32 KB each
@@ -357,11 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain(&sh.mma_done, 0, a.err);
     }
     __syncwarp();
-  } else if (warp < kWarpSoftA) {
+  } else if (warp < kWarpSoftA || warp >= kWarpConv2) {
     // ---------------------------------------- V: E4M3 -> f16 (exact)
     // Input: a TMA tile [128 keys][128 bytes], 128-byte swizzle.  Output:
     // two halves [128 keys][64 f16] (dims 0-63, 64-127), 128-byte swizzle.
-    const int ct = tid - kWarpConv0 * 32;   // 0..63
+    const int ct = warp < kWarpSoftA ? tid - kWarpConv0 * 32 : tid - kWarpConv2 * 32 + 64;
     Walk w;
     w.start(a);
     while (w.valid(a)) {
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_await(&sh.v16_empty[bsel], ((g / kV16Bufs) & 1) ^ 1, sh, a.err, lane)) break;
       const uint8_t* src = smem + kOffV8 + s * kTile8;
       uint8_t* dst = smem + kOffV16 + bsel * kTile16;
-#pragma unroll 4
+#pragma unroll
       for (int k = 0; k < (kT * 8) / kConvThreads; ++k) {
         const int i = ct + kConvThreads * k;
         const int row = i >> 3, c = i & 7;
@@ -438,13 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (whole) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
+          for (int i = 0; i < 32; i += 2)
+            m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             m4[i & 3] = fmaxf(m4[i & 3], 32 * c + i <= climit ? __uint_as_float(v[i]) : -INFINITY);
         }
-        xm = fmaxf(xm, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        xm = fmax3(xm, fmax3(m4[0], m4[1], m4[2]), m4[3]);
       }
       const float mx = xm * sc;   // the row's tile maximum in log2 units
       float f = 1.f;
@@ -475,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pass 2: P = 2^(x sc - m) as f16 pairs into the first 64 columns of S
       // (chunk c of 32 keys -> columns [16c, 16c + 16), all already read)
       const float nm = m > -INFINITY ? -m : 0.f;   // a row that sees no key gets p = 0
-      float ls[2] = {0.f, 0.f};
+      // pairs of keys in packed f32x2 arithmetic: x = s sc - m, the sums
+      const uint64_t sc2 = f32x2_pack(sc, sc), nm2 = f32x2_pack(nm, nm);
+      uint64_t ls2 = f32x2_pack(0.f, 0.f);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -484,20 +489,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float x0 = fmaf(__uint_as_float(v[2 * i]), sc, nm);
-          float x1 = fmaf(__uint_as_float(v[2 * i + 1]), sc, nm);
+          float2 x = f32x2_unpack(
+              f32x2_fma(f32x2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sc2, nm2));
           if (!whole) {
-            x0 = 32 * c + 2 * i <= climit ? x0 : -INFINITY;
-            x1 = 32 * c + 2 * i + 1 <= climit ? x1 : -INFINITY;
+            x.x = 32 * c + 2 * i <= climit ? x.x : -INFINITY;
+            x.y = 32 * c + 2 * i + 1 <= climit ? x.y : -INFINITY;
           }
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          ls[0] += p0;
-          ls[1] += p1;
+          const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+          ls2 = f32x2_add(ls2, f32x2_pack(p0, p1));
           pk[i] = f32x2_to_f16x2(p1, p0);
         }
         tmem_st16(srow + 16 * c, pk);
       }
-      l += ls[0] + ls[1];
+      const float2 ls = f32x2_unpack(ls2);
+      l += ls.x + ls.y;
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&sh.p_ready[x]);
