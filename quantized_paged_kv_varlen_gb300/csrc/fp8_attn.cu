@@ -12,7 +12,8 @@
 // exponentials, the tensor core works on the other tile, and each K/V tile
 // is fetched once for both.  14 warps:
 //   warp 0      TMA: the pair's Q tiles (two slots), K tiles (4-stage ring),
-//               V tiles (2-stage ring), K one step ahead of V
+//               V tiles (2-stage ring), K one step ahead of V; K and V
+//               copies leave together from two lanes
 //   warp 1      tcgen05 MMAs from one thread, per step g of the K/V stream:
 //                 PV_A(g-1) QK_A(g) PV_B(g-1) QK_B(g)
 //               QK: S[128 q x 128 k] = Q . K^T, E4M3 operands (kind::f8f6f4);
@@ -233,50 +234,66 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------- loads
+    // One thread's tensor copies leave one after another (each issue holds
+    // the thread for a few hundred cycles); copies of several lanes in one
+    // instruction go out together.  So lane 0 issues K(g+1) while lane 1
+    // issues V(g), and the unit's two Q tiles go out from lanes 0 and 1.
     if (lane == 0) {
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&k_map);
       tma_prefetch_desc(&v_map);
-      Walk kw, vw;
-      kw.start(a);
-      vw.start(a);
-      int ncopies_k = 0, ncopies_v = 0, nq_slots = 0;
-      bool ok = true;
-      // K of step kw (with the unit's Q tiles at its first step)
-      auto issue_k = [&]() -> bool {
-        if (kw.j == 0) {
-          const int slot = kw.uc & 1;
-          if (!awaitb(&sh.q_free[slot], ((kw.uc >> 1) & 1) ^ 1, sh, a.err)) return false;
-          mbar_arrive_expect_tx(&sh.q_full[slot], (1 + kw.has_b) * kTile8);
-          uint8_t* dst = smem + kOffQ + slot * 2 * kTile8;
-          tma_load_4d(dst, &q_map, &sh.q_full[slot], 0, kw.h, kw.qt * kT, kw.b);
-          if (kw.has_b)
-            tma_load_4d(dst + kTile8, &q_map, &sh.q_full[slot], 0, kw.h, (kw.qt + 1) * kT, kw.b);
-          ++nq_slots;
-        }
-        const int s = kw.g % kKStages;
-        if (!awaitb(&sh.k_empty[s], ((kw.g / kKStages) & 1) ^ 1, sh, a.err)) return false;
-        mbar_arrive_expect_tx(&sh.k_full[s], kTile8);
-        tma_load_4d(smem + kOffK + s * kTile8, &k_map, &sh.k_full[s], 0, kw.h / a.G, kw.j * kT, kw.b);
+    }
+    Walk kw, vw;
+    kw.start(a);
+    vw.start(a);
+    int ncopies_k = 0, ncopies_v = 0, nq_slots = 0;
+    bool ok = true;
+    // the Q tiles of kw's unit (at its first step)
+    auto issue_q = [&]() -> bool {
+      const int slot = kw.uc & 1;
+      if (!warp_await(&sh.q_free[slot], ((kw.uc >> 1) & 1) ^ 1, sh, a.err, lane)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[slot], (1 + kw.has_b) * kTile8);
+      __syncwarp();
+      if (lane <= kw.has_b)
+        tma_load_4d(smem + kOffQ + (slot * 2 + lane) * kTile8, &q_map, &sh.q_full[slot], 0, kw.h,
+                    (kw.qt + lane) * kT, kw.b);
+      __syncwarp();
+      ++nq_slots;
+      return true;
+    };
+    // K of step kw (when do_k) and V of step vw (when do_v), one instruction
+    auto issue = [&](bool do_k, bool do_v) -> bool {
+      const int ks = kw.g % kKStages, vs = vw.g % kVStages;
+      if (do_k) {
+        if (kw.j == 0 && !issue_q()) return false;
+        if (!warp_await(&sh.k_empty[ks], ((kw.g / kKStages) & 1) ^ 1, sh, a.err, lane))
+          return false;
+      }
+      if (do_v && !warp_await(&sh.v_empty[vs], ((vw.g / kVStages) & 1) ^ 1, sh, a.err, lane))
+        return false;
+      if ((lane == 0 && do_k) || (lane == 1 && do_v)) {
+        const bool k = lane == 0;
+        uint64_t* bar = k ? &sh.k_full[ks] : &sh.v_full[vs];
+        const int hh = (k ? kw.h : vw.h) / a.G, jj = k ? kw.j : vw.j, bb = k ? kw.b : vw.b;
+        mbar_arrive_expect_tx(bar, kTile8);
+        tma_load_4d(smem + (k ? kOffK + ks * kTile8 : kOffV8 + vs * kTile8), k ? &k_map : &v_map,
+                    bar, 0, hh, jj * kT, bb);
+      }
+      __syncwarp();
+      if (do_k) {
         ++ncopies_k;
         kw.next(a);
-        return true;
-      };
-      auto issue_v = [&]() -> bool {
-        const int s = vw.g % kVStages;
-        if (!awaitb(&sh.v_empty[s], ((vw.g / kVStages) & 1) ^ 1, sh, a.err)) return false;
-        mbar_arrive_expect_tx(&sh.v_full[s], kTile8);
-        tma_load_4d(smem + kOffV8 + s * kTile8, &v_map, &sh.v_full[s], 0, vw.h / a.G, vw.j * kT, vw.b);
+      }
+      if (do_v) {
         ++ncopies_v;
         vw.next(a);
-        return true;
-      };
-      if (kw.valid(a)) ok = issue_k();
-      while (ok && vw.valid(a)) {
-        if (kw.valid(a)) ok = issue_k();
-        if (ok) ok = issue_v();
       }
-      // this CTA's copies still in flight land before it exits
+      return true;
+    };
+    if (kw.valid(a)) ok = issue(true, false);
+    while (ok && vw.valid(a)) ok = issue(kw.valid(a), true);
+    // this CTA's copies still in flight land before it exits
+    if (lane == 0) {
       for (int i = ncopies_k > kKStages ? ncopies_k - kKStages : 0; i < ncopies_k; ++i)
         drain(&sh.k_full[i % kKStages], (i / kKStages) & 1, a.err);
       for (int i = ncopies_v > kVStages ? ncopies_v - kVStages : 0; i < ncopies_v; ++i)
