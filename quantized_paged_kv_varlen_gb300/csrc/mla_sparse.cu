@@ -16,7 +16,9 @@
 //   mla_prep     sparse ids -> pool rows (block_table lookup; -1 for ids
 //                after the first -1, outside [0, L_kv), or hidden by
 //                sparse_mode 3), and a bulk L2 prefetch of every listed row
-//   mla_qk       one CTA per (token, 512 keys): Q and dequantised-K chunks
+//   mla_qk       one CTA per (token, 512 keys): the group's rows sorted by
+//                pool row first (written back for the PV stage); Q and
+//                dequantised-K chunks
 //                of 64 dims stream through shared memory (TMA for Q, eight
 //                converter warps gather and dequantise the rows), S for the
 //                four 128-key tiles accumulates in tensor memory; the
@@ -29,6 +31,7 @@
 //                P chunks by TMA, V chunks dequantised by the converter
 //                warps, O[128 x 128] in tensor memory, bf16 out.
 // Dequantisation rounds code * scale (fp32 product) once to bf16.
+#include <climits>
 #include <cmath>
 
 #include "common.cuh"
@@ -122,13 +125,60 @@ __device__ __forceinline__ void dequant16(const uint4& w, float s, uint4& p0, ui
 
 
 // ----------------------------------------------------------------- prep
-// Blocks (token, 256-key slice): the first -1 of the token's list (found
-// by every block of the token) ends it; key j is token id * sbs + j % sbs
-// of the listed id = list[j / sbs] (sbs = sparse_block_size, 1 for
-// token-wise lists) and becomes a pool row, or -1: past the list, a block
-// outside the sequence (flagged), a block token at or past L_kv, hidden by
-// the right-down causal rule of sparse_mode 3, or on a page id outside the
-// pool (flagged).
+// Key j of token t is token id * sbs + j % sbs of the listed id
+// list[j / sbs] (sbs = sparse_block_size, 1 for token-wise lists) and
+// becomes a pool row, or -1: past the list (the first -1 of the token's
+// list ends it), a block outside the sequence (flagged), a block token at
+// or past L_kv, hidden by the right-down causal rule of sparse_mode 3, or on
+// a page id outside the pool (flagged).
+struct TokenSeq {
+  int nv;        // listed ids before the first -1
+  int b;         // the token's sequence
+  bool has_seq;
+  int Lq, i, Lk;
+};
+
+__device__ __forceinline__ TokenSeq token_seq(const MlaArgs& a, int t, int nv) {
+  int lo = 0, hi = a.B - 1;   // the sequence of token t: first b with cu[b] > t
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a.cu_q[mid] > t) hi = mid; else lo = mid + 1;
+  }
+  TokenSeq q;
+  q.nv = nv;
+  q.b = lo;
+  q.has_seq = a.cu_q[lo] > t;
+  const int begin = lo > 0 ? a.cu_q[lo - 1] : 0;
+  q.Lq = a.cu_q[lo] - begin;
+  q.i = t - begin;
+  q.Lk = a.lk[lo];
+  return q;
+}
+
+__device__ __forceinline__ int key_row(const MlaArgs& a, const int32_t* ids, const TokenSeq& q,
+                                       int j) {
+  const int li = j / a.sbs;
+  if (!q.has_seq || li >= q.nv) return -1;
+  const int id = ids[li];
+  const long long tok = static_cast<long long>(id) * a.sbs + (j - li * a.sbs);
+  const long long rows_bt = static_cast<long long>(a.bt_stride) * a.bs;
+  if (id < 0 || static_cast<long long>(id) * a.sbs >= q.Lk ||
+      static_cast<long long>(id) * a.sbs >= rows_bt) {
+    if (j == li * a.sbs) report_error(a.err, kDevErrBadIndex);
+    return -1;
+  }
+  if (tok >= q.Lk || tok >= rows_bt || (a.mode == 3 && tok > q.i + q.Lk - q.Lq)) return -1;
+  const int kt = static_cast<int>(tok);
+  const int pg = a.bt[static_cast<size_t>(q.b) * a.bt_stride + kt / a.bs];
+  if (pg < 0 || pg >= a.P) {
+    report_error(a.err, kDevErrBadPage);
+    return -1;
+  }
+  return pg * a.bs + kt % a.bs;
+}
+
+// Blocks (token, 256-key slice): rows in list order, and a bulk L2 prefetch
+// of every listed row.
 __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
   const int t = static_cast<int>(blockIdx.x), j0 = static_cast<int>(blockIdx.y) * 256;
   __shared__ int first_neg;
@@ -138,40 +188,11 @@ __global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
   for (int j = threadIdx.x; j < a.S; j += blockDim.x)
     if (ids[j] == -1) atomicMin(&first_neg, j);
   __syncthreads();
-  const int nv = first_neg;
-  int lo = 0, hi = a.B - 1;   // the sequence of token t: first b with cu[b] > t
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (a.cu_q[mid] > t) hi = mid; else lo = mid + 1;
-  }
-  const int b = lo;
-  const bool has_seq = a.cu_q[b] > t;
-  const int begin = b > 0 ? a.cu_q[b - 1] : 0;
-  const int Lq = a.cu_q[b] - begin, i = t - begin, Lk = a.lk[b];
-  int32_t* out = a.rows + static_cast<size_t>(t) * a.Sp;
-  {
-    const int j = j0 + static_cast<int>(threadIdx.x);
-    const int li = j / a.sbs;
-    int r = -1;
-    if (has_seq && li < nv) {
-      const int id = ids[li];
-      const long long tok = static_cast<long long>(id) * a.sbs + (j - li * a.sbs);
-      const long long rows_bt = static_cast<long long>(a.bt_stride) * a.bs;
-      if (id < 0 || static_cast<long long>(id) * a.sbs >= Lk ||
-          static_cast<long long>(id) * a.sbs >= rows_bt) {
-        if (j == li * a.sbs) report_error(a.err, kDevErrBadIndex);
-      } else if (tok < Lk && tok < rows_bt && (a.mode != 3 || tok <= i + Lk - Lq)) {
-        const int kt = static_cast<int>(tok);
-        const int pg = a.bt[static_cast<size_t>(b) * a.bt_stride + kt / a.bs];
-        if (pg < 0 || pg >= a.P)
-          report_error(a.err, kDevErrBadPage);
-        else
-          r = pg * a.bs + kt % a.bs;
-      }
-    }
-    if (r >= 0) prefetch_row_l2(a.pool + static_cast<size_t>(r) * kRow);
-    if (j < a.Sp) out[j] = r;
-  }
+  const TokenSeq q = token_seq(a, t, first_neg);
+  const int j = j0 + static_cast<int>(threadIdx.x);
+  const int r = key_row(a, ids, q, j);
+  if (r >= 0) prefetch_row_l2(a.pool + static_cast<size_t>(r) * kRow);
+  if (j < a.Sp) a.rows[static_cast<size_t>(t) * a.Sp + j] = r;
 }
 
 // ------------------------------------------------------------------- QK
@@ -188,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ QkShared sh;
+  __shared__ __align__(16) uint8_t key_ok[kKeysQk];   // key of this CTA has a pool row
+  __shared__ int srt[kKeysQk];                         // the group's rows being sorted
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = static_cast<int>(blockIdx.x) / ngroups, g = static_cast<int>(blockIdx.x) % ngroups;
   const int key0 = g * kKeysQk;
@@ -251,9 +274,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // in flight while a unit is converted.
     const int lj = tid - kConv0 * 32;
     const int ka = lj, kb = lj + 256;
-    const int32_t* rws = a.rows + static_cast<size_t>(t) * a.Sp + key0;
-    const int ra = ka < 128 * nt ? rws[ka] : -1;
-    const int rb = kb < 128 * nt ? rws[kb] : -1;
+    int32_t* rws = a.rows + static_cast<size_t>(t) * a.Sp + key0;
+    // The group's keys sorted by pool row (rows of -1 last): attention does
+    // not depend on the order of the keys, and the gathers then walk the
+    // pool in ascending order, neighbouring lanes on neighbouring pages.
+    // The sorted rows go back to the workspace for the PV stage.
+    srt[ka] = ka < 128 * nt && rws[ka] >= 0 ? rws[ka] : INT_MAX;
+    srt[kb] = kb < 128 * nt && rws[kb] >= 0 ? rws[kb] : INT_MAX;
+    named_barrier(2, kConvThreads);
+    for (int k = 2; k <= kKeysQk; k <<= 1) {
+      for (int h = k >> 1; h > 0; h >>= 1) {
+        const int i = (lj / h) * 2 * h + lj % h, o = i + h;   // one pair per thread
+        const int x = srt[i], y = srt[o];
+        if ((x > y) == ((i & k) == 0)) {
+          srt[i] = y;
+          srt[o] = x;
+        }
+        named_barrier(2, kConvThreads);
+      }
+    }
+    const int ra = srt[ka] != INT_MAX ? srt[ka] : -1;
+    const int rb = srt[kb] != INT_MAX ? srt[kb] : -1;
+    if (ka < 128 * nt) rws[ka] = ra;
+    if (kb < 128 * nt) rws[kb] = rb;
+    key_ok[ka] = ra >= 0;
+    key_ok[kb] = rb >= 0;
     const uint8_t* pa = ra >= 0 ? a.pool + static_cast<size_t>(ra) * kRow : nullptr;
     const uint8_t* pb = rb >= 0 ? a.pool + static_cast<size_t>(rb) * kRow : nullptr;
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -324,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the workspace.
     const int sw = warp & 3, part = (warp - kConv0) >> 2, r = sw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+    named_barrier(1, kThreads - kConv0 * 32);   // the converters' key_ok flags are written
     wait_bar(&sh.s_full, 0, a.err);
     __syncwarp();
     tc_fence_after_sync();
-    const int32_t* rws = a.rows + static_cast<size_t>(t) * a.Sp + key0;
     uint16_t* prow = a.p + (static_cast<size_t>(t) * kQN + r) * a.Sp + key0;
     const int ntile = a.Sp / 128;
     for (int n = part; n < nt; n += 3) {
@@ -340,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb0 = 128 * n + 32 * cc;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const int4 rr = __ldg(reinterpret_cast<const int4*>(rws + kb0 + i));
-          m = fmaxf(m, fmaxf(fmaxf(rr.x >= 0 ? __uint_as_float(v[i]) : -INFINITY,
-                                   rr.y >= 0 ? __uint_as_float(v[i + 1]) : -INFINITY),
-                             fmaxf(rr.z >= 0 ? __uint_as_float(v[i + 2]) : -INFINITY,
-                                   rr.w >= 0 ? __uint_as_float(v[i + 3]) : -INFINITY)));
+          const uchar4 rr = *reinterpret_cast<const uchar4*>(key_ok + kb0 + i);
+          m = fmaxf(m, fmaxf(fmaxf(rr.x ? __uint_as_float(v[i]) : -INFINITY,
+                                   rr.y ? __uint_as_float(v[i + 1]) : -INFINITY),
+                             fmaxf(rr.z ? __uint_as_float(v[i + 2]) : -INFINITY,
+                                   rr.w ? __uint_as_float(v[i + 3]) : -INFINITY)));
         }
       }
       m = m > -INFINITY ? m * a.scale_log2 : -INFINITY;   // scale_log2 > 0 keeps the order
@@ -359,11 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const int4 rr = __ldg(reinterpret_cast<const int4*>(rws + kb0 + i));
-          const float p0 = rr.x >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i]), a.scale_log2, nm)) : 0.f;
-          const float p1 = rr.y >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), a.scale_log2, nm)) : 0.f;
-          const float p2 = rr.z >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i + 2]), a.scale_log2, nm)) : 0.f;
-          const float p3 = rr.w >= 0 ? fast_exp2(fmaf(__uint_as_float(v[i + 3]), a.scale_log2, nm)) : 0.f;
+          const uchar4 rr = *reinterpret_cast<const uchar4*>(key_ok + kb0 + i);
+          const float p0 = rr.x ? fast_exp2(fmaf(__uint_as_float(v[i]), a.scale_log2, nm)) : 0.f;
+          const float p1 = rr.y ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), a.scale_log2, nm)) : 0.f;
+          const float p2 = rr.z ? fast_exp2(fmaf(__uint_as_float(v[i + 2]), a.scale_log2, nm)) : 0.f;
+          const float p3 = rr.w ? fast_exp2(fmaf(__uint_as_float(v[i + 3]), a.scale_log2, nm)) : 0.f;
           l += (p0 + p1) + (p2 + p3);
           const __nv_bfloat162 b0 = __floats2bfloat162_rn(p0, p1);
           const __nv_bfloat162 b1 = __floats2bfloat162_rn(p2, p3);
