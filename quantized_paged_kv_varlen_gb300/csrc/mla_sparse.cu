@@ -11,19 +11,18 @@
 //
 // The 128 q heads of a token share its keys, so both products are GEMMs:
 // S[128 heads x n] = Q[128 x 576] . K^T and O[128 x 512] = P . V.  An fp32
-// O of 128 x 512 alone fills tensor memory, so the path runs as four
+// O of 128 x 512 alone fills tensor memory, so the path runs as three
 // stream-ordered kernels:
-//   mla_prep     sparse ids -> pool rows (block_table lookup; -1 for ids
-//                after the first -1, outside [0, L_kv), or hidden by
-//                sparse_mode 3), and a bulk L2 prefetch of every listed row
-//   mla_qk       one CTA per (token, 512 keys): the group's rows sorted by
-//                pool row first (written back for the PV stage); Q and
-//                dequantised-K chunks
-//                of 64 dims stream through shared memory (TMA for Q, eight
-//                converter warps gather and dequantise the rows), S for the
-//                four 128-key tiles accumulates in tensor memory; the
-//                epilogue (12 warps) writes P_tile = 2^(x - m) as bf16 with
-//                each tile's row maximum m and sum
+//   mla_qk       one CTA per (token, 512 keys): the group's sparse ids ->
+//                pool rows (block_table lookup; -1 for ids after the first
+//                -1, outside [0, L_kv), or hidden by sparse_mode 3), sorted
+//                by pool row and written to the workspace for the PV stage;
+//                Q and dequantised-K chunks of 64 dims stream through shared
+//                memory (TMA for Q, eight converter warps gather and
+//                dequantise the rows), S for the four 128-key tiles
+//                accumulates in tensor memory; the epilogue (12 warps)
+//                writes P_tile = 2^(x - m) as bf16 with each tile's row
+//                maximum m and sum
 //   mla_softmax  per (token, head) row: the row's maximum M and sum L from
 //                the tile statistics, P = P_tile * 2^(m - M) / L in place,
 //                and the lse
@@ -86,14 +85,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// One whole cache row into L2 (656 bytes, 16-byte aligned): the gathers
-// later read it in pieces, which from DRAM would be single sectors.
-__device__ __forceinline__ void prefetch_row_l2(const void* p) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
-               "r"(kRow)
-               : "memory");
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -124,7 +115,7 @@ __device__ __forceinline__ void dequant16(const uint4& w, float s, uint4& p0, ui
 }
 
 
-// ----------------------------------------------------------------- prep
+// ---------------------------------------------------------- keys -> rows
 // Key j of token t is token id * sbs + j % sbs of the listed id
 // list[j / sbs] (sbs = sparse_block_size, 1 for token-wise lists) and
 // becomes a pool row, or -1: past the list (the first -1 of the token's
@@ -177,24 +168,6 @@ __device__ __forceinline__ int key_row(const MlaArgs& a, const int32_t* ids, con
   return pg * a.bs + kt % a.bs;
 }
 
-// Blocks (token, 256-key slice): rows in list order, and a bulk L2 prefetch
-// of every listed row.
-__global__ void __launch_bounds__(256) mla_prep_kernel(const MlaArgs a) {
-  const int t = static_cast<int>(blockIdx.x), j0 = static_cast<int>(blockIdx.y) * 256;
-  __shared__ int first_neg;
-  if (threadIdx.x == 0) first_neg = a.S;
-  __syncthreads();
-  const int32_t* ids = a.idx + static_cast<size_t>(t) * a.S;
-  for (int j = threadIdx.x; j < a.S; j += blockDim.x)
-    if (ids[j] == -1) atomicMin(&first_neg, j);
-  __syncthreads();
-  const TokenSeq q = token_seq(a, t, first_neg);
-  const int j = j0 + static_cast<int>(threadIdx.x);
-  const int r = key_row(a, ids, q, j);
-  if (r >= 0) prefetch_row_l2(a.pool + static_cast<size_t>(r) * kRow);
-  if (j < a.Sp) a.rows[static_cast<size_t>(t) * a.Sp + j] = r;
-}
-
 // ------------------------------------------------------------------- QK
 constexpr int kQkStage = 16384 + 4 * 16384;          // Q chunk + K chunk of 4 tiles
 constexpr int kQkSmem = 2 * kQkStage + 1024;
@@ -211,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ QkShared sh;
   __shared__ __align__(16) uint8_t key_ok[kKeysQk];   // key of this CTA has a pool row
   __shared__ int srt[kKeysQk];                         // the group's rows being sorted
+  __shared__ int first_neg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = static_cast<int>(blockIdx.x) / ngroups, g = static_cast<int>(blockIdx.x) % ngroups;
   const int key0 = g * kKeysQk;
@@ -275,12 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lj = tid - kConv0 * 32;
     const int ka = lj, kb = lj + 256;
     int32_t* rws = a.rows + static_cast<size_t>(t) * a.Sp + key0;
-    // The group's keys sorted by pool row (rows of -1 last): attention does
-    // not depend on the order of the keys, and the gathers then walk the
-    // pool in ascending order, neighbouring lanes on neighbouring pages.
-    // The sorted rows go back to the workspace for the PV stage.
-    srt[ka] = ka < 128 * nt && rws[ka] >= 0 ? rws[ka] : INT_MAX;
-    srt[kb] = kb < 128 * nt && rws[kb] >= 0 ? rws[kb] : INT_MAX;
+    // The pool rows of the group's keys (the first -1 of the token's list
+    // ends it) ...
+    const int32_t* ids = a.idx + static_cast<size_t>(t) * a.S;
+    if (lj == 0) first_neg = a.S;
+    named_barrier(2, kConvThreads);
+    for (int j = lj; j < a.S; j += kConvThreads)
+      if (__ldg(ids + j) == -1) atomicMin(&first_neg, j);
+    named_barrier(2, kConvThreads);
+    const TokenSeq tq = token_seq(a, t, first_neg);
+    const int r0 = ka < 128 * nt ? key_row(a, ids, tq, key0 + ka) : -1;
+    const int r1 = kb < 128 * nt ? key_row(a, ids, tq, key0 + kb) : -1;
+    // ... sorted by pool row (rows of -1 last): attention does not depend on
+    // the order of the keys, and the gathers then walk the pool in
+    // ascending order, neighbouring lanes on neighbouring pages.  The sorted
+    // rows go to the workspace for the PV stage.
+    srt[ka] = r0 >= 0 ? r0 : INT_MAX;
+    srt[kb] = r1 >= 0 ? r1 : INT_MAX;
     named_barrier(2, kConvThreads);
     for (int k = 2; k <= kKeysQk; k <<= 1) {
       for (int h = k >> 1; h > 0; h >>= 1) {
@@ -692,10 +677,7 @@ cudaError_t launch_mla_sparse(const qpkv_mla_params& p, cudaStream_t stream, int
     *status = QPKV_ERR_CUDA;
     return cudaErrorInvalidValue;
   }
-  mla_prep_kernel<<<dim3(T, Sp / 256 + (Sp % 256 ? 1 : 0)), 256, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(mla_qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmem);
+  cudaError_t e = cudaFuncSetAttribute(mla_qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkSmem);
   if (e != cudaSuccess) return e;
   const int ngroups = (Sp + kKeysQk - 1) / kKeysQk;
   mla_qk_kernel<<<T * ngroups, kThreads, kQkSmem, stream>>>(qm, a, ngroups);
