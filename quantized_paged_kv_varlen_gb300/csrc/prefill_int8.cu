@@ -18,14 +18,14 @@
 // softmax scale multiply the logits of a tile at once (q and key tiles are
 // aligned to the 128-token blocks).
 //
-// One persistent CTA per SM, 15 warps:
-//   warp 0     issues the int8 Q and K copies (K rows of the pages a key
-//              tile spans, one lane per page box; pages past L_kv read as
-//              zeros) up to four tiles ahead, with the page ids fetched two
-//              tiles earlier into a shared ring (IdRing)
-//   warps 11-14 convert every staged int8 tile (per work item its 128-row
+// One persistent CTA per SM, 12 warps:
+//   warps 0, 11  convert every staged int8 tile (per work item its 128-row
 //              Q tile, then each key tile) into the f16 K-major SW128
-//              operand layout, one 32-column quarter each
+//              operand layout, one 64-column half each; lane 0 of warp 0
+//              issues the int8 Q and K copies (K rows of the pages a key
+//              tile spans; pages past L_kv read as zeros) up to three steps
+//              ahead, with the page ids fetched two tiles earlier into a
+//              shared ring (IdRing)
 //   warp 1     QK MMAs  S[128 q x 128 k] = Q16 . K16^T        (kind::f16)
 //   warp 10    PV MMAs  O[128 q x 128 d] += P . V, and the V copies (one
 //              box per page and 64-column half for bf16 V, one per page
@@ -60,9 +60,8 @@ namespace {
 
 constexpr int kT = 128;                 // q rows per tile = keys per tile
 constexpr int kD = 128;                 // head dim
-constexpr int kThreads = 480;           // 15 warps
-constexpr int kWarpLoad = 0, kWarpQk = 1, kWarpPv = 10, kWarpConv0 = 11;
-constexpr int kConvThreads = 128;       // warps 11-14: one 32-column quarter each
+constexpr int kThreads = 384;           // 12 warps
+constexpr int kWarpLoad = 0, kWarpQk = 1, kWarpPv = 10, kWarpConv = 11;
 constexpr int kSoftmax = 256;           // two threads per query row
 constexpr int kK8Stages = 4;            // staged int8 Q / K tiles
 constexpr int kK16Bufs = 2;             // converted K tiles
@@ -247,34 +246,31 @@ struct Items {
   }
 };
 
-// Conversion of one 32-column quarter of an int8 tile (128 rows of 128
-// codes, SW128 as TMA wrote it) into the f16 K-major SW128 operand (two
-// 64-column halves; quarter `part` holds operand columns [32 part, +32)).
-// Both operands place the codes of a 4-byte group (d0 d1 d2 d3) as the f16
-// pairs (d0, d2), (d1, d3): the same order on both sides, so the dot
-// products are unchanged.
+// Conversion of one 64-column half of an int8 tile (128 rows of 128 codes,
+// SW128 as TMA wrote it) into the f16 K-major SW128 operand (half `part`
+// holds operand columns [64 part, 64 part + 64)).  Both operands place the
+// codes of a 4-byte group (d0 d1 d2 d3) as the f16 pairs (d0, d2), (d1, d3):
+// the same order on both sides, so the dot products are unchanged.
 //   Q (exact):  f16 bits 0x6400 | (x ^ 0x80) = 1152 + x, minus 1152.
 //   K (biased): f16 bits (x ^ 0x80) = (x + 128) * 2^-24, a subnormal; then
 //               S' = 2^-24 (q . k + 128 sum_d q_d), all integers below 2^22,
 //               and the softmax takes the row constant 128 sum_d q_d back out.
-// Lane (r7, cq, rg) takes rows 8 (2g + rg) + r7 and source chunk
-// 2 part + cq, so the eight lanes of a quarter-warp touch eight distinct
-// 16-byte bank groups on both sides; for K four rows are loaded before any
-// is stored.
+// Lane (r7, cq) takes rows 8g + r7 and source chunk 4 part + cq, so the
+// eight lanes of a quarter-warp touch eight distinct 16-byte bank groups on
+// both sides; for K four rows are loaded before any is stored.
 template <bool kIsQ>
-__device__ __forceinline__ void convert_quarter(const uint8_t* src, uint8_t* dst, int lane,
-                                                int part) {
-  const int r7 = lane & 7, c = 2 * part + ((lane >> 3) & 1), rg = lane >> 4;
-  const uint8_t* s0 = src + r7 * 128 + ((c ^ r7) << 4) + rg * 1024;
-  uint8_t* d0 = dst + (c >> 2) * kHalf + r7 * 128 + rg * 1024;
+__device__ __forceinline__ void convert_half(const uint8_t* src, uint8_t* dst, int lane, int part) {
+  const int r7 = lane & 7, c = 4 * part + (lane >> 3);
+  const uint8_t* s0 = src + r7 * 128 + ((c ^ r7) << 4);
+  uint8_t* d0 = dst + part * kHalf + r7 * 128;
   const int g0 = 2 * (c & 3);
   const int o0 = (g0 ^ r7) << 4, o1 = ((g0 + 1) ^ r7) << 4;
   constexpr int kBatch = kIsQ ? 1 : 4;   // Q: once per work item, kept small
 #pragma unroll 1
-  for (int g = 0; g < 8; g += kBatch) {
+  for (int g = 0; g < 16; g += kBatch) {
     uint4 w[kBatch];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) w[i] = *reinterpret_cast<const uint4*>(s0 + (g + i) * 2048);
+    for (int i = 0; i < kBatch; ++i) w[i] = *reinterpret_cast<const uint4*>(s0 + (g + i) * 1024);
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const uint32_t ws[4] = {w[i].x ^ 0x80808080u, w[i].y ^ 0x80808080u, w[i].z ^ 0x80808080u,
@@ -290,7 +286,7 @@ __device__ __forceinline__ void convert_quarter(const uint8_t* src, uint8_t* dst
           h[2 * k + 1] = (ws[k] >> 8) & 0x00FF00FFu;
         }
       }
-      uint8_t* d = d0 + (g + i) * 2048;
+      uint8_t* d = d0 + (g + i) * 1024;
       *reinterpret_cast<uint4*>(d + o0) = make_uint4(h[0], h[1], h[2], h[3]);
       *reinterpret_cast<uint4*>(d + o1) = make_uint4(h[4], h[5], h[6], h[7]);
     }
@@ -376,12 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kK8Stages; ++s) {
       mbar_init(&sh.k8_full[s], 1);
-      mbar_init(&sh.k8_empty[s], kConvThreads);
+      mbar_init(&sh.k8_empty[s], 64);
     }
-    mbar_init(&sh.q16_full, kConvThreads);
+    mbar_init(&sh.q16_full, 64);
     mbar_init(&sh.q16_free, 1);
     for (int s = 0; s < kK16Bufs; ++s) {
-      mbar_init(&sh.k16_full[s], kConvThreads);
+      mbar_init(&sh.k16_full[s], 64);
       mbar_init(&sh.k16_empty[s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
@@ -422,61 +418,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     return id * a.ps + page_offset(a, j, e);
   };
 
-  if (warp == kWarpLoad) {
-    // ------------------------------------------------ Q / K int8 copies
-    // The warp walks the q / key tiles of the work items in order (per item
-    // its Q tile, then its key tiles) and fills the staging ring; a key
-    // tile's page boxes leave from one lane each in a single instruction (a
-    // thread's tensor copies are issued one after another).  Lane 0 keeps
-    // the page-id ring.  Its only wait is for a stage the converters have
-    // finished with.
-    TileWalk ld;
+  if (warp == kWarpLoad || warp == kWarpConv) {
+    // ----------------------------------- Q / K copies and int8 -> f16
+    // Both warps walk the q / key tiles of the work items in order (per
+    // item its Q tile, then its key tiles) and convert one 64-column half
+    // each.  Lane 0 of warp 0 also issues the int8 copies, up to three
+    // steps ahead of the step being converted; its only wait is for a
+    // stage both warps have finished with, which needs no later step here.
+    const int part = warp == kWarpLoad ? 0 : 1;
+    const bool issuer = part == 0 && lane == 0;
+    TileWalk cv, ld;
     const IdRing kr{sh.kring};
-    int ipos = 0;
-    if (lane == 0) {
+    cv.start(a, true);
+    int kpos = 0, ipos = 0, c16 = 0;
+    if (issuer) {
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&k_map);
+      ld.start(a, true);
+      if (ld.live) kr.advanced(a, ld.t, ld.j, -1);
     }
-    ld.start(a, true);
-    if (ld.live && lane == 0) kr.advanced(a, ld.t, ld.j, -1);
-    while (ld.live) {
-      const int s = ipos % kK8Stages;
-      int w = 1;
-      if (lane == 0) w = awaitb(&sh.k8_empty[s], ((ipos / kK8Stages) & 1) ^ 1, sh, a.err) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, w, 0) == 0) break;
-      uint8_t* dst = smem + kOffK8 + s * kI8Tile;
-      const Tile& t = ld.t;
-      if (lane == 0) {
+    auto issue = [&](int upto) -> bool {
+      while (ld.live && ipos <= upto) {
+        const int s = ipos % kK8Stages;
+        if (!awaitb(&sh.k8_empty[s], ((ipos / kK8Stages) & 1) ^ 1, sh, a.err)) return false;
         mbar_arrive_expect_tx(&sh.k8_full[s], kI8Tile);
-        if (ld.j >= 0) cp_async_wait_but_one();   // the tile's page ids landed
+        uint8_t* dst = smem + kOffK8 + s * kI8Tile;
+        const Tile& t = ld.t;
+        if (ld.j < 0) {
+          tma_load_3d(dst, &q_map, &sh.k8_full[s], 0, t.h, t.begin + t.qt * kT);
+        } else {
+          cp_async_wait_but_one();
+#pragma unroll 1
+          for (int i = 0; i < a.nbox; ++i)
+            tma_load_3d(dst + i * a.rows_box * 128, &k_map, &sh.k8_full[s], 0, t.hk,
+                        page_row(ld.t, sh.kring, i, ld.j));
+        }
+        ++ipos;
+        ld.next(a);
+        if (ld.live) kr.advanced(a, ld.t, ld.j, -1);
       }
-      __syncwarp();
-      if (ld.j < 0) {
-        if (lane == 0) tma_load_3d(dst, &q_map, &sh.k8_full[s], 0, t.h, t.begin + t.qt * kT);
-      } else if (lane < a.nbox) {
-        tma_load_3d(dst + lane * a.rows_box * 128, &k_map, &sh.k8_full[s], 0, t.hk,
-                    page_row(ld.t, sh.kring, lane, ld.j));
-      }
-      __syncwarp();
-      ++ipos;
-      ld.next(a);
-      if (ld.live && lane == 0) kr.advanced(a, ld.t, ld.j, -1);
-    }
-    if (lane == 0) {
-      cp_async_wait_all();
-      for (int i = ipos > kK8Stages ? ipos - kK8Stages : 0; i < ipos; ++i)
-        drain(&sh.k8_full[i % kK8Stages], (i / kK8Stages) & 1, a.err);
-    }
-    __syncwarp();
-  } else if (warp >= kWarpConv0) {
-    // -------------------------------------------------- int8 -> f16
-    // Warps 11-14 walk the same tiles and convert one 32-column quarter
-    // each.
-    const int part = warp - kWarpConv0;
-    TileWalk cv;
-    cv.start(a, true);
-    int kpos = 0, c16 = 0;
+      return true;
+    };
     for (int o = 0; cv.live; cv.next(a)) {
+      bool ok = true;
+      if (issuer) ok = issue(kpos + kK8Stages - 1);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
       const bool is_q = cv.j < 0;
       const int s = kpos % kK8Stages, d = c16 % kK16Bufs;
       bool w = is_q ? awaitb(&sh.q16_free, (o & 1) ^ 1, sh, a.err)
@@ -485,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, w)) break;
       const uint8_t* src = smem + kOffK8 + s * kI8Tile;
       if (is_q)
-        convert_quarter<true>(src, smem + kOffQ16, lane, part);
+        convert_half<true>(src, smem + kOffQ16, lane, part);
       else
-        convert_quarter<false>(src, smem + kOffK16 + d * kH16Tile, lane, part);
+        convert_half<false>(src, smem + kOffK16 + d * kH16Tile, lane, part);
       fence_proxy_async_smem();   // generic writes -> tensor-core reads
       mbar_arrive(is_q ? &sh.q16_full : &sh.k16_full[d]);
       mbar_arrive(&sh.k8_empty[s]);
@@ -498,6 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++c16;
       }
     }
+    if (issuer) {
+      cp_async_wait_all();
+      for (int i = ipos > kK8Stages ? ipos - kK8Stages : 0; i < ipos; ++i)
+        drain(&sh.k8_full[i % kK8Stages], (i / kK8Stages) & 1, a.err);
+    }
+    __syncwarp();
   } else if (warp == kWarpQk) {
     // ------------------------------------------------------------ QK MMA
     if (lane == 0) {
