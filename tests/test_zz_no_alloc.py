@@ -9,6 +9,7 @@ with nothing recorded, and oversized batches must be rejected on the host.
 This file sorts last so that a run stopping at the first failure has
 already run every other test."""
 import ctypes
+import gc
 
 import numpy as np
 import pytest
@@ -85,14 +86,23 @@ def test_static_decode_matches_planned_decode_twice(lib, which):
         out = torch.full_like(q, float("nan"))
         lse = torch.full((wl.B, wl.Hq), float("nan"), dtype=torch.float32, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        # collect first and keep the collector off across the call, so that
+        # tensors of earlier tests freed meanwhile do not move the counters
+        gc.collect()
         torch.cuda.synchronize()
-        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
-        assert _call_static(raw, wl, wl.lengths, q, d, out, lse, err, sms) == 0
-        torch.cuda.synchronize()
+        gc.disable()
+        try:
+            free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+            status = _call_static(raw, wl, wl.lengths, q, d, out, lse, err, sms)
+            torch.cuda.synchronize()
+            free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
+        assert status == 0
         if call == 1:
             # nothing allocated by the call itself (the first call may load modules)
-            assert torch.cuda.mem_get_info()[0] == free0
-            assert torch.cuda.memory_allocated() == alloc0
+            assert free1 == free0
+            assert alloc1 == alloc0
         assert int(err.item()) == 0
         assert_attention_close(bf16_to_f64(out), bf16_to_f64(ref))
         assert_lse_close(lse.cpu().numpy(), ref_lse.cpu().numpy())
