@@ -253,3 +253,27 @@ def test_mla_tnd_keys_through_block_size_one(lib):
                                               cu_q, 1.0 / 24.0)
     assert_attention_close(bf16_to_f64(out), want_o)
     assert_lse_close(lse.cpu().numpy().astype(np.float64), want_lse)
+
+
+def test_mla_permuted_ids_give_the_same_output(lib):
+    """The kernel regroups a token's keys by pool row; any order of the
+    listed ids gives the oracle's result (which does not depend on it), over
+    several 512-key groups."""
+    c = _case(77, [1500, 900], 1, 64, 64, 1280, 1100)
+    pool = _gpu_pool(lib, c)
+    got_o, got_lse, err = _run(lib, c, pool, 0)
+    assert err == 0
+    rng = np.random.default_rng(78)
+    c2 = dict(c)
+    idx2 = c["idx"].copy()
+    for t in range(idx2.shape[0]):
+        n = int((idx2[t, 0] >= 0).sum())
+        idx2[t, 0, :n] = idx2[t, 0, :n][rng.permutation(n)]
+    c2["idx"] = idx2
+    got2_o, got2_lse, err2 = _run(lib, c2, pool, 0)
+    assert err2 == 0
+    want_o, want_lse = omla.mla_sparse_decode(c["q"], _oracle_pool(c), c["idx"], c["bt"],
+                                              c["lengths"], c["cu_q"], c["scale"])
+    for o, l in ((got_o, got_lse), (got2_o, got2_lse)):
+        assert_attention_close(o, want_o)
+        assert_lse_close(l, want_lse)

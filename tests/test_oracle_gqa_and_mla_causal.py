@@ -175,3 +175,32 @@ def test_mla_sparse_mode3_right_down_causal():
                                   np.array([c["Lq"]]), scale, sparse_mode=0)
     assert np.allclose(O0, _expected(c, lambda i, j: True, scale), rtol=1e-12, atol=1e-13)
     assert _differs_somewhere(O0[0], O[0]) and np.allclose(O0[2], O[2], rtol=1e-13, atol=1e-14)
+
+
+def test_mla_order_of_the_listed_ids_does_not_matter():
+    """The keys of a token are a set: the oracle's output and lse are the same
+    for any order of the ids before the first -1 (the kernel sorts each
+    512-key group by pool row and relies on this).  The -1 that ends the list
+    is part of the reading: moving it changes which ids count, and that does
+    change the result."""
+    rng = np.random.default_rng(23)
+    L, bs, QN = 300, 16, 4
+    bt, P = synth.page_tables(rng, np.array([L], np.int32), bs)
+    kv = synth.bf16_normal(rng, (L, 576))
+    q = synth.bf16_normal(rng, (1, QN, 576))
+    pool = np.zeros((P, bs, 1, 656), np.uint8)
+    pool, _ = cache.write_mla_rows(kv, np.array([L], np.int32), np.zeros(1, np.int64), bt, bs, pool)
+    ids = rng.permutation(L)[:120].astype(np.int32)
+    idx = np.full((1, 1, 160), -1, np.int32)
+    idx[0, 0, :120] = ids
+    lk, cu = np.array([L], np.int32), np.array([1], np.int32)
+    o1, l1 = mla.mla_sparse_decode(q, pool, idx, bt, lk, cu, 1.0 / np.sqrt(576.0))
+    idx2 = idx.copy()
+    idx2[0, 0, :120] = ids[rng.permutation(120)]
+    o2, l2 = mla.mla_sparse_decode(q, pool, idx2, bt, lk, cu, 1.0 / np.sqrt(576.0))
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
+    # the first -1 ends the list: ids after it are not keys
+    idx3 = idx.copy()
+    idx3[0, 0, 60] = -1
+    o3, _ = mla.mla_sparse_decode(q, pool, idx3, bt, lk, cu, 1.0 / np.sqrt(576.0))
+    assert _differs_somewhere(o1, o3)
