@@ -687,10 +687,19 @@ def run_extras(device, iters=10):
     ms_w = _median_ms(wr, iters)
     flops = float(sum(4.0 * D * H * int(x) * (int(x) + 1) / 2 for x in L))
     tf = flops / (ms / 1e3) / 1e12
+    # the write moves bf16 q, k, v in and int8 q, int8 k, bf16 v out (the
+    # per-block scales are a few KB): 10 bytes per (token, head, dim)
+    w_bytes = float(T) * H * D * (2 + 2 + 2 + 1 + 1 + 2)
+    w_gbs = w_bytes / (ms_w / 1e3) / 1e9
     out["int8_prefill_varlen"] = {
         "workload": f"varlen causal prefill {len(L)} seqs L={L.tolist()} H={H} D={D} page 64, "
                     "INT8 Q/K block-128 scales, bf16 V",
         "ms": ms, "value": tf, "unit": "TFLOP/s", "flops": flops, "write_cache_ms": ms_w,
+        "write_cache_roofline": {
+            "bound": "hbm", "bytes": w_bytes, "achieved": w_gbs, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": w_gbs / pk["hbm_gbs"],
+            "traffic": _extra_traffic("write_int8_block128_rope_8seqs_h32.txt", "write_cache.cu"),
+            "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16, "unit": "TFLOP/s",
                      "frac": tf / bf16, "peak_source": "measured bf16_tflops (f16/bf16 MMAs)",
                      "traffic": _extra_traffic("prefill_int8_8seqs_h32_page64.txt",

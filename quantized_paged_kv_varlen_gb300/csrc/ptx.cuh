@@ -166,6 +166,14 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
                : "memory");
 }
 
+// The same copy reading src_bytes (0 or 16) bytes; the rest of the 16 are
+// zero-filled (nothing is read for 0).
+__device__ __forceinline__ void cp_async_16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
 // Wait until every cp.async this thread issued has landed in shared memory.
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -178,6 +186,11 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 __device__ __forceinline__ void cp_async_wait_but_one() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+// Wait until all but the N most recent groups have landed.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

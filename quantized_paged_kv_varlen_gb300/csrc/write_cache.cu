@@ -8,9 +8,11 @@
 // 功能说明.  Memory-bound elementwise work with small reductions: plain SIMT
 // with 16-byte vector accesses, no tensor cores.
 //
-// Rounding is explicit so the bytes are reproducible: IEEE float32 division
-// (__fdiv_rn), nearest-even conversions, RoPE products and sums rounded
-// separately (__fmul_rn / __fadd_rn / __fsub_rn, no contraction).
+// Rounding is explicit so the bytes are reproducible: the codes are those
+// of IEEE float32 division (__fdiv_rn, or a reciprocal product where that
+// provably rounds the same way), nearest-even conversions, RoPE products
+// and sums rounded separately (__fmul_rn / __fadd_rn / __fsub_rn, no
+// contraction).
 //
 // Options: the HND K/V pool layout (FP8 mode); K smoothing and E4M3 V with
 // per-channel scales (INT8 mode: a first pass writes exact per-block
@@ -166,105 +168,135 @@ __global__ void __launch_bounds__(256) rope_q_kernel(
 }
 
 // ------------------------------- INT8 per-(sequence, 128-token block, head)
-// One CTA (256 threads) per (block, head, sequence).  Thread tid owns token
-// r = tid / 2 of the block and RoPE pairs i in [32*(tid%2), 32*(tid%2)+32),
-// i.e. elements i and i + 64 of the 128-wide head.
+// One CTA of 1024 threads per (sequence, 128-token block, group of kWrHeads
+// heads).  Thread tid owns token row r = tid / 8 of the block and the eight
+// RoPE pairs i in [8j, 8j + 8), j = tid % 8: elements [8j, 8j + 8) and
+// [64 + 8j, 64 + 8j + 8) of every 128-wide head.  A row's cos / sin values
+// and page slot are the same for all heads, so they are read once.  The CTA
+// then walks its heads: every thread copies its own 96 input bytes (Q, K
+// and V) of the next head into a two-stage shared-memory ring with cp.async
+// while the current head is processed.  Q and K are rotated once for their
+// maxima (one block-wide barrier for both), then rotated again from the
+// ring and quantised, which keeps the loop within the 64 registers a
+// 1024-thread CTA allows; V is stored as it is.  A thread reads back only
+// what it copied, so the ring needs no barrier.  The division by the block
+// scale is a multiply by its reciprocal, with the exact division taken for
+// a group of four codes when one of them sits near a rounding boundary.
 constexpr int kBlk = 128;
+constexpr int kWrThreads = 1024, kWrHeads = 8;
+constexpr int kWrPlane = kWrThreads * 16;            // one 16-byte half of one tensor
+constexpr int kWrStage = 6 * kWrPlane;               // Q, K, V halves of one head
+constexpr int kWrSmem = 2 * kWrStage;
+static_assert(kWrThreads == 8 * kBlk && kWrThreads / 32 == 32, "one row per 8 threads");
 
-__device__ __forceinline__ void load_bf16x8(const uint16_t* src, float (&x)[8]) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(src);
+// 1.5 * 2^23: a float of magnitude below 2^22 plus this constant, rounded
+// to float32, is the constant plus the value rounded to an integer (nearest
+// even), held in the low mantissa bits.
+constexpr float kRoundMagic = 12582912.0f;
+// With s = float32(amax / 127) and inv = float32(127 / amax), the product
+// p = float32(y * inv) lies within 3 * 2^-24 * |y / s| of y / s, and the
+// correctly rounded quotient float32(y / s) within 2^-24 * |y / s|; as
+// |y / s| <= 127.00001 (|y| <= amax), the two are at most 3.1e-5 apart.  A
+// product further than 1e-4 from every half-integer therefore rounds to the
+// same integer as the quotient; closer ones take the exact division, and so
+// does every code when s lies outside [1e-30, 1e30] (1 / amax not normal).
+constexpr float kNearHalf = 0.4999f;
+
+// Fast INT8 code of y / s: returns kRoundMagic + n (n = the code), whose low
+// byte is n's two's-complement byte, and folds |p - n| into dev.
+__device__ __forceinline__ float int8_code_fast(float y, float inv, float& dev) {
+  const float p = __fmul_rn(y, inv);
+  const float f = __fadd_rn(p, kRoundMagic);
+  dev = fmaxf(dev, fabsf(__fsub_rn(p, __fsub_rn(f, kRoundMagic))));
+  return f;
+}
+
+// The same code from the correctly rounded float32 quotient, in the same
+// encoding: clamp(RNE(y / scale), -127, 127), 0 for a zero scale.
+__device__ __forceinline__ float int8_code_exact(float y, float scale) {
+  const int c = scale != 0.f ? min(127, max(-127, __float2int_rn(__fdiv_rn(y, scale)))) : 0;
+  return __int_as_float(__float_as_int(kRoundMagic) + c);
+}
+
+// Low bytes of four codes in kRoundMagic + n form -> one little-endian word.
+__device__ __forceinline__ uint32_t low_bytes4(float a, float b, float c, float d) {
+  const uint32_t lo = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0040);
+  const uint32_t hi = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&x)[8]) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFF);
-    x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = bf16_bits_to_float(w[e] & 0xFFFF);
+    x[2 * e + 1] = bf16_bits_to_float(w[e] >> 16);
   }
 }
 
-__device__ __forceinline__ float block_max_256(float v, float* red) {
-  v = warp_max(v);
-  const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) red[warp] = v;
-  __syncthreads();
-  float m = red[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
-  __syncthreads();
-  return m;
+__device__ __forceinline__ void load_bf16x8(const uint16_t* src, float (&x)[8]) {
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(src), x);
 }
 
-// Rotate, subtract the smoothing mean km (shared, 128 floats; NULL: none),
-// quantise to INT8 with one block scale, and store the codes.
-// Returns nothing; writes codes to dst_row (128 int8) and the scale via *scale_out.
-__device__ __forceinline__ void rope_quant_block(const uint16_t* __restrict__ src_row, bool valid,
-                                                 int pos, int half, const float* __restrict__ cos_t,
-                                                 const float* __restrict__ sin_t, const float* km,
-                                                 int8_t* dst_row, float* scale_out, float* red) {
-  float y1[32], y2[32];
+// Rotate-half RoPE of one thread's 8 pairs (products and sums rounded
+// separately), minus the smoothing mean km (shared, 128 floats; NULL: none);
+// y[0..7] are elements 8j + e, y[8..15] elements 64 + 8j + e.  Rows outside
+// the sequence come out zero: their ring bytes and cos / sin are zero and
+// they pass no mean.  Returns the bits of max |y| (non-negative floats order
+// like their bit patterns).
+__device__ __forceinline__ uint32_t rope_row(const uint4& lo, const uint4& hi,
+                                             const float (&cs)[8], const float (&sn)[8],
+                                             const float* km, int j, float (&y)[16]) {
+  float a[8], c[8];
+  unpack_bf16x8(lo, a);
+  unpack_bf16x8(hi, c);
   float amax = 0.f;
-  if (valid) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float a[8], bb[8];
-      load_bf16x8(src_row + half * 32 + c * 8, a);
-      load_bf16x8(src_row + 64 + half * 32 + c * 8, bb);
-      // this chunk's 8 cos / sin values: two 16-byte loads each
-      const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * 64 +
-                                                         half * 32 + c * 8);
-      const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * 64 +
-                                                         half * 32 + c * 8);
-      const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
-      const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float cs = cv[j];
-        const float sn = sv[j];
-        float r1 = __fsub_rn(__fmul_rn(a[j], cs), __fmul_rn(bb[j], sn));
-        float r2 = __fadd_rn(__fmul_rn(bb[j], cs), __fmul_rn(a[j], sn));
-        if (km != nullptr) {
-          r1 = __fsub_rn(r1, km[half * 32 + c * 8 + j]);
-          r2 = __fsub_rn(r2, km[64 + half * 32 + c * 8 + j]);
-        }
-        y1[c * 8 + j] = r1;
-        y2[c * 8 + j] = r2;
-        amax = fmaxf(amax, fmaxf(fabsf(r1), fabsf(r2)));
-      }
+  for (int e = 0; e < 8; ++e) {
+    float r1 = __fsub_rn(__fmul_rn(a[e], cs[e]), __fmul_rn(c[e], sn[e]));
+    float r2 = __fadd_rn(__fmul_rn(c[e], cs[e]), __fmul_rn(a[e], sn[e]));
+    if (km != nullptr) {
+      r1 = __fsub_rn(r1, km[8 * j + e]);
+      r2 = __fsub_rn(r2, km[64 + 8 * j + e]);
     }
+    y[e] = r1;
+    y[8 + e] = r2;
+    amax = fmax3(amax, fabsf(y[e]), fabsf(y[8 + e]));
   }
-  amax = block_max_256(amax, red);
+  return __float_as_uint(amax);
+}
+
+// Scale amax / 127 (float32 division) and the codes of y: fast path from
+// 127 / amax, exact division where a product sits near a half-integer or
+// the reciprocal would not be a normal float.  Stores the 16 codes at dst
+// (row base + 8j; NULL: none).
+__device__ __forceinline__ float quant_row(const float (&y)[16], float amax, int8_t* dst) {
   const float scale = __fdiv_rn(amax, 127.0f);
-  if (threadIdx.x == 0) *scale_out = scale;
-  if (!valid) return;
-  uint32_t w1[8], w2[8];
+  const float inv = __fdiv_rn(127.0f, amax);
+  const bool fast = scale >= 1e-30f && scale <= 1e30f;
+  uint32_t w[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t p1 = 0, p2 = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      int c1 = 0, c2 = 0;
-      if (scale != 0.f) {
-        c1 = min(127, max(-127, __float2int_rn(__fdiv_rn(y1[4 * j + e], scale))));
-        c2 = min(127, max(-127, __float2int_rn(__fdiv_rn(y2[4 * j + e], scale))));
-      }
-      p1 |= (static_cast<uint32_t>(c1) & 0xFFu) << (8 * e);
-      p2 |= (static_cast<uint32_t>(c2) & 0xFFu) << (8 * e);
-    }
-    w1[j] = p1;
-    w2[j] = p2;
+  for (int g = 0; g < 4; ++g) {
+    float dev = 0.f;
+    w[g] = low_bytes4(int8_code_fast(y[4 * g], inv, dev), int8_code_fast(y[4 * g + 1], inv, dev),
+                      int8_code_fast(y[4 * g + 2], inv, dev), int8_code_fast(y[4 * g + 3], inv, dev));
+    if (!fast || !(dev <= kNearHalf))   // rare: this group of four by division
+      w[g] = low_bytes4(int8_code_exact(y[4 * g], scale), int8_code_exact(y[4 * g + 1], scale),
+                        int8_code_exact(y[4 * g + 2], scale), int8_code_exact(y[4 * g + 3], scale));
   }
-  uint4* d1 = reinterpret_cast<uint4*>(dst_row + half * 32);
-  uint4* d2 = reinterpret_cast<uint4*>(dst_row + 64 + half * 32);
-  d1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-  d1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
-  d2[0] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-  d2[1] = make_uint4(w2[4], w2[5], w2[6], w2[7]);
+  if (dst != nullptr) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    *reinterpret_cast<uint2*>(dst + 64) = make_uint2(w[2], w[3]);
+  }
+  return scale;
 }
 
 // K smoothing, pass 1: per (sequence, 128-token block, kv head) the int64 sum
 // over the block's tokens of RNE(clamp(k_rot, -2^15, 2^15) * 2^24) per dim
-// (exact, so the order of the sums does not matter); two row phases of 128
-// threads, thread d owns dim d.  The rotation is the one the write applies.
+// (exact, so the order of the sums does not matter).  Thread tid takes rows
+// tid / 8 + 32 i and the eight RoPE pairs of j = tid % 8 (16-byte loads, as
+// in the write); the 32 row phases meet in shared memory.  The rotation is
+// the one the write applies.
 constexpr float kMeanClamp = 32768.0f, kMeanOne = 16777216.0f;   // 2^15, 2^24
 
 __global__ void __launch_bounds__(256) k_block_sum_kernel(
@@ -272,50 +304,99 @@ __global__ void __launch_bounds__(256) k_block_sum_kernel(
     const uint16_t* __restrict__ k,
     const float* __restrict__ cos_t, const float* __restrict__ sin_t,
     long long* __restrict__ partial) {
-  __shared__ long long part[128];
+  __shared__ long long part[32][128];
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int begin = seq_begin(cu, b);
   const int L = __ldg(cu + b) - begin;
   if (blk * kBlk >= L) return;
-  const int d = threadIdx.x & 127, phase = threadIdx.x >> 7, i = d & 63;
+  const int rp = threadIdx.x >> 3, j = threadIdx.x & 7;
   // tokens past the launched blocks or the RoPE tables are the write's to flag
   const int n = min(kBlk, min(L, max_pos) - blk * kBlk);
-  long long acc = 0;
-  for (int r = phase; r < n; r += 2) {
+  long long acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0;
+#pragma unroll
+  for (int i = 0; i < kBlk / 32; ++i) {
+    const int r = rp + 32 * i;
+    if (r >= n) break;
     const int pos = blk * kBlk + r;
-    const uint16_t* row = k + (static_cast<size_t>(begin + pos) * Hkv + h) * 128;
-    const float a = bf16_bits_to_float(__ldg(row + i)), bb = bf16_bits_to_float(__ldg(row + 64 + i));
-    const float cs = __ldg(cos_t + static_cast<size_t>(pos) * 64 + i);
-    const float sn = __ldg(sin_t + static_cast<size_t>(pos) * 64 + i);
-    const float y = d < 64 ? __fsub_rn(__fmul_rn(a, cs), __fmul_rn(bb, sn))
-                           : __fadd_rn(__fmul_rn(bb, cs), __fmul_rn(a, sn));
-    acc += __float2ll_rn(fminf(fmaxf(y, -kMeanClamp), kMeanClamp) * kMeanOne);
+    const uint16_t* row = k + (static_cast<size_t>(begin + pos) * Hkv + h) * 128 + 8 * j;
+    float a[8], c[8];
+    load_bf16x8(row, a);
+    load_bf16x8(row + 64, c);
+    const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * 64 + 8 * j);
+    const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * 64 + 8 * j);
+    const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float y1 = __fsub_rn(__fmul_rn(a[e], cs[e]), __fmul_rn(c[e], sn[e]));
+      const float y2 = __fadd_rn(__fmul_rn(c[e], cs[e]), __fmul_rn(a[e], sn[e]));
+      acc[e] += __float2ll_rn(fminf(fmaxf(y1, -kMeanClamp), kMeanClamp) * kMeanOne);
+      acc[8 + e] += __float2ll_rn(fminf(fmaxf(y2, -kMeanClamp), kMeanClamp) * kMeanOne);
+    }
   }
-  if (phase == 1) part[d] = acc;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    part[rp][8 * j + e] = acc[e];
+    part[rp][64 + 8 * j + e] = acc[8 + e];
+  }
   __syncthreads();
-  if (phase == 0)
-    partial[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + d] = acc + part[d];
+  if (threadIdx.x < 128) {
+    long long sum = 0;
+#pragma unroll 8
+    for (int p = 0; p < 32; ++p) sum += part[p][threadIdx.x];
+    partial[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + threadIdx.x] = sum;
+  }
 }
 
 // FP8 V, pass 1: per (sequence, 128-token block, kv head) the largest |v|
-// of each channel over the block's tokens (a maximum: order-free).
-__global__ void __launch_bounds__(128) v_block_max_kernel(
+// of each channel over the block's tokens (a maximum: order-free); the same
+// thread layout as the K sums.
+__global__ void __launch_bounds__(256) v_block_max_kernel(
     int Hkv, int num_blocks, const int32_t* __restrict__ cu, const uint16_t* __restrict__ v,
     float* __restrict__ vmax) {
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  __shared__ float part[32][128];
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int begin = seq_begin(cu, b);
   const int L = __ldg(cu + b) - begin;
   if (blk * kBlk >= L) return;
+  const int rp = threadIdx.x >> 3, j = threadIdx.x & 7;
   const int n = min(kBlk, L - blk * kBlk);
-  float m = 0.f;
-  for (int r = 0; r < n; ++r)
-    m = fmaxf(m, fabsf(bf16_bits_to_float(
-                     __ldg(v + (static_cast<size_t>(begin + blk * kBlk + r) * Hkv + h) * 128 + d))));
-  vmax[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + d] = m;
+  float m[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) m[e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kBlk / 32; ++i) {
+    const int r = rp + 32 * i;
+    if (r >= n) break;
+    const uint16_t* row = v + (static_cast<size_t>(begin + blk * kBlk + r) * Hkv + h) * 128 + 8 * j;
+    float a[8], c[8];
+    load_bf16x8(row, a);
+    load_bf16x8(row + 64, c);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      m[e] = fmaxf(m[e], fabsf(a[e]));
+      m[8 + e] = fmaxf(m[8 + e], fabsf(c[e]));
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    part[rp][8 * j + e] = m[e];
+    part[rp][64 + 8 * j + e] = m[8 + e];
+  }
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    float mx = 0.f;
+#pragma unroll 8
+    for (int p = 0; p < 32; ++p) mx = fmaxf(mx, part[p][threadIdx.x]);
+    vmax[((static_cast<size_t>(b) * num_blocks + blk) * Hkv + h) * 128 + threadIdx.x] = mx;
+  }
 }
 
-__global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
-    int B, int Hq, int Hkv, int ps, int num_pages, int bt_stride, int num_blocks,
+__global__ void __launch_bounds__(kWrThreads, 1) write_int8_block128_rope_kernel(
+    int B, int Hq, int Hkv, int ps, int num_pages, int bt_stride, int num_blocks, int nblk_launch,
     const int32_t* __restrict__ cu, const int32_t* __restrict__ bt,
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     const uint16_t* __restrict__ v, const float* __restrict__ cos_t,
@@ -324,101 +405,153 @@ __global__ void __launch_bounds__(256) write_int8_block128_rope_kernel(
     int32_t* __restrict__ slots, const long long* __restrict__ partial, float* __restrict__ k_mean,
     const float* __restrict__ vmax, float* __restrict__ v_cscale, int max_pos, int* err) {
   constexpr int D = 128;
-  __shared__ float red[8];
-  __shared__ float km[D];
-  __shared__ float vsc[D];
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  __shared__ uint2 red[2][32];          // per warp: max |y| bits of Q and of K
+  __shared__ float km[kWrHeads][D];    // K smoothing means of the group's heads
+  __shared__ float vsc[kWrHeads][D];   // FP8 V channel scales of the group's heads
+  extern __shared__ __align__(16) uint8_t ring[];
+  const int hmax = max(Hq, Hkv);
+  const int ngroups = (hmax + kWrHeads - 1) / kWrHeads;
+  const int hg = blockIdx.x % ngroups;
+  const int b = (blockIdx.x / ngroups) % B, blk = blockIdx.x / ngroups / B;
   const int begin = seq_begin(cu, b);
   const int L = __ldg(cu + b) - begin;
   if (blk * kBlk >= L) return;  // block past this sequence's end
   // a sequence longer than the launch (max_seqlen) or the RoPE tables
   const int nblk = (L + kBlk - 1) / kBlk;
-  if ((nblk > static_cast<int>(gridDim.x) || L > max_pos) && blk == 0 && h == 0 &&
-      threadIdx.x == 0)
+  if ((nblk > nblk_launch || L > max_pos) && blk == 0 && hg == 0 && threadIdx.x == 0)
     report_error(err, kDevErrBadLength);
-  const bool smooth = partial != nullptr && h < Hkv;
-  if (smooth) {
-    // K smoothing, pass 2: the sequence's mean from the exact block sums
-    if (threadIdx.x < D) {
-      long long sum = 0;
-      const int nsum = min(nblk, static_cast<int>(gridDim.x));
-      for (int j = 0; j < nsum; ++j)
-        sum += partial[((static_cast<size_t>(b) * num_blocks + j) * Hkv + h) * D + threadIdx.x];
-      const float m =
-          __double2float_rn(__ll2double_rn(sum) / (static_cast<double>(L) * static_cast<double>(kMeanOne)));
-      km[threadIdx.x] = m;
-      if (blk == 0) k_mean[(static_cast<size_t>(b) * Hkv + h) * D + threadIdx.x] = m;
-    }
-    __syncthreads();
-  }
-  const bool v8 = vmax != nullptr && h < Hkv;
-  if (v8) {
-    // FP8 V, pass 2: the channel's absmax over the sequence -> scale / 448
-    if (threadIdx.x < D) {
-      float amax = 0.f;
-      const int nsum = min(nblk, static_cast<int>(gridDim.x));
-      for (int j = 0; j < nsum; ++j)
-        amax = fmaxf(amax, vmax[((static_cast<size_t>(b) * num_blocks + j) * Hkv + h) * D + threadIdx.x]);
-      const float sc = __fdiv_rn(amax, 448.0f);
-      vsc[threadIdx.x] = sc;
-      if (blk == 0) v_cscale[(static_cast<size_t>(b) * Hkv + h) * D + threadIdx.x] = sc;
-    }
-    __syncthreads();
-  }
-  const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int h0 = hg * kWrHeads, nh = min(kWrHeads, hmax - h0);
+  const int r = threadIdx.x >> 3, j = threadIdx.x & 7;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pos = blk * kBlk + r;
   const bool valid = pos < L && pos < max_pos;
-  const int t = begin + pos;
+  const size_t t = static_cast<size_t>(begin + pos);
 
-  if (h < Hq) {
-    const uint16_t* src = q + (static_cast<size_t>(t) * Hq + h) * D;
-    int8_t* dst = q_out + (static_cast<size_t>(t) * Hq + h) * D;
-    rope_quant_block(src, valid, pos, half, cos_t, sin_t, nullptr, dst,
-                     q_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hq + h, red);
+  // ring stage s, tensor u (Q, K, V), half (elements 8j.. / 64 + 8j..):
+  // planes of 16 bytes per thread, so a warp's accesses are contiguous
+  auto at = [&](int s, int u, int half) {
+    return ring + s * kWrStage + (2 * u + half) * kWrPlane + threadIdx.x * 16;
+  };
+  auto copy_in = [&](int s, int u, const uint16_t* src) {
+    const uint32_t n = valid ? 16u : 0u;
+    cp_async_16_zfill(at(s, u, 0), src + 8 * j, n);
+    cp_async_16_zfill(at(s, u, 1), src + 64 + 8 * j, n);
+  };
+  auto fetch = [&](int hh) {
+    if (hh < nh) {
+      const int h = h0 + hh, s = hh & 1;
+      const size_t row = valid ? t : 0;
+      if (h < Hq) copy_in(s, 0, q + (row * Hq + h) * D);
+      if (h < Hkv) {
+        copy_in(s, 1, k + (row * Hkv + h) * D);
+        if (valid) copy_in(s, 2, v + (row * Hkv + h) * D);
+      }
+    }
+    cp_async_commit();
+  };
+  auto ring16 = [&](int s, int u, int half) { return *reinterpret_cast<const uint4*>(at(s, u, half)); };
+  fetch(0);
+
+  float cs[8], sn[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) cs[e] = sn[e] = 0.f;
+  if (valid) {
+    const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * 64 + 8 * j);
+    const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * 64 + 8 * j);
+    const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+    cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+    cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+    sn[0] = s0.x; sn[1] = s0.y; sn[2] = s0.z; sn[3] = s0.w;
+    sn[4] = s1.x; sn[5] = s1.y; sn[6] = s1.z; sn[7] = s1.w;
   }
-  if (h < Hkv) {
-    int page = 0;
-    if (valid) page = pool_page(bt, bt_stride, b, pos, ps, num_pages, half == 0 ? err : nullptr);
-    const bool ok = valid && page >= 0;
-    const size_t slot = static_cast<size_t>(ok ? page : 0) * ps + (pos % ps);
-    if (ok && slots != nullptr && h == 0 && half == 0) slots[t] = static_cast<int32_t>(slot);
-    const uint16_t* src = k + (static_cast<size_t>(t) * Hkv + h) * D;
-    int8_t* dst = k_pool + (slot * Hkv + h) * D;
-    // the block reduction needs every thread; an invalid page only drops the store
-    __shared__ __align__(16) int8_t sink[2 * D];
-    rope_quant_block(src, valid, pos, half, cos_t, sin_t, smooth ? km : nullptr, ok ? dst : sink,
-                     k_bscale + (static_cast<size_t>(b) * num_blocks + blk) * Hkv + h, red);
-    if (ok && !v8) {
-      const uint4* vs = reinterpret_cast<const uint4*>(v + (static_cast<size_t>(t) * Hkv + h) * D +
-                                                       half * 64);
-      uint4* vd = reinterpret_cast<uint4*>(v_pool + (slot * Hkv + h) * D + half * 64);
+  size_t slot = 0;
+  bool ok = false;
+  if (valid && h0 < Hkv) {
+    const int page = pool_page(bt, bt_stride, b, pos, ps, num_pages, j == 0 ? err : nullptr);
+    ok = page >= 0;
+    slot = static_cast<size_t>(ok ? page : 0) * ps + (pos % ps);
+    if (ok && slots != nullptr && hg == 0 && j == 0) slots[t] = static_cast<int32_t>(slot);
+  }
+
+  const bool smooth = partial != nullptr, v8 = vmax != nullptr;
+  if ((smooth || v8) && h0 < Hkv) {
+    // pass 2 of K smoothing (the sequence's mean from the exact block sums)
+    // and of FP8 V (the channel's absmax over the sequence -> scale / 448)
+    const int nsum = min(nblk, nblk_launch);
+    for (int idx = threadIdx.x; idx < nh * D; idx += kWrThreads) {
+      const int hh = idx / D, d = idx % D, h = h0 + hh;
+      if (h >= Hkv) continue;
+      const size_t o = (static_cast<size_t>(b) * Hkv + h) * D + d;
+      if (smooth) {
+        long long sum = 0;
+        for (int jb = 0; jb < nsum; ++jb)
+          sum += partial[((static_cast<size_t>(b) * num_blocks + jb) * Hkv + h) * D + d];
+        const float m = __double2float_rn(
+            __ll2double_rn(sum) / (static_cast<double>(L) * static_cast<double>(kMeanOne)));
+        km[hh][d] = m;
+        if (blk == 0) k_mean[o] = m;
+      }
+      if (v8) {
+        float amax = 0.f;
+        for (int jb = 0; jb < nsum; ++jb)
+          amax = fmaxf(amax, vmax[((static_cast<size_t>(b) * num_blocks + jb) * Hkv + h) * D + d]);
+        const float sc = __fdiv_rn(amax, 448.0f);
+        vsc[hh][d] = sc;
+        if (blk == 0) v_cscale[o] = sc;
+      }
+    }
+    __syncthreads();
+  }
+
+  for (int hh = 0; hh < nh; ++hh) {
+    fetch(hh + 1);
+    cp_async_wait_group<1>();   // this head's group has landed
+    const int s = hh & 1, h = h0 + hh;
+    const bool has_q = h < Hq, has_k = h < Hkv;   // the same for the whole CTA
+    const float* kmh = smooth && valid ? km[hh] : nullptr;   // this head's K mean
+    float y[16];
+    uint32_t mq = 0u, mk = 0u;
+    if (has_q) mq = rope_row(ring16(s, 0, 0), ring16(s, 0, 1), cs, sn, nullptr, j, y);
+    if (has_k) mk = rope_row(ring16(s, 1, 0), ring16(s, 1, 1), cs, sn, kmh, j, y);
+    mq = __reduce_max_sync(0xffffffffu, mq);
+    mk = __reduce_max_sync(0xffffffffu, mk);
+    if (lane == 0) red[hh & 1][warp] = make_uint2(mq, mk);
+    __syncthreads();
+    const uint2 m = red[hh & 1][lane];
+    mq = __reduce_max_sync(0xffffffffu, m.x);
+    mk = __reduce_max_sync(0xffffffffu, m.y);
+    const size_t sb = static_cast<size_t>(b) * num_blocks + blk;
+    if (has_q) {
+      rope_row(ring16(s, 0, 0), ring16(s, 0, 1), cs, sn, nullptr, j, y);
+      int8_t* dst = valid ? q_out + (t * Hq + h) * D + 8 * j : nullptr;
+      const float sc = quant_row(y, __uint_as_float(mq), dst);
+      if (threadIdx.x == 0) q_bscale[sb * Hq + h] = sc;
+    }
+    if (has_k) {
+      rope_row(ring16(s, 1, 0), ring16(s, 1, 1), cs, sn, kmh, j, y);
+      int8_t* dst = ok ? k_pool + (slot * Hkv + h) * D + 8 * j : nullptr;
+      const float sc = quant_row(y, __uint_as_float(mk), dst);
+      if (threadIdx.x == 0) k_bscale[sb * Hkv + h] = sc;
+      if (ok && !v8) {
+        uint4* vd = reinterpret_cast<uint4*>(v_pool + (slot * Hkv + h) * D + 8 * j);
+        vd[0] = ring16(s, 2, 0);
+        vd[8] = ring16(s, 2, 1);   // elements 64 + 8j
+      } else if (ok) {
+        // E4M3 codes of v / channel scale (float32 division); one byte per element
+        uint8_t* vd = reinterpret_cast<uint8_t*>(v_pool) + (slot * Hkv + h) * D + 8 * j;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) vd[c] = vs[c];
-    } else if (ok) {
-      // E4M3 codes of v / channel scale (float32 division), this thread's 64
-      // channels; the pool holds one byte per element
-      const uint16_t* vs = v + (static_cast<size_t>(t) * Hkv + h) * D + half * 64;
-      uint8_t* vd = reinterpret_cast<uint8_t*>(v_pool) + (slot * Hkv + h) * D + half * 64;
+        for (int g = 0; g < 2; ++g) {
+          float x[8];
+          unpack_bf16x8(ring16(s, 2, g), x);
+          uint32_t w[2] = {0u, 0u};
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float xa[8], xb[8];
-        load_bf16x8(vs + 16 * g, xa);
-        load_bf16x8(vs + 16 * g + 8, xb);
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint32_t word = 0;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int c = 16 * g + 4 * e + k;
-            const float sc = vsc[half * 64 + c];
-            const float xv = 4 * e + k < 8 ? xa[4 * e + k] : xb[4 * e + k - 8];
-            const uint32_t code = sc != 0.f ? f32_to_e4m3(__fdiv_rn(xv, sc)) : 0u;
-            word |= code << (8 * k);
+          for (int e = 0; e < 8; ++e) {
+            const float sc = vsc[hh][64 * g + 8 * j + e];
+            const uint32_t code = sc != 0.f ? f32_to_e4m3(__fdiv_rn(x[e], sc)) : 0u;
+            w[e / 4] |= code << (8 * (e % 4));
           }
-          w[e] = word;
+          *reinterpret_cast<uint2*>(vd + 64 * g) = make_uint2(w[0], w[1]);
         }
-        *reinterpret_cast<uint4*>(vd + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }
@@ -608,7 +741,7 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
         vmax = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) +
                                         static_cast<size_t>(p.num_seqs) * p.num_blocks *
                                             p.num_heads_kv * 128 * sizeof(long long));
-        v_block_max_kernel<<<dim3(nblk, p.num_heads_kv, p.num_seqs), 128, 0, stream>>>(
+        v_block_max_kernel<<<dim3(nblk, p.num_heads_kv, p.num_seqs), 256, 0, stream>>>(
             p.num_heads_kv, p.num_blocks, p.cu_seqlens_q, static_cast<const uint16_t*>(p.v), vmax);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -622,10 +755,15 @@ cudaError_t launch_write_cache(const qpkv_write_params& p, cudaStream_t stream) 
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
       }
-      dim3 grid(nblk, hmax, p.num_seqs);
-      write_int8_block128_rope_kernel<<<grid, threads, 0, stream>>>(
+      // blocks outermost, so the heavier full blocks start first and the
+      // CTAs reading one block's cos / sin rows run together
+      const long ctas = static_cast<long>(nblk) * p.num_seqs * ((hmax + kWrHeads - 1) / kWrHeads);
+      cudaError_t e = cudaFuncSetAttribute(write_int8_block128_rope_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kWrSmem);
+      if (e != cudaSuccess) return e;
+      write_int8_block128_rope_kernel<<<static_cast<unsigned>(ctas), kWrThreads, kWrSmem, stream>>>(
           p.num_seqs, p.num_heads_q, p.num_heads_kv, p.page_size, p.num_pages, p.bt_stride,
-          p.num_blocks, p.cu_seqlens_q, p.block_table, static_cast<const uint16_t*>(p.q),
+          p.num_blocks, nblk, p.cu_seqlens_q, p.block_table, static_cast<const uint16_t*>(p.q),
           static_cast<const uint16_t*>(p.k), static_cast<const uint16_t*>(p.v), p.rope_cos,
           p.rope_sin, static_cast<int8_t*>(p.k_pool), static_cast<uint16_t*>(p.v_pool),
           p.k_block_scale, static_cast<int8_t*>(p.q_out), p.q_block_scale, p.slot_mapping,

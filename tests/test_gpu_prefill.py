@@ -277,7 +277,9 @@ def test_prefill_bad_page_sets_error_word(lib):
 def test_prefill_full_size_sampled(lib):
     """8 sequences, L ~ U{256..4096}, 32 heads, page 64: the GPU writes the
     cache and runs the prefill (the benchmark's launch); the oracle rebuilds
-    two sequences' caches from the same bf16 draws and checks sampled rows."""
+    two sequences' caches from the same bf16 draws, which must match the
+    written bytes and scales exactly (about 30M codes, so thousands sit near
+    a rounding boundary), and checks sampled attention rows."""
     wl = synth.varlen_prefill(0)
     lengths = wl.lengths
     cos, sin = orope.cos_sin_table(int(lengths.max()), 128, wl.theta)
@@ -300,6 +302,15 @@ def test_prefill_full_size_sampled(lib):
             wl.q[sl], wl.k[sl], wl.v[sl], np.array([L], np.int32), bt1, 64, cos, sin,
             (L + 127) // 128, np.zeros((npg, 64, H, 128), np.int8),
             np.zeros((npg, 64, H, 128), np.uint16))
+        rows_b = d["slots"][begin[b]:begin[b] + L].long()
+        got_k = d["k_pool"].reshape(-1, H, 128)[rows_b].cpu().numpy()
+        got_v = d["v_pool"].reshape(-1, H, 128)[rows_b].cpu().view(torch.int16).numpy()
+        assert np.array_equal(got_k, kp.reshape(-1, H, 128)[:L])
+        assert np.array_equal(got_v.view(np.uint16), vp.reshape(-1, H, 128)[:L])
+        assert np.array_equal(d["q8"][begin[b]:begin[b] + L].cpu().numpy(), q8)
+        nblk = (L + 127) // 128
+        assert np.array_equal(_u32(d["ks"][b, :nblk].cpu().numpy()), _u32(kscale[0, :nblk]))
+        assert np.array_equal(_u32(d["qs"][b, :nblk].cpu().numpy()), _u32(qscale[0, :nblk]))
         toks = sorted({0, 1, 127, 128, L // 2, L - 2, L - 1})
         rows = [(t, h) for t in toks for h in (0, 13, 31)]
         want_o, want_lse = oatt.paged_prefill_int8(q8, qscale, kp, kscale, vp, bt1,
