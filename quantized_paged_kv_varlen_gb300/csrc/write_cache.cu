@@ -312,23 +312,41 @@ __global__ void __launch_bounds__(256) k_block_sum_kernel(
   const int rp = threadIdx.x >> 3, j = threadIdx.x & 7;
   // tokens past the launched blocks or the RoPE tables are the write's to flag
   const int n = min(kBlk, min(L, max_pos) - blk * kBlk);
+  // all four rows' loads first (rows past the block read as zeros, which
+  // add nothing), then the arithmetic
+  constexpr int kRows = kBlk / 32;
+  uint4 raw[kRows][2];
+  float4 cv[kRows][2], sv[kRows][2];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int r = rp + 32 * i, pos = blk * kBlk + r;
+    raw[i][0] = raw[i][1] = make_uint4(0u, 0u, 0u, 0u);
+    cv[i][0] = cv[i][1] = sv[i][0] = sv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < n) {
+      const uint4* row = reinterpret_cast<const uint4*>(
+          k + (static_cast<size_t>(begin + pos) * Hkv + h) * 128 + 8 * j);
+      raw[i][0] = __ldcs(row);
+      raw[i][1] = __ldcs(row + 8);   // elements 64 + 8j
+      const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * 64 + 8 * j);
+      const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * 64 + 8 * j);
+      cv[i][0] = __ldg(cp);
+      cv[i][1] = __ldg(cp + 1);
+      sv[i][0] = __ldg(sp);
+      sv[i][1] = __ldg(sp + 1);
+    }
+  }
   long long acc[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) acc[e] = 0;
 #pragma unroll
-  for (int i = 0; i < kBlk / 32; ++i) {
-    const int r = rp + 32 * i;
-    if (r >= n) break;
-    const int pos = blk * kBlk + r;
-    const uint16_t* row = k + (static_cast<size_t>(begin + pos) * Hkv + h) * 128 + 8 * j;
+  for (int i = 0; i < kRows; ++i) {
     float a[8], c[8];
-    load_bf16x8(row, a);
-    load_bf16x8(row + 64, c);
-    const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * 64 + 8 * j);
-    const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * 64 + 8 * j);
-    const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
-    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    unpack_bf16x8(raw[i][0], a);
+    unpack_bf16x8(raw[i][1], c);
+    const float cs[8] = {cv[i][0].x, cv[i][0].y, cv[i][0].z, cv[i][0].w,
+                         cv[i][1].x, cv[i][1].y, cv[i][1].z, cv[i][1].w};
+    const float sn[8] = {sv[i][0].x, sv[i][0].y, sv[i][0].z, sv[i][0].w,
+                         sv[i][1].x, sv[i][1].y, sv[i][1].z, sv[i][1].w};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const float y1 = __fsub_rn(__fmul_rn(a[e], cs[e]), __fmul_rn(c[e], sn[e]));
@@ -364,17 +382,27 @@ __global__ void __launch_bounds__(256) v_block_max_kernel(
   if (blk * kBlk >= L) return;
   const int rp = threadIdx.x >> 3, j = threadIdx.x & 7;
   const int n = min(kBlk, L - blk * kBlk);
+  constexpr int kRows = kBlk / 32;
+  uint4 raw[kRows][2];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int r = rp + 32 * i;
+    raw[i][0] = raw[i][1] = make_uint4(0u, 0u, 0u, 0u);   // rows past the block: zeros
+    if (r < n) {
+      const uint4* row = reinterpret_cast<const uint4*>(
+          v + (static_cast<size_t>(begin + blk * kBlk + r) * Hkv + h) * 128 + 8 * j);
+      raw[i][0] = __ldcs(row);
+      raw[i][1] = __ldcs(row + 8);   // elements 64 + 8j
+    }
+  }
   float m[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) m[e] = 0.f;
 #pragma unroll
-  for (int i = 0; i < kBlk / 32; ++i) {
-    const int r = rp + 32 * i;
-    if (r >= n) break;
-    const uint16_t* row = v + (static_cast<size_t>(begin + blk * kBlk + r) * Hkv + h) * 128 + 8 * j;
+  for (int i = 0; i < kRows; ++i) {
     float a[8], c[8];
-    load_bf16x8(row, a);
-    load_bf16x8(row + 64, c);
+    unpack_bf16x8(raw[i][0], a);
+    unpack_bf16x8(raw[i][1], c);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       m[e] = fmaxf(m[e], fabsf(a[e]));
